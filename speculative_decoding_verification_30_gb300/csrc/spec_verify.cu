@@ -59,6 +59,7 @@ struct Params {
   int ept;                  // elements per thread (contiguous range)
   int bulk_ok;              // rows are 16-byte aligned: use bulk copies
   int nlev;                 // radix levels: 2 (bf16) or 4 (fp32)
+  uint32_t keymask;         // key bits that vary: 0xffff0000 for bf16 logits, all for fp32
   float fix_scale;          // 2^S
   int32_t* out_tokens;
   int32_t* out_n;
@@ -111,6 +112,15 @@ struct Work {
   unsigned long long bcast_u[4];
   double bcast_d[4];
 };
+
+// Order key restricted to the bits a logit of this dtype can set. For bf16 the
+// low 16 bits of okey() are all zeros (positive) or all ones (negative), so
+// they are dropped; the radix levels then build exactly these masked keys.
+__device__ __forceinline__ uint32_t mkey(float z, uint32_t mask) { return okey(z) & mask; }
+// Float value of a masked key (inverse of mkey on values of the dtype).
+__device__ __forceinline__ float mkey_to_float(uint32_t k, uint32_t mask) {
+  return key_to_float((k & 0x80000000u) ? k : (k | ~mask));
+}
 
 template <typename DT>
 __device__ __forceinline__ float ld_elem(const DT* d, int j) {
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
   uint32_t kth[2] = {KEY_ALL, KEY_ALL};
   if (!greedy && topk_on && kk <= NT) {
     for (int r = 0; r < nrows; ++r)
-      kth[r] = block_kth_largest(okey(best[r]), j1 > j0, kk, W.kthh[r], W.scan32, P.nlev);
+      kth[r] = block_kth_largest(mkey(best[r], P.keymask), j1 > j0, kk, W.kthh[r], W.scan32, P.nlev);
   }
   // block reductions (deterministic butterflies)
 #pragma unroll
@@ -530,7 +540,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     const int r = tid;
     const double tau_d = log((double)V / (1.0 - (double)topp)) + 0.05;
     const float zt = (float)((double)W.row[r].m - tau_d * (double)T);
-    W.row[r].tau = (zt > W.row[r].zmin && isfinite(zt)) ? okey(zt) : KEY_ALL;
+    W.row[r].tau = (zt > W.row[r].zmin && isfinite(zt)) ? mkey(zt, P.keymask) : KEY_ALL;
   }
   if (!topk_on && !topp_on && tid < 2) W.row[tid].tau = KEY_ALL;
   __syncthreads();
@@ -570,7 +580,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
         const uint32_t tau = W.row[r].tau;
         for (int j = j0; j < j1; ++j) {
           const float z = ld_elem<DT>(data[r], j);
-          const uint32_t key = okey(z);
+          const uint32_t key = mkey(z, P.keymask);
           bool in;
           if (stage == 0) {
             in = key >= tau;
@@ -660,7 +670,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     }
     // stage result
     for (int r = 0; r < nrows; ++r) {
-      const unsigned long long Et = to_fixed(weight(key_to_float(prefix[r]), sc[r]), fscale);
+      const unsigned long long Et = to_fixed(weight(mkey_to_float(prefix[r], P.keymask), sc[r]), fscale);
       if (stage == 0) {
         tk[r] = prefix[r];
         jk[r] = (unsigned int)kk - cabove[r];
@@ -688,7 +698,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     unsigned int cnt[2] = {0, 0};
     for (int r = 0; r < nrows; ++r)
       if (need_tie[r])
-        for (int j = j0; j < j1; ++j) cnt[r] += (okey(ld_elem<DT>(data[r], j)) == thr[r]);
+        for (int j = j0; j < j1; ++j) cnt[r] += (mkey(ld_elem<DT>(data[r], j), P.keymask) == thr[r]);
     unsigned int excl[2], tot[2];
     for (int r = 0; r < 2; ++r) excl[r] = block_excl_scan<unsigned int>(cnt[r], W.scan32, &tot[r]);
     const int buf = xbuf;
@@ -709,7 +719,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
       if (cnt[r] > 0 && target >= lo && target < lo + cnt[r]) {
         unsigned int seen = lo;
         for (int j = j0; j < j1; ++j)
-          if (okey(ld_elem<DT>(data[r], j)) == thr[r]) {
+          if (mkey(ld_elem<DT>(data[r], j), P.keymask) == thr[r]) {
             if (seen == target) {
               found[r] = v0 + j;
               break;
@@ -764,8 +774,9 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     }
   }
 
+  const uint32_t kmask = P.keymask;
   auto kept = [&](int r, float z, int id) -> bool {
-    const uint32_t key = okey(z);
+    const uint32_t key = mkey(z, kmask);
     return key > thr[r] || (key == thr[r] && id <= tie[r]);
   };
 
@@ -945,6 +956,7 @@ static void fill_geometry(Params& p, int V, sv_dtype dt, Geometry* g) {
   p.slice = g->slice;
   p.ept = g->ept;
   p.nlev = dt == SV_BF16 ? 2 : 4;
+  p.keymask = dt == SV_BF16 ? 0xFFFF0000u : 0xFFFFFFFFu;
   p.fix_scale = ldexpf(1.0f, fix_scale_shift(V));
 }
 

@@ -62,7 +62,10 @@ def _probs_case(rows, T, k, P):
         if t.topp_margin < 1e-6:
             cut_boundary += 1
             continue
-        assert set(np.nonzero(got[r])[0]) == set(t.kept.tolist()), r
+        # weights below 2^-S of the maximum are zero in the kernel's fixed point
+        kept = set(t.kept.tolist())
+        assert set(np.nonzero(got[r])[0]) <= kept, r
+        assert set(np.nonzero(t.probs > 1e-12)[0]) <= set(np.nonzero(got[r])[0]), r
         worst = max(worst, float(np.max(np.abs(got[r] - t.probs))))
     return worst, cut_boundary
 
@@ -162,7 +165,8 @@ def test_identical_draft_rows_are_always_accepted():
     out, n = _run(b, dtok, 5, 5)
     # a drafted token outside the kept set has p = q = 0 and is rejected: compare to the oracle
     res = oracle_verify(b.target, b.draft, dtok, b.temperature, b.top_k, b.top_p, 5, 5)
-    assert compare(out, n, res, b.temperature).mismatches == 0
+    rep = compare(out, n, res, b.temperature)
+    assert rep.mismatches == 0, [(m[0], m[1], m[2], m[3], m[4]) for m in rep.bad_mismatches]
     kept_all = [all(res[s][0][i] == int(dtok[s, i]) for i in range(w.K)) for s in range(16)]
     assert sum(kept_all) >= 4
     for s in range(16):
