@@ -43,6 +43,19 @@
 
 namespace sv {
 
+// Phase timestamps for profiling builds (-DSV_TRACE): CTA rank 0, thread 0 of
+// the first 256 units records %globaltimer at each marker. Compiled out otherwise.
+#ifdef SV_TRACE
+__device__ unsigned long long g_trace[256 * 16];
+#define SV_MARK(k)                                                              \
+  do {                                                                         \
+    if (threadIdx.x == 0 && cluster_rank() == 0 && unit < 256)                 \
+      g_trace[unit * 16 + (k)] = global_timer_ns();                            \
+  } while (0)
+#else
+#define SV_MARK(k) ((void)0)
+#endif
+
 enum Mode { MODE_VERIFY = 0, MODE_PROBS = 1, MODE_SAMPLE = 2 };
 
 struct Params {
@@ -359,6 +372,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     }
   }
 
+  SV_MARK(0);
   const int v0 = (int)rank * P.slice;
   const int n = max(0, min(V, v0 + P.slice) - v0);
 
@@ -393,6 +407,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     __syncthreads();
   }
 
+  SV_MARK(1);
   const int j0 = tid * P.ept;
   const int j1 = min(n, j0 + P.ept);
 
@@ -471,7 +486,9 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     }
   }
   __syncthreads();
+  SV_MARK(2);
   cluster_sync();  // X1
+  SV_MARK(3);
   if (tid < 2) {
     const int r = tid;
     float bb = -INFINITY, zz = INFINITY;
@@ -566,8 +583,22 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     unsigned long long mabove[2] = {0, 0};
     double need_m[2] = {0, 0};
     unsigned int lastcnt[2] = {0, 0};
-    for (int lev = 0; lev < P.nlev; ++lev) {
-      const int shift = 24 - 8 * lev;
+    // Top-p over the whole row: a first level of 256 linear bins in
+    // temperature-scaled distance from the maximum, d = (m - z)/T in
+    // [0, ln(V/(1-top_p))], spreads flat rows over many bins (key bytes would
+    // put them in a handful). Later levels refine exact keys inside the bin.
+    const bool use_dbin = (stage == 1 && !topk_on);
+    const float dscale =
+        use_dbin ? (float)(256.0 / (log((double)V / (1.0 - (double)topp)) + 0.05)) : 0.f;
+    int dsel[2] = {-1, -1};
+    auto dbin = [&](float z, int r) -> int {
+      const float d = (sc[r].m - z) * sc[r].inv_hi;
+      return min(255, (int)(d * dscale));
+    };
+    const int nl = P.nlev + (use_dbin ? 1 : 0);
+    for (int lev = 0; lev < nl; ++lev) {
+      const bool dlev = use_dbin && lev == 0;
+      const int shift = 24 - 8 * (lev - (use_dbin ? 1 : 0));
       const int buf = xbuf;
       xbuf ^= 1;
       for (int t = tid; t < 2 * 256; t += NT) {
@@ -590,8 +621,9 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
             in = key >= tau;
             if (!in && lev == 0) zfar_t[r] += weight_fast(z, sc[r]);
           }
+          if (in && use_dbin && !dlev) in = dbin(z, r) == dsel[r];
           if (in && (key & pmask) == prefix[r]) {
-            const unsigned int dg = (key >> shift) & 255u;
+            const unsigned int dg = dlev ? 255u - (unsigned int)dbin(z, r) : (key >> shift) & 255u;
             atomicAdd(&W.hcnt[buf][r][dg], 1u);
             const unsigned long long E = to_fixed(weight(z, sc[r]), fscale);
             if (E) atomicAdd(&W.hmass[buf][r][dg], E);
@@ -614,7 +646,9 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
         }
       }
       __syncthreads();
+      SV_MARK(10 + 2 * stage);
       cluster_sync();
+      SV_MARK(11 + 2 * stage);
       // cluster-wide histogram: thread t -> row t>>8, digit t&255
       {
         const int r = tid >> 8, dg = tid & 255;
@@ -660,12 +694,15 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
       }
       __syncthreads();
       for (int r = 0; r < nrows; ++r) {
-        prefix[r] |= (uint32_t)W.bcast_i[r] << shift;
+        if (dlev)
+          dsel[r] = 255 - W.bcast_i[r];
+        else
+          prefix[r] |= (uint32_t)W.bcast_i[r] << shift;
         cabove[r] += (unsigned int)W.bcast_i[2 + r];
         mabove[r] += W.bcast_u[r];
         lastcnt[r] = (unsigned int)W.bcast_i[4 + r];
       }
-      pmask |= 255u << shift;
+      if (!dlev) pmask |= 255u << shift;
       __syncthreads();
     }
     // stage result
@@ -692,6 +729,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     }
   }
 
+  SV_MARK(4);
   // ---------------------------------------------------- tie split by token id
   for (int r = 0; r < nrows; ++r) need_tie[r] = any_sel && jt[r] < neq_all[r];
   if (need_tie[0] || need_tie[1]) {
@@ -751,6 +789,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
   int tie[2] = {W.row[0].tie, W.row[1].tie};
   for (int r = 0; r < 2; ++r) thr[r] = W.row[r].thr;
 
+  SV_MARK(5);
   // -------------------------------------- full support: exact normaliser
   const bool need_norm = !any_sel && (MODE == MODE_PROBS || (MODE == MODE_VERIFY && i < P.K));
   if (need_norm) {
@@ -794,6 +833,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     return;
   }
 
+  SV_MARK(6);
   // ------------------------------------------------------------ acceptance
   bool flag = false;
   if (MODE == MODE_VERIFY && i < P.K) {
@@ -811,6 +851,7 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     flag = (double)ku * 5.9604644775390625e-08 * pq[1] < pq[0];
   }
 
+  SV_MARK(7);
   // ------------------------------------------- inverse-CDF in token-id order
   uint32_t ku, kv;
   philox_uniform_bits(P.seed, P.offset, (uint32_t)b, (uint32_t)i, &ku, &kv);
@@ -823,8 +864,9 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     const float ep = weight(z, sc[0]);
     if (!res) return to_fixed(ep, fscale);
     const float zq = ld_elem<DT>(data[1], j);
-    const float q = kept(1, zq, v0 + j) ? weight(zq, sc[1]) * sq : 0.0f;
-    const float d = ep * sp - q;
+    // rounded products and difference (no FMA contraction): identical rows give d == 0
+    const float q = kept(1, zq, v0 + j) ? __fmul_rn(weight(zq, sc[1]), sq) : 0.0f;
+    const float d = __fsub_rn(__fmul_rn(ep, sp), q);
     return d > 0.0f ? __float2ull_rz(d * 4611686018427387904.0f) : 0ull;
   };
   bool use_res = residual;
@@ -869,7 +911,9 @@ __global__ void __launch_bounds__(NT, 1) sv_kernel(const Params P) {
     }
     break;
   }
+  SV_MARK(8);
   cluster_sync();   // keep this CTA's shared memory alive until every peer is done
+  SV_MARK(9);
 }
 
 __global__ void philox_kernel(uint64_t seed, uint64_t offset, int B, int K1, uint32_t* out) {
@@ -1105,5 +1149,11 @@ const char* sv_status_string(sv_status status) {
 }
 
 int sv_version(void) { return 100; }
+
+#ifdef SV_TRACE
+int sv_trace_copy(unsigned long long* host, size_t n) {
+  return (int)cudaMemcpyFromSymbol(host, sv::g_trace, n * sizeof(unsigned long long));
+}
+#endif
 
 }  // extern "C"
