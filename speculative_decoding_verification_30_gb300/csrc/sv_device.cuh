@@ -11,7 +11,7 @@
 
 namespace sv {
 
-constexpr int NT = 512;             // threads per CTA
+constexpr int NT = 256;             // threads per CTA
 constexpr int NWARP = NT / 32;
 
 // ---------------------------------------------------------------- clusters
@@ -165,45 +165,70 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
 }
 
 // ---------------------------------------------------------------- weights
-// Per-row constants of the temperature-scaled softmax.
-struct RowScale {
-  float m;        // row maximum (raw logit)
-  float inv_hi;   // 1/T split in two floats: inv_hi + inv_lo == 1/T to ~2^-48
-  float inv_lo;
-  float c2;       // log2(e)/T for the fast approximate weight
-};
-__device__ __forceinline__ RowScale make_scale(float m, float T) {
-  const double inv = 1.0 / (double)T;
-  RowScale s;
-  s.m = m;
-  s.inv_hi = (float)inv;
-  s.inv_lo = (float)(inv - (double)s.inv_hi);
-  s.c2 = (float)(1.4426950408889634 * inv);
-  return s;
-}
-// exp((z - m)/T) in fp32 with the argument carried to ~2^-48 relative error:
-// z - m as an exact two-term sum, times 1/T as a two-term product, then
-// exp(x_hi) * (1 + x_lo).
-__device__ __forceinline__ float weight(float z, const RowScale& s) {
-  if (z == -INFINITY) return 0.0f;
-  const float d = z - s.m;                       // TwoSum of z and -m
-  const float bb = d - z;
-  const float d_lo = (z - (d - bb)) + (-s.m - bb);
-  const float x = d * s.inv_hi;
-  const float x_lo = fmaf(d, s.inv_hi, -x) + fmaf(d, s.inv_lo, d_lo * s.inv_hi);
-  const float e = expf(x);
-  return fmaf(e, x_lo, e);
-}
-// Fast approximate weight for far-tail mass: 2^((z - m) * log2(e)/T).
-__device__ __forceinline__ float weight_fast(float z, const RowScale& s) {
-  float y = (z - s.m) * s.c2, r;
+__device__ __forceinline__ float ex2_approx(float y) {
+  float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
   return r;
 }
+
+// Per-row constants of the temperature-scaled softmax weights
+//   e(z) = exp((z - m)/T) = 2^((z - m) * log2(e)/T).
+// Tokens within `head` nats of the maximum (z >= zh) get the argument carried
+// to ~2^-48 relative error (z - m as an exact two-term sum, log2(e)/T as a
+// two-term product) and e = 2^y_hi * (1 + y_lo * ln 2), about 2.5e-7 relative
+// error overall. Tokens further out (each weighing less than e^-head of the
+// maximum) use 2^((z - m) * log2(e)/T) directly.
+struct RowW {
+  float m;       // row maximum (raw logit)
+  float c2;      // log2(e)/T, rounded
+  float c2_lo;   // log2(e)/T - c2
+  float zh;      // accurate-weight threshold
+  float invT;    // 1/T, rounded (distance bins)
+};
+
+__device__ __forceinline__ float hweight(float z, const RowW& w) {
+  const float dz = z - w.m;
+  if (z >= w.zh) {
+    const float bb = dz - z;
+    const float dz_lo = (z - (dz - bb)) + (-w.m - bb);
+    const float y = dz * w.c2;
+    const float y_lo = fmaf(dz, w.c2, -y) + fmaf(dz, w.c2_lo, dz_lo * w.c2);
+    const float e = ex2_approx(y);
+    return fmaf(e, y_lo * 0.69314718055994531f, e);
+  }
+  return ex2_approx(dz * w.c2);   // z = -inf gives 0
+}
+
 // Fixed-point weight: floor(e * 2^shift), e in [0, 1]. Integer sums of these are
 // exact and independent of summation order.
 __device__ __forceinline__ uint64_t to_fixed(float e, float scale_pow2) {
   return __float2ull_rz(e * scale_pow2);
+}
+
+// ------------------------------------------------------------ shared loads
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+// Logit j of a row slice whose shared-memory byte address is `base`.
+template <typename DT>
+__device__ __forceinline__ float lds_logit(uint32_t base, int j);
+template <>
+__device__ __forceinline__ float lds_logit<float>(uint32_t base, int j) {
+  return __uint_as_float(lds_u32(base + 4u * (uint32_t)j));
+}
+template <>
+__device__ __forceinline__ float lds_logit<__nv_bfloat16>(uint32_t base, int j) {
+  return __uint_as_float(((uint32_t)lds_u16(base + 2u * (uint32_t)j)) << 16);
+}
+__device__ __forceinline__ void st_peer_u64(void* p, uint32_t rank, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(peer_addr(p, rank)), "l"(v) : "memory");
 }
 
 // ---------------------------------------------------- block-level helpers
@@ -252,6 +277,23 @@ __device__ __forceinline__ bool mul_gt(uint64_t a, uint64_t b, uint64_t c, uint6
   const uint64_t ah = __umul64hi(a, b), al = a * b;
   const uint64_t ch = __umul64hi(c, d), cl = c * d;
   return ah > ch || (ah == ch && al > cl);
+}
+
+// Warp-aggregated append of index j to a shared list when pred holds; every
+// lane of the warp must call it. Entries beyond cap are counted but dropped.
+__device__ __forceinline__ void list_push(bool pred, uint16_t j, uint16_t* list, unsigned int* cnt,
+                                          unsigned int cap) {
+  const unsigned int mk = __ballot_sync(0xffffffffu, pred);
+  if (mk == 0u) return;
+  const int lane = lane_id();
+  const int leader = __ffs(mk) - 1;
+  unsigned int base = 0;
+  if (lane == leader) base = atomicAdd(cnt, (unsigned int)__popc(mk));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  if (pred) {
+    const unsigned int pos = base + (unsigned int)__popc(mk & ((1u << lane) - 1u));
+    if (pos < cap) list[pos] = j;
+  }
 }
 
 }  // namespace sv
