@@ -77,7 +77,8 @@ typedef enum {
   SV_ERR_DTYPE = 3,      /* unknown dtype */
   SV_ERR_WORKSPACE = 4,  /* workspace too small or misaligned */
   SV_ERR_CUDA = 5,       /* kernel launch or attribute call failed */
-  SV_ERR_ALIGN = 6       /* a pointer is not aligned to its element size */
+  SV_ERR_ALIGN = 6,      /* a pointer is not aligned to its element size */
+  SV_ERR_SCRATCH = 7     /* (B, K) needs more than spec_verify_noalloc's fixed scratch */
 } sv_status;
 
 /* Bytes of device workspace spec_verify needs for (B, K). The workspace must
@@ -107,6 +108,35 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
                       uint64_t philox_offset, int B, int K, int V, int32_t* out_tokens,
                       int32_t* out_n_accepted, void* workspace, size_t workspace_bytes,
                       void* stream /* cudaStream_t */);
+
+/* spec_verify without a caller workspace. Same arguments, semantics and results as
+ * spec_verify, minus the workspace: the workspace is a fixed array of
+ * SV_NOALLOC_SCRATCH_BYTES bytes in the library's own device memory (a file-scope
+ * __device__ array; one copy per device). The pages describe no such variant: it
+ * exists for callers that cannot allocate device memory around the step, such as
+ * plain C hosts without a device allocator, or runtimes that keep a fixed memory
+ * budget and allow no allocation while a decode step runs.
+ *   - Nothing is allocated: no cudaMalloc/cudaFree and no allocating library call.
+ *   - Limit: spec_verify_workspace_bytes(B, K) must not exceed
+ *     SV_NOALLOC_SCRATCH_BYTES; larger batches return SV_ERR_SCRATCH and launch
+ *     nothing (use spec_verify with a workspace).
+ *   - The scratch is zero when the library loads, and each call leaves it zero
+ *     again; a call must run to completion before the next one starts.
+ *   - The first call on a device looks up the scratch's device address with that
+ *     device current (cudaGetSymbolAddress, which may load the module); make that
+ *     first call outside any stream capture. Later calls reuse the cached address.
+ *   - All calls on one device share the one scratch: two calls that may overlap
+ *     (different streams, or host threads without ordering) race and corrupt each
+ *     other's results. Order them on one stream or synchronise between them.
+ * Returns the status spec_verify returns, or SV_ERR_SHAPE / SV_ERR_SCRATCH /
+ * SV_ERR_CUDA (address lookup failed) before launching. */
+#define SV_NOALLOC_SCRATCH_BYTES (1u << 20)
+sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                              sv_dtype dtype, const int32_t* draft_tokens,
+                              const float* temperature, const int32_t* top_k,
+                              const float* top_p, uint64_t philox_seed, uint64_t philox_offset,
+                              int B, int K, int V, int32_t* out_tokens, int32_t* out_n_accepted,
+                              void* stream /* cudaStream_t */);
 
 /* The truncated distribution of R independent rows, through the same device
  * code as spec_verify (a test and inspection hook).

@@ -15,12 +15,14 @@ import torch
 
 from ._build import LIB, build
 
-__all__ = ["load", "spec_verify", "spec_verify_workspace_bytes", "spec_truncated_probs",
+__all__ = ["load", "spec_verify", "spec_verify_noalloc", "spec_verify_workspace_bytes",
+           "spec_truncated_probs", "NOALLOC_SCRATCH_BYTES",
            "spec_sample", "spec_philox_uniforms", "sv_version", "Workspace", "SV_BF16", "SV_F32", "SpecVerifyError"]
 
 SV_BF16, SV_F32 = 0, 1
 _STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "workspace", 5: "cuda",
-           6: "alignment"}
+           6: "alignment", 7: "scratch"}
+NOALLOC_SCRATCH_BYTES = 1 << 20     # SV_NOALLOC_SCRATCH_BYTES in include/spec_verify.h
 _lib = None
 
 
@@ -43,6 +45,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify.argtypes = [vp, vp, i32, vp, vp, vp, vp, u64, u64, i32, i32, i32, vp, vp,
                                 vp, sz, vp]
     lib.spec_verify.restype = i32
+    lib.spec_verify_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, vp, u64, u64, i32, i32, i32, vp,
+                                        vp, vp]
+    lib.spec_verify_noalloc.restype = i32
     lib.spec_truncated_probs.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.spec_truncated_probs.restype = i32
     lib.spec_sample.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, u64, u64, vp, vp]
@@ -132,6 +137,35 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor | None, draft_tokens: 
         _dev(out_tokens, "out_tokens", torch.int32), _dev(out_n, "out_n", torch.int32),
         workspace.buf.data_ptr(), workspace.nbytes, _stream(stream))
     _check(st, "spec_verify")
+    return out_tokens, out_n
+
+
+def spec_verify_noalloc(target: torch.Tensor, draft: torch.Tensor | None,
+                        draft_tokens: torch.Tensor, temperature: torch.Tensor,
+                        top_k: torch.Tensor, top_p: torch.Tensor, seed: int, offset: int,
+                        out_tokens: torch.Tensor | None = None, out_n: torch.Tensor | None = None,
+                        stream=None):
+    """spec_verify with the library's fixed device scratch instead of a workspace.
+
+    Calls on one device must not overlap (they share the scratch); batches whose
+    workspace would exceed NOALLOC_SCRATCH_BYTES raise (status 7)."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    if out_n is None:
+        out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    if draft is not None and (draft.shape != (B, K, V) or draft.dtype != target.dtype):
+        raise SpecVerifyError("draft must be [B, K, V] with the target's dtype")
+    st = load().spec_verify_noalloc(
+        _dev(target, "target"), None if draft is None else _dev(draft, "draft"),
+        _dtype_code(target), _dev(draft_tokens, "draft_tokens", torch.int32),
+        _dev(temperature, "temperature", torch.float32), _dev(top_k, "top_k", torch.int32),
+        _dev(top_p, "top_p", torch.float32), seed & (2**64 - 1), offset & (2**64 - 1), B, K, V,
+        _dev(out_tokens, "out_tokens", torch.int32), _dev(out_n, "out_n", torch.int32),
+        _stream(stream))
+    _check(st, "spec_verify_noalloc")
     return out_tokens, out_n
 
 

@@ -1790,6 +1790,7 @@ const char* sv_status_string(sv_status status) {
     case SV_ERR_WORKSPACE: return "workspace too small or not 16-byte aligned";
     case SV_ERR_CUDA: return "CUDA launch or attribute call failed";
     case SV_ERR_ALIGN: return "pointer not aligned to its element size";
+    case SV_ERR_SCRATCH: return "batch needs more workspace than spec_verify_noalloc's fixed scratch";
   }
   return "unknown status";
 }

@@ -33,7 +33,7 @@ def test_library_builds_and_exports_every_declared_symbol():
 def test_version_and_status_strings():
     lib = sv.load()
     assert sv.sv_version() >= 100
-    for s in range(7):
+    for s in range(8):
         assert lib.sv_status_string(s)
 
 
@@ -67,3 +67,14 @@ def test_other_entry_points_validate_arguments():
     assert lib.spec_sample(1 << 12, 1, 1, 1, 1, 1 << 12, 1 << 12, 1 << 12, 0, 0, 1 << 12, None) == 2
     assert lib.spec_philox_uniforms(0, 0, 0, 1, 1 << 12, None) == 2
     assert lib.spec_philox_uniforms(0, 0, 1, 1, None, None) == 1
+
+
+def test_noalloc_entry_point_rejects_oversized_batches_before_any_cuda_call():
+    lib = sv.load()
+    args = lambda B, K: (1 << 12, 1 << 12, 0, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 0, 0, B, K,
+                         1024, 1 << 12, 1 << 12, None)
+    need = sv.spec_verify_workspace_bytes(65535, 16)
+    assert need > sv.NOALLOC_SCRATCH_BYTES
+    assert lib.spec_verify_noalloc(*args(65535, 16)) == 7
+    assert lib.spec_verify_noalloc(*args(0, 4)) == 2
+    assert lib.spec_verify_noalloc(*args(4, 17)) == 2
