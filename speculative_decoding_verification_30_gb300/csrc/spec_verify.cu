@@ -1,46 +1,45 @@
 // spec_verify.cu -- verify-and-sample kernels for GB300 (sm_103a) and the C ABI.
 //
-// Work decomposition. A "unit" is one (sequence b, position i) pair, i in
-// [0, K]: for i < K it owns target row i and draft row i, for i == K the
-// target row K (bonus position). One thread-block cluster of C CTAs serves one
-// unit; CTA c holds the vocabulary slice [c*slice, (c+1)*slice) of the unit's
-// rows in shared memory, loaded once from HBM by bulk copies (TMA engine).
-// Every later pass reads shared memory only; CTAs combine partial results
-// through distributed shared memory (DSMEM).
-//
 // Method (pages cited in include/spec_verify.h): temperature scaling, matched
-// top-k / top-p truncation of target and draft, acceptance with min(1, p/q) in
-// order, replacement from (p - q)+ or the bonus token from p_K, greedy
+// top-k / top-p truncation of target and draft rows, acceptance with min(1, p/q)
+// in order, replacement from (p - q)+ or the bonus token from p_K, and greedy
 // argmax-prefix matching at temperature 0.
 //
-// Passes per row of a sampling unit:
-//   A  row maximum (NaN/+inf check), argmax, per-thread maxima.       [X1]
-//   B  top-k rows: collect the tokens that can be in the top k (at or above
-//      the largest per-CTA k-th largest per-thread maximum: each CTA alone
-//      holds k tokens that large). No exponentials.
-//      top-p rows: weights e = exp((z - m)/T) once per token; exact mass of
-//      the head (tokens within 8 nats of the maximum, listed); private
-//      per-thread mass/count histograms of the tail in 1-nat distance bins
-//      (no shared-memory atomics: every thread owns its counters).     [X2]
-//   R  (top-p rows whose cut lies in the tail) refinement: the bin holding
-//      the cut is split into 16 sub-bins, touching only tokens inside it,
-//      until the range holding the cut is small enough to list.        [X3..]
-//   L  list the tokens of that range.
-//   S  the listed tokens of every CTA are pushed to CTA 0, which sorts them
-//      by (logit desc, id asc) and finds the cut exactly.          [push, res]
-//   then the probabilities of the draft token, and the inverse-CDF scan of
-//   (p - q)+ (or p) in token-id order across the cluster.              [CDF]
-// Rows where the lists would not fit take the general path: a distributed
-// radix selection over the whole slice (slower, same results).
+// Work decomposition. A "unit" is one (sequence b, position i): for i < K the
+// target row i and the draft row i (one row at temperature 0), for i == K the
+// target row K. A persistent thread-block cluster of C CTAs walks a strided
+// share of the units; CTA r holds the vocabulary slice [r*slice, (r+1)*slice)
+// of a unit's rows in shared memory. Row slices arrive by bulk copies (the TMA
+// engine) into a ring of slots that is filled one or more units ahead, so the
+// next unit's rows stream in while the current one is computed. Every logit
+// leaves HBM once; CTAs combine partial results through distributed shared
+// memory (DSMEM) at a few cluster barriers per unit.
 //
-// Sums: weights are converted to fixed point floor(e * 2^S), S = 63 -
-// ceil(log2 V); histogram masses and the normaliser are integer sums of
-// per-thread partial sums. The inverse-CDF decision C_j * 2^24 > k_v * S is
-// taken exactly on 64-bit integers.
-
+// Per sampling row:
+//   A  the slice maximum (packed bf16x2 max; NaN/+inf detection).
+//   B  weights e = 2^(z*c - R), c = log2(e)/T, in a CTA-local frame R (an even
+//      integer >= the slice maximum * c), summed per thread into 16 bins of two
+//      binades of e each (bin = the exponent of e, no atomics), then reduced to
+//      exact 64-bit fixed-point bin masses. Frames differ between CTAs by a
+//      whole number of bins, so the cluster merges bins by shifting.
+//      Top-k rows (k <= 256) instead list the tokens at or above the CTA's
+//      k-th largest per-thread maximum (each CTA alone holds k tokens that
+//      large, so the listed tokens contain the top k).
+//   S1 cluster exchange: maxima, frames, bins or list sizes.
+//   the bin holding the top-p cut is refined over logit keys (256 sub-bins per
+//      level, one level for bf16 in practice) until one logit value remains;
+//      its run of equal logits is split by token id.                    [S2..]
+//   D  acceptance in the CTA that owns the drafted token; the residual
+//      (p - q)+ or bonus p summed in token-id order per thread.          [S3]
+//      The CTA holding the crossing of v * total finds the token.
+//
+// Sums that decide a token (normaliser, cut, inverse CDF) are exact integer
+// sums of fixed-point weights, independent of summation order; identical target
+// and draft rows give identical p and q.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -49,304 +48,979 @@
 
 namespace sv {
 
-// Phase timestamps for profiling builds (-DSV_TRACE): CTA rank 0, thread 0 of
-// the first 256 units records %globaltimer at each marker. Compiled out otherwise.
-#ifdef SV_TRACE
-__device__ unsigned long long g_trace[256 * 16];
-#define SV_MARK(k)                                                              \
-  do {                                                                         \
-    if (threadIdx.x == 0 && cluster_rank() == 0 && unit < 256)                 \
-      g_trace[unit * 16 + (k)] = global_timer_ns();                            \
-  } while (0)
-#else
-#define SV_MARK(k) ((void)0)
-#endif
+enum { MODE_VERIFY = 0, MODE_PROBS = 1, MODE_SAMPLE = 2 };
 
-enum Mode { MODE_VERIFY = 0, MODE_PROBS = 1, MODE_SAMPLE = 2 };
+constexpr int NB = 16;          // mass bins (two binades of the weight each)
+constexpr int NSUB = 256;       // sub-bins of one refinement level
+constexpr int LC = 512;         // listed top-k candidates per CTA and row
+constexpr int GCAP = 1024;      // gathered top-k candidates per row
+constexpr int KFAST = 256;      // largest top_k served by the candidate lists
+constexpr int MAXLEV = 8;       // refinement levels before giving up (error)
+constexpr int MR = 32;          // unit metadata ring
+constexpr int NSMAX = 4;        // row slots
+constexpr int FIX = 44;         // fixed-point weights: floor(e * 2^44)
+
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+// X1 row flags
+constexpr uint32_t F_NAN = 1u, F_PINF = 2u, F_EXTREME = 4u, F_OVER = 8u;
 
 struct Params {
-  const void* rows0;        // VERIFY: target [B,K+1,V]; PROBS/SAMPLE: logits
-  const void* rows1;        // VERIFY: draft [B,K,V] (may be null)
-  const int32_t* dtok;      // [B,K]
+  const void* rows0;            // target [B][K+1][V] | probs rows [R][V] | draft [B][K][V]
+  const void* rows1;            // draft [B][K][V] (verify)
+  const int32_t* dtok;          // [B][K]
   const float* temp;
   const int32_t* topk;
   const float* topp;
   uint64_t seed, offset;
-  int B, K, V;
-  int nunits;
-  int slice;                // elements per CTA per row (multiple of 16)
-  int ept;                  // elements per thread (contiguous range)
-  int bulk_ok;              // rows are 16-byte aligned: use bulk copies
-  int nlev;                 // radix levels of the general path: 2 (bf16) or 4 (fp32)
-  uint32_t keymask;         // key bits that vary: 0xffff0000 for bf16 logits, all for fp32
-  float fix_scale;          // 2^S
-  int32_t* out_tokens;
+  int B, K, V, nunits;
+  int C, slice, ept, slot_elems, NS;
+  int bulk_ok;
+  int32_t* out_tokens;          // verify [B][K+1]; sample [B][K]
   int32_t* out_n;
   float* out_probs;
-  unsigned long long* ws_units;  // per unit: bit 0..31 token, bit 32 flag, bit 33 error
-  unsigned int* ws_tickets;      // per sequence
-  unsigned int* ws_error;        // sticky: bit 0 = a bulk copy did not complete in time
+  unsigned long long* ws_units; // per unit: bits 0..31 token, bit 32 flag, bit 33 error
+  unsigned int* ws_tickets;     // per sequence
+  unsigned int* ws_error;       // sticky: bit 0 = a bulk copy did not complete in time
 };
 
-constexpr uint32_t KEY_ALL = 0u;          // threshold that admits every token
-constexpr int NO_TIE = 0x7fffffff;        // tie id admitting the whole tie group
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
-constexpr float DHEAD = 8.0f;             // head: within 8 nats of the row maximum
-constexpr int NB = 16;                    // bins per histogram level
-constexpr int NBH = NB + 1;               // level 0 adds a bin for >= 16 nats beyond the head
-constexpr int LCAP = 512;                 // per-CTA list capacity (entries per row)
-constexpr int GCAP = 1024;                // entries per row gathered at the selecting CTA
-constexpr int MAXLEV = 5;                 // histogram levels before the general path
-
-enum RowMode { RM_FULL = 0, RM_TOPK = 1, RM_TOPP = 2 };
-enum Need { ND_DONE = 0, ND_REFINE = 1, ND_LIST = 2, ND_GENERAL = 3, ND_TIE = 4 };
-
-// Per-row state; identical in every CTA of the cluster after each exchange.
-struct RowK {
-  RowW w;
-  int argmax;
-  int bad;
-  int mode;
-  int kk;                      // k' (top-k count; V when off)
-  float topp;
-  uint32_t tau;                // top-k list admission: key >= tau
-  int lev;                     // level of the current range (-1: head / top-k list)
-  int q;                       // index of the current range at that level
-  int need;
-  int pad;
-  unsigned long long Z;        // total mass (top-p and full-support rows)
-  unsigned long long Zh;       // head mass (top-p rows)
-  unsigned long long above;    // mass strictly above the current range
-  double X;                    // top-p target mass (fixed-point units)
-  uint32_t thr;                // result: kept iff key > thr or (key == thr and id <= tie)
-  int tie;
-  unsigned long long ZL;       // result: kept mass
-  unsigned int jt;             // tie group: members to keep (ND_TIE)
-  unsigned int rc[16];         // per-CTA entries of the list being gathered
+struct Meta {
+  float T, P;
+  int k, d;
 };
 
-struct XA {                    // X1 payload per row
-  float best;
-  int best_id;
-  int bad;
-  uint32_t kth;
+// Exchanged through DSMEM after the first cluster barrier of a unit.
+struct X1Row {
+  float m;                // CTA maximum (raw logit), -inf when none is finite
+  uint32_t flags;         // F_*
+  float R;                // CTA frame
+  uint32_t ncand;         // listed top-k candidates
+  unsigned long long best;  // (okey(max) << 32) | ~argmax  (greedy)
+  unsigned long long bins[NB];
+  uint32_t cnts[NB];
+};
+struct X3 {
+  unsigned long long R, P;  // residual and target mass of this CTA (fixed 2^-40)
+  uint32_t flag;            // acceptance flag (owner CTA of the drafted token)
+  uint32_t pad;
+};
+// One refinement level of one row: counts and masses per sub-bin.
+struct X2Row {
+  uint32_t cnt[NSUB];
+  unsigned long long mass[NSUB];
 };
 
-struct XB {                    // pass-B / refinement payload per row
-  unsigned long long zh, zt;
-  unsigned int lcnt;
-  unsigned int kmin, kmax;     // key range of the tokens in the refined range
-  unsigned int pad;
-  unsigned long long hm[NBH];
-  unsigned int hc[NBH];
+enum { ST_DONE = 0, ST_KEYS = 1 };
+enum { T_MASS = 0, T_COUNT = 1 };
+enum { RM_ALL = 0, RM_TOPP = 1, RM_LIST = 2, RM_GENERAL = 3 };
+
+// Cluster-wide state of one row of the current unit (identical in every CTA
+// except the fields marked local).
+struct RowG {
+  float c;                // log2(e)/T (rounded)
+  float Rg;               // cluster frame
+  float mg;               // cluster maximum
+  float Rl;               // local: this CTA's frame
+  int sh;                 // local: Rg - Rl in binades (even, >= 0)
+  int extreme;            // weights 2^((z - mg) * c), one frame for all CTAs
+  int err;
+  int mode;               // RM_*
+  int stage;              // ST_*
+  int tkind;              // T_*
+  int then_mass;          // general path: mass target after the count target
+  int nlev;
+  float P;
+  int kk;                 // top-k size (k' <= V)
+  unsigned long long Y;   // mass target: kept iff exclusive mass <= Y
+  unsigned long long need;   // count target
+  unsigned long long above_m, above_c;
+  int ebin;
+  uint32_t klo, khi;
+  int kshift, nsub;
+  float zlo_f, zhi_f;
+  unsigned long long Z;   // mass of all tokens
+  // result
+  float zt;               // cut logit: kept iff z > zt, or z == zt and id <= idcut
+  int idcut;              // local: rule for this CTA's ties (INT_MAX all, -1 none)
+  int partial;            // local: this CTA must find idcut among its ties
+  uint32_t quota;         // local: ties this CTA keeps when partial
+  unsigned long long Zk;  // kept mass (fixed 2^-44)
+  float invZ;             // 2^44 / Zk
 };
 
-struct Work {
-  unsigned long long mbar;
-  unsigned long long pad0;
-  XA xa[2];
-  XB xb[2][2];                              // [buffer][row]
-  RowK rk[2];
-  unsigned long long xs[2][2];              // [buffer][slot] small exchanges
+struct Shared {
+  unsigned long long full[NSMAX];       // slot mbarriers
+  X1Row x1[2][2];                       // [exchange parity][row]
+  X3 x3;
+  RowG rg[2];
+  float Rc[2][16];                      // per-CTA frames (cluster copies)
+  uint32_t coff[2][17];                 // candidate offsets per CTA
+  unsigned long long gb[2][NB];         // merged bins
+  uint32_t gc[2][NB];
   unsigned long long scan64[NWARP];
-  unsigned int scan32[NWARP];
-  unsigned int lcnt[2];
-  unsigned int kthh[2][256];
-  int bi[8];
-  unsigned long long bu[4];
-  uint32_t res_thr[2];
-  int res_tie[2];
-  unsigned long long res_zl[2];
-  int res_fail[2];
-  uint16_t list[2][LCAP];
-  union {
-    struct {
-      float pmass[NBH][NT];                 // private per-thread histograms
-      uint8_t pcnt[NBH][NT];
-    } ph;
-    unsigned long long g[2][GCAP];          // gathered entries at the selecting CTA
-    struct {                                // general path
-      unsigned long long hmass[2][2][256];
-      unsigned int hcnt[2][2][256];
-      unsigned long long gmass[2][256];
-      unsigned int gcnt[2][256];
-    } gp;
-  } u;
+  unsigned long long scan64b[NWARP];
+  uint32_t scan32[NWARP];
+  float redf[NWARP];
+  uint32_t redu[NWARP];
+  uint32_t list_n[2];
+  int res_i[8];
+  unsigned long long res_u[8];
+  Meta meta[MR];
+  uint32_t timeout;
 };
 
-// Order key restricted to the bits a logit of this dtype can set. For bf16 the
-// low 16 bits of okey() are all zeros (positive) or all ones (negative), so
-// they are dropped; radix levels then build exactly these masked keys.
-__device__ __forceinline__ uint32_t mkey(float z, uint32_t mask) { return okey(z) & mask; }
-// Float value of a masked key (inverse of mkey on values of the dtype).
-__device__ __forceinline__ float mkey_to_float(uint32_t k, uint32_t mask) {
-  return key_to_float((k & 0x80000000u) ? k : (k | ~mask));
-}
+// Dynamic shared memory layout: [Shared][slots][H][G]
+//   H (union): per-thread bins float[NB][NT] + counts u8[NB][NT] | top-k lists
+//              u64[2][LC] | refinement exchange X2Row[2 parity][2 rows]
+//   G (union): per-CTA shifted bins for the merge | gathered candidates u64[GCAP]
+//              | per-thread sampling sums
+constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
+constexpr size_t H_BYTES = cmax(cmax(4 * sizeof(X2Row), (size_t)NB * NT * 5), 2 * LC * 8);
+constexpr size_t G_BYTES = cmax(cmax((size_t)GCAP * 8, (size_t)4 * NT * 8), (size_t)2 * 16 * NB * 12);
+constexpr size_t SHARED_BYTES = (sizeof(Shared) + 127) & ~(size_t)127;
 
+#ifdef SV_TRACE
+// Phase timestamps of the first 64 units of CTA 0 of cluster 0 (trace builds).
+__device__ unsigned long long g_trace[64 * 16 + 16];
+#define SV_MARK(k)                                                         \
+  do {                                                                     \
+    if (cid == 0 && rank == 0 && threadIdx.x == 0 && j < 64)               \
+      g_trace[j * 16 + (k)] = global_timer_ns();                           \
+  } while (0)
+#else
+#define SV_MARK(k) \
+  do {             \
+  } while (0)
+#endif
+
+// ------------------------------------------------------------ logit access
+// Logits of a slot; keys are 16-bit for bf16 (the logit's full bit pattern in
+// order) and 32-bit for fp32.
 template <typename DT>
-__device__ __forceinline__ float ld_peer_logit(uint32_t local_base, int j, uint32_t rank);
+struct Lg;
 template <>
-__device__ __forceinline__ float ld_peer_logit<float>(uint32_t local_base, int j, uint32_t rank) {
-  uint32_t a, v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_base + 4u * j), "r"(rank));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return __uint_as_float(v);
-}
+struct Lg<__nv_bfloat16> {
+  static constexpr int ES = 2;
+  __device__ static __forceinline__ float at(const void* s, int l) {
+    return __uint_as_float(lds_u16(smem_addr(s) + 2u * (uint32_t)l) << 16);
+  }
+  __device__ static __forceinline__ uint32_t key(float z) { return okey(z) >> 16; }
+  __device__ static __forceinline__ float key_float(uint32_t k) {
+    return key_to_float((k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu));
+  }
+};
 template <>
-__device__ __forceinline__ float ld_peer_logit<__nv_bfloat16>(uint32_t local_base, int j,
-                                                              uint32_t rank) {
-  uint32_t a;
-  uint16_t v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_base + 2u * j), "r"(rank));
-  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-  return __uint_as_float(((uint32_t)v) << 16);
+struct Lg<float> {
+  static constexpr int ES = 4;
+  __device__ static __forceinline__ float at(const void* s, int l) {
+    return __uint_as_float(lds_u32(smem_addr(s) + 4u * (uint32_t)l));
+  }
+  __device__ static __forceinline__ uint32_t key(float z) { return okey(z); }
+  __device__ static __forceinline__ float key_float(uint32_t k) { return key_to_float(k); }
+};
+
+// Calls f(z, l) for every logit of the slot in coalesced 16-byte vectors
+// (thread t takes vectors t, t + NT, ...; l is the index in the slice).
+template <typename DT, typename F>
+__device__ __forceinline__ void for_each_logit(const void* slot, int nvec, F&& f) {
+  const uint4* v = reinterpret_cast<const uint4*>(slot);
+  for (int q = threadIdx.x; q < nvec; q += NT) {
+    const uint4 w = v[q];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    if constexpr (sizeof(DT) == 2) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        f(__uint_as_float(ws[h] << 16), q * 8 + 2 * h);
+        f(__uint_as_float(ws[h] & 0xFFFF0000u), q * 8 + 2 * h + 1);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) f(__uint_as_float(ws[h]), q * 4 + h);
+    }
+  }
 }
 
-__device__ __forceinline__ float pow16(int l) {
-  return __int_as_float((127 + 4 * l) << 23);   // 16^l, exact
+// --------------------------------------------------------------- weights
+// Bin of a weight e in [0, 2): two binades per bin, the last bin takes the rest.
+__device__ __forceinline__ int wbin(float e) {
+  return 63 - (int)max(__float_as_uint(e) >> 24, (uint32_t)(64 - NB));
 }
-// Distance beyond the head in temperature-scaled nats, clamped at 0. Every
-// pass uses this same expression, so bin membership is consistent.
-__device__ __forceinline__ float tail_dist(float z, const RowW& w) {
-  return fmaxf(fmaf(w.m - z, w.invT, -DHEAD), 0.0f);
+// Weight in the CTA frame (normal rows): 2^(z*c - Rl).
+__device__ __forceinline__ float wloc(float z, float c, float negR) {
+  return ex2_approx(fmaf(z, c, negR));
+}
+// Weight of rows whose frames cannot be used (|max * c| too large): one frame
+// for the cluster, 2^((z - mg) * c).
+__device__ __forceinline__ float wext(float z, float mg, float c) {
+  return ex2_approx(z == mg ? 0.0f : (z - mg) * c);
+}
+// Weight of logit z in this CTA's frame (bulk weight).
+__device__ __forceinline__ float wbulk(float z, const RowG& g) {
+  return g.extreme ? wext(z, g.mg, g.c) : wloc(z, g.c, -g.Rl);
+}
+// Fixed-point weight in the cluster frame from a CTA-frame weight.
+__device__ __forceinline__ unsigned long long fixg(float e, int sh) {
+  return fix_pow2(e, FIX - sh);
+}
+// Bulk weight of logit z as CTA r computes it, in the cluster frame (fixed).
+__device__ __forceinline__ unsigned long long fix_of(float z, const RowG& g, float Rr) {
+  if (g.extreme) return fixg(wext(z, g.mg, g.c), 0);
+  if (!(Rr > -INFINITY)) return 0ull;           // CTA without finite logits
+  return fixg(wloc(z, g.c, -Rr), (int)(g.Rg - Rr));
+}
+// Weight used for probabilities, in the cluster frame: the product z*c is kept
+// exactly as a two-term sum and split into integer and fraction, so the
+// fraction keeps full precision. It uses the same c as the bulk weights (whose
+// sums normalise it), so numerator and normaliser agree to rounding.
+__device__ __forceinline__ float wacc(float z, const RowG& g) {
+  if (g.extreme) return wext(z, g.mg, g.c);
+  const float t = z * g.c;
+  if (!(t > -1.0e9f)) return 0.0f;               // -inf logit, or 2^(very negative)
+  const float tl = fmaf(z, g.c, -t);
+  const float n = rintf(t);
+  const float f = (t - n) + tl;
+  return ex2_approx(f) * pow2i((int)(n - g.Rg));
+}
+__device__ __forceinline__ unsigned long long fixr(float p) {
+  return fix_pow2(p, 40);
+}
+__device__ __forceinline__ bool kept(float z, int gid, float zt, int idcut) {
+  return z > zt || (z == zt && gid <= idcut);
 }
 
-// ------------------------------------------------------------------------
-// k-th largest of the CTA's per-thread maxima (block radix select on keys).
-// Returns KEY_ALL when fewer than k threads hold a token.
-__device__ uint32_t block_kth_largest(uint32_t key, bool valid, int k, unsigned int* hist,
-                                      unsigned int* scratch, int nlev) {
-  uint32_t prefix = 0, mask = 0;
-  int need = k;
-  for (int lev = 0; lev < nlev; ++lev) {
-    const int shift = 24 - 8 * lev;
-    for (int t = threadIdx.x; t < 256; t += NT) hist[t] = 0;
+// Exclusive-mass threshold of a top-p cut: a token is kept iff the mass before
+// it (fixed point) is <= Y, i.e. < P * Z exactly. P in (0, 1) is m * 2^-s with a
+// 24-bit integer m, so Y = floor((m * Z - 1) / 2^s) in 128-bit arithmetic.
+__device__ __forceinline__ unsigned long long mass_threshold(float P, unsigned long long Z) {
+  int e;
+  const float fr = frexpf(P, &e);                 // P = fr * 2^e, fr in [0.5, 1)
+  const unsigned long long m = (unsigned long long)(fr * 16777216.0f);
+  const int s = 24 - e;                           // >= 24
+  unsigned long long lo = m * Z, hi = __umul64hi(m, Z);
+  if (lo == 0ull && hi == 0ull) return 0ull;
+  if (lo == 0ull) --hi;
+  --lo;
+  if (s >= 128) return 0ull;
+  if (s >= 64) return hi >> (s - 64);
+  return (hi << (64 - s)) | (lo >> s);
+}
+
+// --------------------------------------------------------- block helpers
+__device__ __forceinline__ float block_max_nan(float v, float* red) {
+  v = warp_max_nan(v);
+  __syncthreads();
+  if (lane_id() == 0) red[warp_id()] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int i = 1; i < NWARP; ++i) r = fmax_nan(r, red[i]);
+  return r;
+}
+__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, uint32_t* red) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if (lane_id() == 0) red[warp_id()] = v;
+  __syncthreads();
+  uint32_t r = red[0];
+#pragma unroll
+  for (int i = 1; i < NWARP; ++i) r = min(r, red[i]);
+  return r;
+}
+
+// ------------------------------------------------------------------ passes
+// Per-thread maximum of a slot (NaN propagates).
+template <typename DT>
+__device__ __forceinline__ float thread_max(const void* slot, int nvec) {
+  const uint4* v = reinterpret_cast<const uint4*>(slot);
+  if constexpr (sizeof(DT) == 2) {
+    __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+    for (int q = threadIdx.x; q < nvec; q += NT) {
+      const uint4 w = v[q];
+      __nv_bfloat162 a, b, c, d;
+      memcpy(&a, &w.x, 4);
+      memcpy(&b, &w.y, 4);
+      memcpy(&c, &w.z, 4);
+      memcpy(&d, &w.w, 4);
+      m2 = __hmax2_nan(__hmax2_nan(m2, a), __hmax2_nan(__hmax2_nan(b, c), d));
+    }
+    return fmax_nan(__low2float(m2), __high2float(m2));
+  } else {
+    float m = -INFINITY;
+    for (int q = threadIdx.x; q < nvec; q += NT) {
+      const uint4 w = v[q];
+      m = fmax_nan(fmax_nan(m, __uint_as_float(w.x)),
+                   fmax_nan(__uint_as_float(w.y), fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w))));
+    }
+    return m;
+  }
+}
+
+// Lowest slice index holding the value m in this thread's vectors (UINT_MAX if none).
+template <typename DT>
+__device__ __forceinline__ uint32_t thread_first_index(const void* slot, int nvec, float m) {
+  const uint4* v = reinterpret_cast<const uint4*>(slot);
+  constexpr int PV = 16 / sizeof(DT);
+  for (int q = threadIdx.x; q < nvec; q += NT) {
+    const uint4 w = v[q];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      if constexpr (sizeof(DT) == 2) {
+        if (__uint_as_float(ws[h] << 16) == m) return (uint32_t)(q * PV + 2 * h);
+        if (__uint_as_float(ws[h] & 0xFFFF0000u) == m) return (uint32_t)(q * PV + 2 * h + 1);
+      } else {
+        if (__uint_as_float(ws[h]) == m) return (uint32_t)(q * PV + h);
+      }
+    }
+  }
+  return UINT_MAX;
+}
+
+// Pass B: per-thread bin masses (and counts) of the slot's weights, then the
+// CTA's fixed-point bin masses in the CTA frame, written to x.bins / x.cnts.
+template <typename DT, bool COUNTS>
+__device__ void pass_bins(const void* slot, int nvec, int vlen, const RowG& g, float* hist,
+                          uint8_t* hcnt, X1Row& x) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    hist[j * NT + tid] = 0.0f;
+    if (COUNTS) hcnt[j * NT + tid] = 0;
+  }
+  float* hb = hist + tid + 63 * NT;
+  uint8_t* cb = hcnt + tid + 63 * NT;
+  if (!g.extreme) {
+    const float c = g.c, negR = -g.Rl;
+    for_each_logit<DT>(slot, nvec, [&](float z, int l) {
+      const float e = wloc(z, c, negR);
+      const int o = -(int)max(__float_as_uint(e) >> 24, (uint32_t)(64 - NB)) * NT;
+      hb[o] += e;
+      if (COUNTS && l < vlen) cb[o] += 1;
+    });
+  } else {
+    const float c = g.c, mg = g.mg;
+    for_each_logit<DT>(slot, nvec, [&](float z, int l) {
+      const float e = wext(z, mg, c);
+      const int o = -(int)max(__float_as_uint(e) >> 24, (uint32_t)(64 - NB)) * NT;
+      hb[o] += e;
+      if (COUNTS && l < vlen) cb[o] += 1;
+    });
+  }
+  __syncthreads();
+  // warp w reduces bins 2w and 2w+1 (the per-thread counts of one bin stay <= 255:
+  // a thread holds at most ept logits of a row)
+  const int l = lane_id();
+  for (int j = 2 * warp_id(); j < 2 * warp_id() + 2; ++j) {
+    unsigned long long s = 0;
+    uint32_t n = 0;
+#pragma unroll
+    for (int k = 0; k < NT / 32; ++k) {
+      s += fix_pow2(hist[j * NT + l + 32 * k], FIX);
+      if (COUNTS) n += hcnt[j * NT + l + 32 * k];
+    }
+    s = warp_sum(s);
+    if (COUNTS) n = warp_sum(n);
+    if (l == 0) {
+      x.bins[j] = s;
+      x.cnts[j] = COUNTS ? n : 0u;
+    }
+  }
+}
+
+// Top-k rows: the 16-bit key prefix of the CTA's k-th largest per-thread maximum
+// (k <= NT), by two rounds of 256-bin counting over the thread maxima.
+__device__ uint32_t block_kth_prefix16(float tmax, int k, uint32_t* h, uint32_t* res) {
+  const int tid = threadIdx.x;
+  const uint32_t key = okey(tmax) >> 16;
+  uint32_t above = 0, prefix = 0;
+  for (int round = 0; round < 2; ++round) {
+    h[tid] = 0;
     __syncthreads();
-    if (valid && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    const bool in = round == 0 || (key >> 8) == prefix;
+    if (in) atomicAdd(&h[round == 0 ? (key >> 8) : (key & 0xFFu)], 1u);
     __syncthreads();
     if (warp_id() == 0) {
+      // lane l owns digits 255-8l-7 .. 255-8l (descending); find the digit where
+      // the count from the top reaches k - above
       const int l = lane_id();
-      unsigned int c[8], s = 0;
+      uint32_t c[8], s = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        c[q] = hist[255 - (8 * l + q)];
-        s += c[q];
+      for (int j = 0; j < 8; ++j) {
+        c[j] = h[255 - 8 * l - j];
+        s += c[j];
       }
-      unsigned int incl = s;
+      uint32_t incl = s;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        unsigned int t = __shfl_up_sync(0xffffffffu, incl, o);
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
         if (l >= o) incl += t;
       }
-      const unsigned int excl = incl - s;
-      const unsigned int total = __shfl_sync(0xffffffffu, incl, 31);
-      int digit = -1;
-      unsigned int above = 0;
-      if ((int)total >= need && (int)excl < need && (int)incl >= need) {
-        unsigned int run = excl;
+      uint32_t run = incl - s;
+      const uint32_t want = (uint32_t)k - above;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (digit < 0 && (int)(run + c[q]) >= need) {
-            digit = 255 - (8 * l + q);
-            above = run;
-          }
-          run += c[q];
+      for (int j = 0; j < 8; ++j) {
+        if (run < want && run + c[j] >= want) {
+          res[0] = (uint32_t)(255 - 8 * l - j);
+          res[1] = run;
         }
-      }
-      const unsigned int who = __ballot_sync(0xffffffffu, digit >= 0);
-      if (who == 0) {
-        if (l == 0) scratch[0] = 0xffffffffu;
-      } else {
-        const int src = __ffs(who) - 1;
-        digit = __shfl_sync(0xffffffffu, digit, src);
-        above = __shfl_sync(0xffffffffu, above, src);
-        if (l == 0) {
-          scratch[0] = (unsigned int)digit;
-          scratch[1] = above;
-        }
+        run += c[j];
       }
     }
     __syncthreads();
-    const unsigned int dg = scratch[0];
-    const unsigned int ab = scratch[1];
+    const uint32_t d = res[0];
+    above += res[1];
+    prefix = round == 0 ? d : ((prefix << 8) | d);
     __syncthreads();
-    if (dg == 0xffffffffu) return KEY_ALL;
-    prefix |= dg << shift;
-    mask |= 255u << shift;
-    need -= (int)ab;
   }
   return prefix;
 }
 
-// ------------------------------------------------------------------------
-// General path: digit where the cumulative (from the top) count or mass of a
-// cluster-wide 256-bin histogram first reaches the target (warp-level).
-struct DigitPick {
-  int digit;
-  unsigned int cnt_above;
-  unsigned long long mass_above;
-};
+// Top-k rows: lists (okey << 32 | ~id) of the slot's logits >= zt (cap LC).
+template <typename DT>
+__device__ void pass_list(const void* slot, int nvec, int vlen, float zt, int base,
+                          unsigned long long* list, uint32_t* count) {
+  for_each_logit<DT>(slot, nvec, [&](float z, int l) {
+    const bool pred = z >= zt && l < vlen;
+    const uint32_t mk = __ballot_sync(0xffffffffu, pred);
+    if (mk) {
+      const int lane = lane_id(), leader = __ffs(mk) - 1;
+      uint32_t pos = 0;
+      if (lane == leader) pos = atomicAdd(count, (uint32_t)__popc(mk));
+      pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(mk & ((1u << lane) - 1u));
+      if (pred && pos < (uint32_t)LC)
+        list[pos] = ((unsigned long long)okey(z) << 32) | (uint32_t)~(uint32_t)(base + l);
+    }
+  });
+}
 
-__device__ DigitPick pick_digit(const unsigned int* gcnt, const unsigned long long* gmass,
-                                bool by_mass, unsigned long long need_cnt, double need_mass) {
-  const int l = lane_id();
-  unsigned int c[8];
-  unsigned long long w[8];
-  unsigned long long sc = 0, sw = 0;
+// One refinement level: counts (and, when a sub-bin spans several keys,
+// fixed-point masses) of the slot's logits that lie in the row's key range and
+// whose weight falls in the cut bin. Single-key sub-bins (the usual bf16 case,
+// where long runs of equal logits make direct atomics contend) are first
+// listed as byte-sized sub-bin indices, then counted warp by warp: a warp sorts
+// 32 listed indices and adds each run with one atomic. Entries beyond the list
+// capacity are counted directly.
+template <typename DT>
+__device__ void pass_level(const void* slot, int nvec, int vlen, const RowG& gs, X2Row* x,
+                           uint8_t* list, uint32_t* list_n, int cap) {
+  // row constants in registers (the loop stores to shared memory, which would
+  // otherwise force reloads of the shared row state)
+  const float lo = gs.zlo_f, hi = gs.zhi_f, c = gs.c, negR = -gs.Rl, mg = gs.mg;
+  const bool extreme = gs.extreme != 0;
+  const int hsh = gs.sh >> 1, fsh = extreme ? 0 : gs.sh, ebin = gs.ebin, kshift = gs.kshift;
+  const uint32_t klo = gs.klo, nsub = (uint32_t)gs.nsub;
+  const bool listed = kshift == 0 && nsub <= 255u;
+  // per-warp list segment, fill count kept in a register (warp-uniform)
+  const uint32_t wcap = (uint32_t)cap / NWARP;
+  uint8_t* wl = list + (size_t)warp_id() * wcap;
+  uint32_t wn = 0;
+  (void)list_n;
+  for_each_logit<DT>(slot, nvec, [&](float z, int l) {
+    uint32_t sub = 0xFFFFFFFFu;
+    float e = 0.0f;
+    if (z >= lo && z <= hi && l < vlen) {
+      e = extreme ? wext(z, mg, c) : wloc(z, c, negR);
+      const int b = extreme ? wbin(e) : min(wbin(e) + hsh, NB - 1);
+      if (b == ebin) {
+        const uint32_t sb = (Lg<DT>::key(z) - klo) >> kshift;
+        if (sb < nsub) sub = sb;
+      }
+    }
+    const bool hit = sub != 0xFFFFFFFFu;
+    if (!listed) {
+      if (hit) {
+        atomicAdd(&x->cnt[sub], 1u);
+        if (kshift > 0) atomicAdd(&x->mass[sub], fixg(e, fsh));
+      }
+      return;
+    }
+    const uint32_t mk = __ballot_sync(0xffffffffu, hit);
+    if (hit) {
+      const uint32_t pos = wn + (uint32_t)__popc(mk & ((1u << lane_id()) - 1u));
+      if (pos < wcap) wl[pos] = (uint8_t)sub;
+      else atomicAdd(&x->cnt[sub], 1u);
+    }
+    wn += (uint32_t)__popc(mk);
+  });
+  if (!listed) return;
+  // each warp counts its own segment: sort 32 entries, one atomic per run
+  const uint32_t n = min(wn, wcap);
+  const int lane = lane_id();
+  for (uint32_t b0 = 0; b0 < n; b0 += 32) {
+    uint32_t v = b0 + lane < n ? wl[b0 + lane] : 0xFFu;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int dg = 255 - (8 * l + q);
-    c[q] = gcnt[dg];
-    w[q] = gmass[dg];
-    sc += c[q];
-    sw += w[q];
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int jj = k >> 1; jj > 0; jj >>= 1) {
+        const uint32_t o = __shfl_xor_sync(0xffffffffu, v, jj);
+        const bool up = ((lane & k) == 0) == ((lane & jj) == 0);
+        v = up ? min(v, o) : max(v, o);
+      }
+    }
+    const uint32_t prev = __shfl_up_sync(0xffffffffu, v, 1);
+    const bool start = lane == 0 || prev != v;
+    const uint32_t starts = __ballot_sync(0xffffffffu, start);
+    if (start && v != 0xFFu) {
+      const uint32_t later = starts & ~((2u << lane) - 1u);
+      const int next = later ? __ffs(later) - 1 : 32;
+      atomicAdd(&x->cnt[v], (uint32_t)(next - lane));
+    }
   }
-  unsigned long long ic = sc, iw = sw;
+}
+
+// -------------------------------------------------------- cluster merges
+// Warp 0 after an exchange barrier: cluster maximum, flags, frames and list
+// sizes of row `rho` (lanes 0..C-1 read CTA lane's X1).
+__device__ void merge_head(Shared& S, RowG& g, const X1Row* x1p, int rho, int C, uint32_t rank,
+                           bool* err, bool* extreme, bool* over, uint32_t* ncand_total) {
+  const int l = lane_id();
+  float m = -INFINITY, R = -INFINITY;
+  uint32_t fl = 0, nc = 0;
+  if (l < C) {
+    m = ld_peer_f32(&x1p->m, l);
+    fl = ld_peer_u32(&x1p->flags, l);
+    R = ld_peer_f32(&x1p->R, l);
+    nc = ld_peer_u32(&x1p->ncand, l);
+  }
+  float mg = warp_max_nan(m);
+  float Rg = R;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) Rg = fmaxf(Rg, __shfl_xor_sync(0xffffffffu, Rg, o));
+  uint32_t f = fl;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) f |= __shfl_xor_sync(0xffffffffu, f, o);
+  uint32_t incl = nc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    unsigned long long tc = __shfl_up_sync(0xffffffffu, ic, o);
-    unsigned long long tw = __shfl_up_sync(0xffffffffu, iw, o);
-    if (l >= o) {
-      ic += tc;
-      iw += tw;
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (l >= o) incl += t;
+  }
+  if (l < 16) {
+    S.Rc[rho][l] = R;
+    S.coff[rho][l + 1] = incl;
+  }
+  if (l == 0) S.coff[rho][0] = 0;
+  *err = isnan(mg) || (f & (F_NAN | F_PINF)) || !(mg > -INFINITY);
+  *extreme = (f & F_EXTREME) != 0;
+  *over = (f & F_OVER) != 0 || __shfl_sync(0xffffffffu, incl, 31) > (uint32_t)GCAP;
+  *ncand_total = __shfl_sync(0xffffffffu, incl, 31);
+  if (l == 0) {
+    g.mg = mg;
+    g.Rg = Rg;
+  }
+}
+
+// All threads: cluster bins (and counts) of row rho in the cluster frame.
+// Thread (r, j) shifts CTA r's bin j into cluster bin min(j + h_r, NB-1); the
+// half-warp of CTA r folds the bins that land in the last bin; then thread j
+// sums cluster bin j over the CTAs.
+__device__ void merge_bins(Shared& S, const X1Row* x1p, int rho, int C, bool extreme,
+                           unsigned long long* tmpb, uint32_t* tmpc) {
+  const int t = threadIdx.x, r = t >> 4, j = t & 15;
+  unsigned long long v = 0;
+  uint32_t n = 0;
+  int gj = j;
+  if (r < C) {
+    const float Rr = S.Rc[rho][r];
+    const bool live = extreme || Rr > -INFINITY;
+    const int sh = extreme ? 0 : (live ? (int)fminf(S.rg[rho].Rg - Rr, 4096.0f) : 4096);
+    const unsigned long long b = ld_peer_u64(&x1p->bins[j], r);
+    const uint32_t c = ld_peer_u32(&x1p->cnts[j], r);
+    if (live) {
+      v = sh >= 64 ? 0ull : (b >> sh);
+      n = c;
+      gj = min(j + (sh >> 1), NB - 1);
     }
   }
-  unsigned long long rc = ic - sc, rw = iw - sw;
-  int digit = -1;
-  unsigned long long ac = 0, aw = 0;
+  // fold the bins of this CTA that map to the last cluster bin (16-lane groups)
+  unsigned long long vl = gj == NB - 1 ? v : 0ull;
+  uint32_t nl = gj == NB - 1 ? n : 0u;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const unsigned long long nc = rc + c[q], nw = rw + w[q];
-    const bool hit = by_mass ? ((double)nw >= need_mass) : (nc >= need_cnt);
-    if (digit < 0 && hit) {
-      digit = 255 - (8 * l + q);
-      ac = rc;
-      aw = rw;
-    }
-    rc = nc;
-    rw = nw;
+  for (int o = 8; o; o >>= 1) {
+    vl += __shfl_xor_sync(0xffffffffu, vl, o);
+    nl += __shfl_xor_sync(0xffffffffu, nl, o);
   }
-  const unsigned int who = __ballot_sync(0xffffffffu, digit >= 0);
-  DigitPick p;
-  if (who == 0) {              // target beyond the total: take the smallest non-empty digit
-    const unsigned long long tc = __shfl_sync(0xffffffffu, ic, 31);
-    const unsigned long long tw = __shfl_sync(0xffffffffu, iw, 31);
-    int lowest = -1;
-    for (int dg = 0; dg < 256; ++dg)
-      if (gcnt[dg] != 0) {
-        lowest = dg;
+  tmpb[r * NB + j] = 0ull;
+  tmpc[r * NB + j] = 0u;
+  __syncthreads();
+  if (r < C) {
+    if (gj < NB - 1) {
+      tmpb[r * NB + gj] = v;
+      tmpc[r * NB + gj] = n;
+    } else if (j == NB - 1) {
+      tmpb[r * NB + NB - 1] = vl;
+      tmpc[r * NB + NB - 1] = nl;
+    }
+  }
+  __syncthreads();
+  if (t < NB) {
+    unsigned long long sum = 0;
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      sum += tmpb[q * NB + t];
+      cnt += tmpc[q * NB + t];
+    }
+    S.gb[rho][t] = sum;
+    S.gc[rho][t] = cnt;
+  }
+  __syncthreads();
+}
+
+// The weight bin a cut lies in, and the key range of that bin (thread 0).
+template <typename DT>
+__device__ void ebin_pick(Shared& S, RowG& g, int rho) {
+  unsigned long long cm = g.above_m, cc = g.above_c;
+  int j = 0;
+  for (; j < NB - 1; ++j) {
+    const bool stop = g.tkind == T_MASS ? (cm + S.gb[rho][j] > g.Y)
+                                        : (cc + S.gc[rho][j] >= g.need);
+    if (stop) break;
+    cm += S.gb[rho][j];
+    cc += S.gc[rho][j];
+  }
+  g.above_m = cm;
+  g.above_c = cc;
+  g.ebin = j;
+  // bin j holds y = z*c - Rg in [-2j-1, -2j+1) (extreme rows: y = (z - mg)*c)
+  const float ylo = -2.0f * j - 1.0f, yhi = -2.0f * j + 1.0f;
+  float zlo, zhi;
+  if (g.extreme) {
+    zlo = g.mg + ylo / g.c;
+    zhi = g.mg + yhi / g.c;
+  } else {
+    zlo = (g.Rg + ylo) / g.c;
+    zhi = (g.Rg + yhi) / g.c;
+  }
+  if (j == 0 || !(zhi == zhi)) zhi = INFINITY;
+  if (j == NB - 1 || !(zlo == zlo)) zlo = -INFINITY;
+  zlo = zlo - fabsf(zlo) * 1.52587890625e-05f - 1e-30f;   // widen by 2^-16 relative
+  zhi = zhi + fabsf(zhi) * 1.52587890625e-05f + 1e-30f;
+  g.zlo_f = zlo;
+  g.zhi_f = zhi;
+  g.klo = Lg<DT>::key(zlo);
+  g.khi = Lg<DT>::key(zhi);
+  const uint32_t span = g.khi - g.klo;
+  const int bits = span ? 32 - __clz(span) : 0;
+  g.kshift = max(0, bits - 8);
+  g.nsub = (int)(span >> g.kshift) + 1;
+  g.stage = ST_KEYS;
+}
+
+// After a refinement level: merge the sub-bins of row rho, pick the one holding
+// the cut; resolve the run of equal logits when a sub-bin is a single key.
+template <typename DT>
+__device__ void level_pick(Shared& S, RowG& g, int rho, const X2Row* xp, int C, uint32_t rank,
+                           unsigned char* Gr) {
+  const int t = threadIdx.x;
+  const int s = g.nsub - 1 - t;             // thread order = descending keys
+  unsigned long long mass = 0;
+  uint32_t cnt = 0;
+  uint32_t* pc = reinterpret_cast<uint32_t*>(Gr);          // [16] counts of the picked key
+  uint32_t nn[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) nn[r] = 0u;
+  if (s >= 0) {
+    unsigned long long mm[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r < C) {
+        nn[r] = ld_peer_u32(&xp->cnt[s], r);
+        mm[r] = ld_peer_u64(&xp->mass[s], r);
+      } else {
+        mm[r] = 0ull;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      cnt += nn[r];
+      mass += mm[r];
+    }
+  }
+  unsigned long long tm;
+  const unsigned long long em = block_excl_scan<unsigned long long>(mass, S.scan64, &tm);
+  uint32_t tc;
+  const uint32_t ec = block_excl_scan<uint32_t>(cnt, S.scan32, &tc);
+  if (t == 0) S.res_i[0] = -1;
+  __syncthreads();
+  if (s >= 0) {
+    bool hit;
+    if (g.tkind == T_MASS) hit = g.above_m + em <= g.Y && g.above_m + em + mass > g.Y;
+    else hit = g.above_c + ec < g.need && g.above_c + ec + cnt >= g.need;
+    if (hit) {
+      S.res_i[0] = s;
+      S.res_u[0] = em;
+      S.res_u[1] = ec;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) pc[r] = nn[r];
+    }
+  }
+  __syncthreads();
+  const int sp = S.res_i[0];
+  if (sp >= 0 && g.kshift == 0 && warp_id() == 0) {
+    // one logit value: split its run of equal logits by token id, CTA by CTA
+    // (lane r handles CTA r's members, which follow CTAs 0..r-1 in id order)
+    const int l = lane_id();
+    const float zk = Lg<DT>::key_float(g.klo + (uint32_t)sp);
+    const uint32_t n = l < C ? pc[l] : 0u;
+    const unsigned long long E = l < C ? fix_of(zk, g, S.Rc[rho][l]) : 0ull;
+    unsigned long long bm = (unsigned long long)n * E;
+    unsigned long long bc = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long a = __shfl_up_sync(0xffffffffu, bm, o);
+      const unsigned long long c2 = __shfl_up_sync(0xffffffffu, bc, o);
+      if (l >= o) {
+        bm += a;
+        bc += c2;
+      }
+    }
+    const unsigned long long A = g.above_m + S.res_u[0] + bm - (unsigned long long)n * E;
+    const unsigned long long before = g.above_c + S.res_u[1] + bc - n;
+    uint32_t take;
+    if (g.tkind == T_MASS) {
+      if (A > g.Y) take = 0;
+      else if (E == 0) take = n;
+      else {
+        const unsigned long long q = (g.Y - A) / E + 1;
+        take = q < n ? (uint32_t)q : n;
+      }
+    } else {
+      take = g.need > before ? (uint32_t)min((unsigned long long)n, g.need - before) : 0u;
+    }
+    const unsigned long long kept_m =
+        g.above_m + S.res_u[0] + warp_sum<unsigned long long>((unsigned long long)take * E);
+    const uint32_t my_n = __shfl_sync(0xffffffffu, take, (int)rank);
+    const uint32_t my_cnt = __shfl_sync(0xffffffffu, n, (int)rank);
+    if (l == 0) {
+      g.zt = zk;
+      g.quota = my_n;
+      g.partial = (my_n > 0 && my_n < my_cnt) ? 1 : 0;
+      g.idcut = my_n == my_cnt ? INT_MAX : (my_n == 0 ? -1 : 0);
+      if (g.tkind == T_COUNT && g.then_mass) {
+        // top-k set found (its mass is kept_m); now the top-p cut inside it
+        g.Z = kept_m;
+        g.Y = mass_threshold(g.P, kept_m);
+        g.tkind = T_MASS;
+        g.then_mass = 0;
+        g.above_m = 0;
+        g.above_c = 0;
+        g.nlev = 0;
+        ebin_pick<DT>(S, g, rho);
+      } else {
+        g.Zk = kept_m;
+        g.stage = ST_DONE;
+      }
+    }
+  } else if (t == 0) {
+    if (sp < 0) {
+      g.err = 1;                            // no sub-bin holds the cut: inconsistent data
+      g.stage = ST_DONE;
+    } else if (g.kshift > 0) {
+      g.above_m += S.res_u[0];
+      g.above_c += S.res_u[1];
+      const uint32_t lo = g.klo + ((uint32_t)sp << g.kshift);
+      const uint32_t hi = min(g.khi, lo + ((1u << g.kshift) - 1u));
+      g.klo = lo;
+      g.khi = hi;
+      const uint32_t span = hi - lo;
+      const int bits = span ? 32 - __clz(span) : 0;
+      g.kshift = max(0, bits - 8);
+      g.nsub = (int)(span >> g.kshift) + 1;
+      g.zlo_f = Lg<DT>::key_float(lo);
+      g.zhi_f = Lg<DT>::key_float(hi);
+      if (++g.nlev > MAXLEV) {
+        g.err = 1;
+        g.stage = ST_DONE;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Sorts n composites (okey << 32 | ~id) in descending order (logit desc, id asc).
+// n <= NT: rank sort into out; otherwise bitonic in place (out = in).
+__device__ unsigned long long* sort_desc(unsigned long long* in, int n, unsigned long long* out) {
+  const int t = threadIdx.x;
+  if (n <= NT) {
+    if (t < n) {
+      const unsigned long long v = in[t];
+      int rk = 0;
+      for (int q = 0; q < n; ++q) rk += in[q] > v;
+      out[rk] = v;
+    }
+    __syncthreads();
+    return out;
+  }
+  int N = 2;
+  while (N < n) N <<= 1;
+  for (int p = n + t; p < N; p += NT) in[p] = 0ull;
+  __syncthreads();
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int p = t; p < N; p += NT) {
+        const int q = p ^ jj;
+        if (q > p) {
+          const unsigned long long a = in[p], c = in[q];
+          const bool desc = (p & k) == 0;
+          if (desc ? a < c : a > c) {
+            in[p] = c;
+            in[q] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  return in;
+}
+
+// Top-k rows: gather the listed candidates of every CTA, sort them, keep the
+// first k, then the top-p prefix of those. Sets zt / idcut (global id) / Zk.
+template <typename DT>
+__device__ void list_select(Shared& S, RowG& g, int rho, const unsigned long long* lists, int C,
+                            uint32_t n, int slice, unsigned long long* gbuf) {
+  const int t = threadIdx.x;
+  for (uint32_t idx = t; idx < n; idx += NT) {
+    int r = 0;
+    while (r + 1 < C && S.coff[rho][r + 1] <= idx) ++r;
+    gbuf[idx] = ld_peer_u64(&lists[rho * LC + (idx - S.coff[rho][r])], r);
+  }
+  __syncthreads();
+  unsigned long long* sorted = sort_desc(gbuf, (int)n, gbuf + 512);
+  const int kk = min(g.kk, (int)n);
+  unsigned long long E = 0;
+  unsigned long long comp = 0;
+  if (t < kk) {
+    comp = sorted[t];
+    const float z = key_to_float((uint32_t)(comp >> 32));
+    const int gid = (int)~(uint32_t)comp;
+    E = fix_of(z, g, S.Rc[rho][min(gid / slice, C - 1)]);
+  }
+  unsigned long long tot;
+  const unsigned long long ex = block_excl_scan<unsigned long long>(E, S.scan64, &tot);
+  unsigned long long Y = ~0ull;
+  if (g.P < 1.0f) Y = mass_threshold(g.P, tot);
+  const uint32_t keep = (t < kk && ex <= Y) ? 1u : 0u;
+  uint32_t nk;
+  block_excl_scan<uint32_t>(keep, S.scan32, &nk);
+  if (nk == 0) nk = 1;
+  if (t == (int)nk - 1) {
+    g.zt = key_to_float((uint32_t)(comp >> 32));
+    g.idcut = (int)~(uint32_t)comp;
+    g.Zk = ex + E;
+    g.Z = tot;
+    g.partial = 0;
+    g.stage = ST_DONE;
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------- phase D helpers
+// The partial CTA of a run of equal logits finds the id of its quota-th member
+// (token-id order): per-thread counts over contiguous id ranges, a block scan,
+// then the thread holding that member scans its range.
+template <typename DT>
+__device__ void tie_pass(Shared& S, RowG& g, const void* slot, int ept, int vlen, int base) {
+  const int t = threadIdx.x;
+  const int l0 = t * ept, l1 = min(l0 + ept, vlen);
+  const float zt = g.zt;
+  uint32_t n = 0;
+  for (int l = l0; l < l1; ++l) n += Lg<DT>::at(slot, l) == zt;
+  uint32_t tot;
+  const uint32_t ex = block_excl_scan<uint32_t>(n, S.scan32, &tot);
+  if (ex < g.quota && ex + n >= g.quota) {
+    uint32_t k = ex;
+    for (int l = l0; l < l1; ++l) {
+      if (Lg<DT>::at(slot, l) == zt && ++k == g.quota) {
+        g.idcut = base + l;
         break;
       }
-    p.digit = lowest < 0 ? 0 : lowest;
-    p.cnt_above = (unsigned int)(tc - (lowest < 0 ? 0 : gcnt[lowest]));
-    p.mass_above = tw - (lowest < 0 ? 0 : gmass[lowest]);
-    return p;
+    }
   }
-  const int src = __ffs(who) - 1;
-  p.digit = __shfl_sync(0xffffffffu, digit, src);
-  p.cnt_above = (unsigned int)__shfl_sync(0xffffffffu, ac, src);
-  p.mass_above = __shfl_sync(0xffffffffu, aw, src);
-  return p;
+  __syncthreads();
+}
+
+// Sampling weight of slice index l: the residual (p - q)+ (paired units) or p,
+// and p itself (both 0 outside the target's kept set).
+template <typename DT>
+__device__ __forceinline__ void elem_w(const void* s0, const void* s1, bool paired,
+                                       const RowG& g0, const RowG& g1, int l, int base,
+                                       float* r, float* p) {
+  const float zp = Lg<DT>::at(s0, l);
+  const int gid = base + l;
+  *r = 0.0f;
+  *p = 0.0f;
+  if (kept(zp, gid, g0.zt, g0.idcut)) {
+    const float pp = __fmul_rn(wacc(zp, g0), g0.invZ);
+    float q = 0.0f;
+    if (paired) {
+      const float zq = Lg<DT>::at(s1, l);
+      if (kept(zq, gid, g1.zt, g1.idcut)) q = __fmul_rn(wacc(zq, g1), g1.invZ);
+    }
+    *r = fmaxf(__fsub_rn(pp, q), 0.0f);
+    *p = pp;
+  }
+}
+
+// Residual and target mass over a contiguous id range, as fixed-point sums (2^-40).
+template <typename DT>
+__device__ __forceinline__ void sample_range(const void* s0, const void* s1, bool paired,
+                                             const RowG& g0s, const RowG& g1s, int l0, int l1,
+                                             int base, unsigned long long* R,
+                                             unsigned long long* Pm) {
+  const RowG g0 = g0s, g1 = g1s;            // row constants in registers
+  unsigned long long ra = 0, pa = 0;
+  for (int l = l0; l < l1; ++l) {
+    const float zp = Lg<DT>::at(s0, l);
+    if (!(zp > g0.zt || (zp == g0.zt && base + l <= g0.idcut))) continue;
+    float r, p;
+    elem_w<DT>(s0, s1, paired, g0, g1, l, base, &r, &p);
+    ra += fixr(r);
+    pa += fixr(p);
+  }
+  *R = ra;
+  *Pm = pa;
+}
+
+// Warp: the first id in [a0, a1) at which the running sum (from acc) times 2^24
+// exceeds kv * S; `useR` selects the residual or p. -1 if none.
+template <typename DT>
+__device__ int warp_sample_find(const void* s0, const void* s1, bool paired, const RowG& g0,
+                                const RowG& g1, int a0, int a1, int base, unsigned long long acc,
+                                bool useR, uint32_t kv, unsigned long long S) {
+  const int ln = lane_id();
+  for (int c0 = a0; c0 < a1; c0 += 32) {
+    const int l = c0 + ln;
+    unsigned long long w = 0;
+    if (l < a1) {
+      float r, p;
+      elem_w<DT>(s0, s1, paired, g0, g1, l, base, &r, &p);
+      w = fixr(useR ? r : p);
+    }
+    unsigned long long inc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (ln >= o) inc += v;
+    }
+    const bool hit = l < a1 && mul_gt(acc + inc, 1ull << 24, kv, S);
+    const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+    if (bal) return base + c0 + __ffs(bal) - 1;
+    acc += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  return -1;
+}
+
+// Probabilities of a row slice (truncated-probabilities mode).
+template <typename DT>
+__device__ void write_probs(const void* slot, const RowG& gs, int vlen, int base, float* out) {
+  const RowG g = gs;
+  for (int l = threadIdx.x; l < vlen; l += NT) {
+    const float z = Lg<DT>::at(slot, l);
+    out[base + l] = kept(z, base + l, g.zt, g.idcut) ? __fmul_rn(wacc(z, g), g.invZ) : 0.0f;
+  }
 }
 
 // Publishes one unit's result; the last of the K+1 units of sequence b writes
@@ -359,13 +1033,14 @@ __device__ void publish_unit(const Params& P, int unit, int b, int token, bool f
   if (old != (unsigned int)P.K) return;
   __threadfence();
   int nacc = P.K, bad = 0;
-  const volatile unsigned long long* u = P.ws_units + (size_t)b * (P.K + 1);
+  const volatile unsigned long long* u = P.ws_units;
+  auto rec = [&](int q) { return u[q < P.K ? (size_t)b * P.K + q : (size_t)P.B * P.K + b]; };
   for (int q = 0; q <= P.K; ++q) {
-    const unsigned long long rec = u[q];
-    bad |= (int)((rec >> 33) & 1ull);
-    if (q < P.K && nacc == P.K && !((rec >> 32) & 1ull)) nacc = q;
+    const unsigned long long r = rec(q);
+    bad |= (int)((r >> 33) & 1ull);
+    if (q < P.K && nacc == P.K && !((r >> 32) & 1ull)) nacc = q;
   }
-  const int last = (int)(uint32_t)u[nacc];
+  const int last = (int)(uint32_t)rec(nacc);
   int32_t* ot = P.out_tokens + (size_t)b * (P.K + 1);
   for (int q = 0; q <= P.K; ++q) {
     int v = -1;
@@ -373,1183 +1048,615 @@ __device__ void publish_unit(const Params& P, int unit, int b, int token, bool f
     ot[q] = v;
   }
   P.out_n[b] = bad ? -1 : nacc;
-  for (int q = 0; q <= P.K; ++q) P.ws_units[(size_t)b * (P.K + 1) + q] = 0ull;
+  for (int q = 0; q <= P.K; ++q)
+    P.ws_units[q < P.K ? (size_t)b * P.K + q : (size_t)P.B * P.K + b] = 0ull;
   P.ws_tickets[b] = 0u;
 }
 
-// ------------------------------------------------------------------------
-// Exact cut over n gathered entries (composite (key << 32) | ~id, n <= GCAP),
-// run by the whole CTA. Sorting the composites in descending order gives the
-// token order (logit desc, id asc). Top-k rows: the first kk entries, then the
-// top-p prefix inside them. Top-p rows: entries after `above` mass, cut where
-// the exclusive mass reaches X. Writes thr/tie/ZL (kept iff key > thr or key
-// == thr and id <= tie).
-__device__ void local_select(unsigned long long* g, int n, const RowK& rk, float fscale,
-                             uint32_t kmask, unsigned long long* scan, uint32_t* out_thr,
-                             int* out_tie, unsigned long long* out_zl, int* out_fail) {
-  const int tid = threadIdx.x;
-  int N = 2;
-  while (N < n) N <<= 1;
-  for (int p = n + tid; p < N; p += NT) g[p] = 0ull;
-  __syncthreads();
-  for (int k = 2; k <= N; k <<= 1) {              // bitonic sort, descending
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int p = tid; p < N; p += NT) {
-        const int q = p ^ j;
-        if (q > p) {
-          const unsigned long long a = g[p], c = g[q];
-          const bool desc = (p & k) == 0;
-          if (desc ? (a < c) : (a > c)) {
-            g[p] = c;
-            g[q] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  constexpr int PER = GCAP / NT;
-  unsigned long long e[PER];
-  unsigned long long s = 0;
-#pragma unroll
-  for (int u = 0; u < PER; ++u) {
-    const int p = tid * PER + u;
-    e[u] = 0;
-    if (p < n) {
-      const uint32_t key = (uint32_t)(g[p] >> 32);
-      e[u] = to_fixed(hweight(mkey_to_float(key, kmask), rk.w), fscale);
-    }
-    s += e[u];
-  }
-  unsigned long long tot;
-  const unsigned long long base = block_excl_scan<unsigned long long>(s, scan, &tot);
-  int limit = n;
-  double X = rk.X;
-  unsigned long long above = rk.above;
-  const bool topp = rk.topp < 1.0f;
-  __shared__ unsigned long long z1s;
-  __shared__ unsigned int kept_s;
-  if (rk.mode == RM_TOPK) {
-    limit = min(n, rk.kk);
-    above = 0;
-    if (tid == 0) z1s = 0;
-    __syncthreads();
-    unsigned long long run = base;
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int p = tid * PER + u;
-      if (p == limit - 1) z1s = run + e[u];
-      run += e[u];
-    }
-    __syncthreads();
-    X = (double)rk.topp * (double)z1s;
-  }
-  unsigned int c = 0;
-  {
-    unsigned long long run = base;
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int p = tid * PER + u;
-      if (p < limit && (!topp || (double)(above + run) < X)) ++c;
-      run += e[u];
-    }
-  }
-  unsigned int kept = block_sum<unsigned int>(c, (unsigned int*)scan);
-  if (rk.mode == RM_TOPK && kept < 1) kept = 1;
-  if (tid == 0) kept_s = kept;
-  __syncthreads();
-  kept = kept_s;
-  if (tid == 0) {
-    if (kept == 0) {
-      // the cut lies just above the listed range: keep only what is above it
-      *out_thr = (uint32_t)(g[0] >> 32);
-      *out_tie = -1;
-      *out_zl = above;
-    } else {
-      const unsigned long long last = g[kept - 1];
-      *out_thr = (uint32_t)(last >> 32);
-      *out_tie = (int)(~(uint32_t)last);
-    }
-    *out_fail = (rk.mode == RM_TOPK && n < rk.kk) ? 1 : 0;
-  }
-  {
-    unsigned long long run = base;
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int p = tid * PER + u;
-      if (kept > 0 && p == (int)kept - 1) *out_zl = above + run + e[u];
-      run += e[u];
-    }
-  }
-  __syncthreads();
-}
-
-// Logit j of a row slice in shared memory (plain loads the compiler schedules).
-template <typename DT>
-__device__ __forceinline__ float ld_logit(const unsigned char* base, int j) {
-  return to_f32<DT>(reinterpret_cast<const DT*>(base)[j]);
-}
-// Two consecutive logits j, j+1 (j even) of a bf16 row from one 32-bit word.
-__device__ __forceinline__ void ld_pair(const unsigned char* base, int j, float& z0, float& z1) {
-  const uint32_t w = reinterpret_cast<const uint32_t*>(base)[j >> 1];
-  z0 = __uint_as_float(w << 16);
-  z1 = __uint_as_float(w & 0xffff0000u);
-}
-
-// Pass B over one row slice: see the file header. zh: fixed-point head mass,
-// zt: fp32 tail mass (full-support rows), histograms in pm/pc (stride NT).
-template <typename DT>
-__device__ __forceinline__ void passB_row(const unsigned char* base, int j0, int j1, int ept,
-                                          int mode, const RowW w, uint32_t tau, uint32_t kmask,
-                                          float fscale, float* pm, uint8_t* pc, uint16_t* list,
-                                          unsigned int* lcnt, unsigned long long& zh, float& zt) {
-  constexpr int PAIR = sizeof(DT) == 2 ? 2 : 1;
-  auto topp_elem = [&](float z) -> bool {
-    const float e = hweight(z, w);
-    if (z >= w.zh) {
-      zh += to_fixed(e, fscale);
-      return true;
-    }
-    const float dd = tail_dist(z, w);
-    const int bb = dd < 16.0f ? (int)dd : NB;
-    pm[bb * NT] += e;
-    pc[bb * NT] += 1;
-    return false;
-  };
-  for (int s = 0; s < ept; s += PAIR) {
-    const int j = j0 + s;
-    float z[2];
-    bool v[2];
-    if (PAIR == 2) {
-      v[0] = j < j1;
-      v[1] = j + 1 < j1;
-      if (v[0]) ld_pair(base, j, z[0], z[1]);
-    } else {
-      v[0] = j < j1;
-      if (v[0]) z[0] = ld_logit<DT>(base, j);
-    }
-#pragma unroll
-    for (int k = 0; k < PAIR; ++k) {
-      bool in = false;
-      if (v[k]) {
-        if (mode == RM_TOPK) {
-          in = mkey(z[k], kmask) >= tau;
-        } else if (mode == RM_TOPP) {
-          in = topp_elem(z[k]);
-        } else {
-          const float e = hweight(z[k], w);
-          if (z[k] >= w.zh) zh += to_fixed(e, fscale);
-          else zt += e;
-        }
-      }
-      if (mode != RM_FULL) list_push(in, (uint16_t)(j + k), list, lcnt, LCAP);
-    }
-  }
-}
-
-// One refinement pass over the tail tokens of range q at level lev - 1:
-// mass/count per sub-bin of level lev, and the key range of those tokens.
-template <typename DT>
-__device__ __forceinline__ void refine_row(const unsigned char* base, int j0, int j1, const RowW w,
-                                           int q, float sc_prev, float sc_cur, uint32_t kmask,
-                                           float* pm, uint8_t* pc, uint32_t& kmn, uint32_t& kmx) {
-  for (int j = j0; j < j1; ++j) {
-    const float z = ld_logit<DT>(base, j);
-    if (z >= w.zh) continue;
-    const float dd = tail_dist(z, w);
-    if (dd >= 16.0f || (int)(dd * sc_prev) != q) continue;
-    const int sub = ((int)(dd * sc_cur)) & (NB - 1);
-    pm[sub * NT] += hweight(z, w);
-    pc[sub * NT] += 1;
-    const uint32_t key = mkey(z, kmask);
-    kmn = min(kmn, key);
-    kmx = max(kmx, key);
-  }
-}
-
-// Lists the tail tokens of range q at level lev (scale = 16^lev).
-template <typename DT>
-__device__ __forceinline__ void list_range_row(const unsigned char* base, int j0, int j1, int ept,
-                                               const RowW w, int q, float scl, uint16_t* list,
-                                               unsigned int* lcnt) {
-  for (int s = 0; s < ept; ++s) {
-    const int j = j0 + s;
-    bool in = false;
-    if (j < j1) {
-      const float z = ld_logit<DT>(base, j);
-      if (z < w.zh) {
-        const float dd = tail_dist(z, w);
-        in = dd < 16.0f && (int)(dd * scl) == q;
-      }
-    }
-    list_push(in, (uint16_t)j, list, lcnt, LCAP);
-  }
-}
-
-// Token id of the target-th (0-based) member, in id order, of the tie group
-// {key == thr} of each row flagged in `want`; NO_TIE for rows not flagged.
-// Every CTA of the cluster calls it (two cluster barriers). Per-thread ranges
-// are contiguous and CTAs hold consecutive slices, so thread order and CTA
-// order are token-id order.
-template <typename DT>
-__device__ void tie_split(const bool want[2], const uint32_t thr[2], const unsigned int target[2],
-                          const unsigned char* rb0, const unsigned char* rb1, int j0, int j1,
-                          int v0, uint32_t kmask, Work& W, int& xb, uint32_t C, uint32_t rank,
-                          int out[2]) {
-  const int tid = threadIdx.x;
-  unsigned int cnt[2] = {0, 0};
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    if (!want[r]) continue;
-    const unsigned char* rb = r == 0 ? rb0 : rb1;
-    for (int j = j0; j < j1; ++j) cnt[r] += (mkey(ld_logit<DT>(rb, j), kmask) == thr[r]);
-  }
-  unsigned int excl[2], tot[2];
-  excl[0] = block_excl_scan<unsigned int>(cnt[0], W.scan32, &tot[0]);
-  excl[1] = block_excl_scan<unsigned int>(cnt[1], W.scan32, &tot[1]);
-  const int buf = xb;
-  xb ^= 1;
-  if (tid == 0) {
-    W.xs[buf][0] = tot[0];
-    W.xs[buf][1] = tot[1];
-  }
-  __syncthreads();
-  cluster_sync();
-  int found[2] = {NO_TIE, NO_TIE};
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    if (!want[r]) continue;
-    unsigned int off = 0;
-    for (uint32_t q = 0; q < rank; ++q) off += (unsigned int)ld_peer_u64(&W.xs[buf][r], q);
-    const unsigned int lo = off + excl[r];
-    if (cnt[r] > 0 && target[r] >= lo && target[r] < lo + cnt[r]) {
-      const unsigned char* rb = r == 0 ? rb0 : rb1;
-      unsigned int seen = lo;
-      for (int j = j0; j < j1; ++j)
-        if (mkey(ld_logit<DT>(rb, j), kmask) == thr[r]) {
-          if (seen == target[r]) {
-            found[r] = v0 + j;
-            break;
-          }
-          ++seen;
-        }
-    }
-  }
-  const int buf2 = xb;
-  xb ^= 1;
-  if (tid < 2) W.xs[buf2][tid] = NO_TIE;
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < 2; ++r)
-    if (found[r] != NO_TIE) W.xs[buf2][r] = (unsigned long long)found[r];
-  __syncthreads();
-  cluster_sync();
-  if (tid < 2) {
-    int f = NO_TIE;
-    for (uint32_t q = 0; q < C; ++q) f = min(f, (int)ld_peer_u64(&W.xs[buf2][tid], q));
-    W.bi[6 + tid] = f;
-  }
-  __syncthreads();
-  out[0] = W.bi[6];
-  out[1] = W.bi[7];
-  __syncthreads();
-}
-
-// ------------------------------------------------------------------------
-template <typename DT, int MODE>
-__global__ void __launch_bounds__(NT, 3) sv_kernel(const Params P) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const uint32_t C = cluster_size();
-  const uint32_t rank = cluster_rank();
-  const int unit = blockIdx.x / C;
-  const int tid = threadIdx.x;
-  const int V = P.V;
-  const int es = (int)sizeof(DT);
-  const size_t row_bytes = ((size_t)P.slice * es + 15) & ~(size_t)15;
-  Work& W = *reinterpret_cast<Work*>(smem + 2 * row_bytes);
-  const uint32_t sb0 = smem_addr(smem);                 // shared addresses (DSMEM peers)
-  const uint32_t sb1 = smem_addr(smem + row_bytes);
-  const unsigned char* rb0 = smem;                       // row slices for local loads
-  const unsigned char* rb1 = smem + row_bytes;
-  const uint32_t kmask = P.keymask;
-  const float fscale = P.fix_scale;
-
-  // ---------------------------------------------------------------- unit
-  int b, i, seq;
-  const DT* g0;
-  const DT* g1 = nullptr;
+// ------------------------------------------------------------------ kernel
+template <int MODE>
+__device__ __forceinline__ void decode_unit(const Params& P, int u, int* b, int* i) {
   if (MODE == MODE_VERIFY) {
-    b = unit / (P.K + 1);
-    i = unit % (P.K + 1);
-    seq = b;
-    g0 = reinterpret_cast<const DT*>(P.rows0) + ((size_t)b * (P.K + 1) + i) * V;
-  } else if (MODE == MODE_SAMPLE) {
-    b = unit / P.K;
-    i = unit % P.K;
-    seq = b;
-    g0 = reinterpret_cast<const DT*>(P.rows0) + (size_t)unit * V;
+    const int nb = P.B * P.K;
+    if (u < nb) {
+      *b = u / P.K;
+      *i = u - *b * P.K;
+    } else {
+      *b = u - nb;
+      *i = P.K;
+    }
+  } else if (MODE == MODE_PROBS) {
+    *b = u;
+    *i = 0;
   } else {
-    b = unit;
-    i = 0;
-    seq = unit;
-    g0 = reinterpret_cast<const DT*>(P.rows0) + (size_t)unit * V;
+    *b = u / P.K;
+    *i = u - *b * P.K;
   }
-  const float T = P.temp[seq];
-  const int topk = P.topk[seq];
-  const float topp = P.topp[seq];
-  const bool greedy = (T == 0.0f);
-  bool param_bad = !(T >= 0.0f) || !(topp > 0.0f) || topk < 0;   // NaN fails >= and >
-  int dtok = -1;
+}
+
+template <int MODE>
+__device__ __forceinline__ bool param_error(const Params& P, const Meta& m, int i) {
+  if (!(m.T >= 0.0f) || m.T == INFINITY || !(m.P > 0.0f) || m.k < 0) return true;
   if (MODE == MODE_VERIFY && i < P.K) {
-    dtok = P.dtok[(size_t)b * P.K + i];
-    if (dtok < 0 || dtok >= V) param_bad = true;
+    if (m.d < 0 || m.d >= P.V) return true;
+    if (m.T > 0.0f && P.rows1 == nullptr) return true;
   }
-  int nrows = 1;
-  if (MODE == MODE_VERIFY && i < P.K && !greedy && !param_bad) {
-    if (P.rows1 == nullptr) {
-      param_bad = true;
-    } else {
-      nrows = 2;
-      g1 = reinterpret_cast<const DT*>(P.rows1) + ((size_t)b * P.K + i) * V;
-    }
-  }
-  SV_MARK(0);
-  const int v0 = (int)rank * P.slice;
-  const int n = max(0, min(V, v0 + P.slice) - v0);
+  return false;
+}
 
-  // ---------------------------------------------------------------- load
+// Rows a unit reads: 0 on a parameter error, 2 for a sampling position i < K.
+template <int MODE>
+__device__ __forceinline__ int unit_rows(const Params& P, const Meta& m, int i) {
+  if (param_error<MODE>(P, m, i)) return 0;
+  if (MODE == MODE_VERIFY && i < P.K && m.T > 0.0f) return 2;
+  return 1;
+}
+
+template <typename DT, int MODE>
+__device__ __forceinline__ const DT* row_src(const Params& P, int b, int i, int which) {
+  const DT* r0 = static_cast<const DT*>(P.rows0);
+  if (MODE == MODE_VERIFY) {
+    if (which == 0) return r0 + ((size_t)b * (P.K + 1) + i) * P.V;
+    return static_cast<const DT*>(P.rows1) + ((size_t)b * P.K + i) * P.V;
+  }
+  if (MODE == MODE_PROBS) return r0 + (size_t)b * P.V;
+  return r0 + ((size_t)b * P.K + i) * P.V;
+}
+
+template <int MODE>
+__device__ void load_meta(Shared& S, const Params& P, int cid, int ncl, int nmine, int j0, int cnt) {
+  for (int t = threadIdx.x; t < cnt; t += NT) {
+    const int j = j0 + t;
+    if (j >= nmine) break;
+    int b, i;
+    decode_unit<MODE>(P, cid + j * ncl, &b, &i);
+    Meta m;
+    m.T = P.temp[b];
+    m.P = P.topp[b];
+    m.k = P.topk[b];
+    m.d = (MODE == MODE_VERIFY && i < P.K) ? P.dtok[(size_t)b * P.K + i] : 0;
+    S.meta[j % MR] = m;
+  }
+}
+
+template <typename DT>
+__device__ __forceinline__ DT neg_inf();
+template <>
+__device__ __forceinline__ float neg_inf<float>() {
+  return -INFINITY;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 neg_inf<__nv_bfloat16>() {
+  return __ushort_as_bfloat16((unsigned short)0xFF80u);
+}
+
+template <typename DT, int MODE>
+__global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  Shared& S = *reinterpret_cast<Shared*>(smem);
+  const size_t slot_bytes = (size_t)P.slot_elems * sizeof(DT);
+  unsigned char* slots = smem + SHARED_BYTES;
+  unsigned char* H = slots + (size_t)P.NS * slot_bytes;
+  float* hist = reinterpret_cast<float*>(H);
+  uint8_t* hcnt = H + (size_t)NB * NT * 4;
+  unsigned long long* lists = reinterpret_cast<unsigned long long*>(H);
+  X2Row* x2 = reinterpret_cast<X2Row*>(H);
+  unsigned char* Gr = H + H_BYTES;
+  unsigned long long* gbuf = reinterpret_cast<unsigned long long*>(Gr);
+
+  const int tid = threadIdx.x;
+  const uint32_t rank = cluster_rank();
+  const int C = P.C;
+  const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
+  const int base = (int)rank * P.slice;
+  const int vlen = max(0, min(P.slice, P.V - base));
+  const int nvec = (int)(slot_bytes / 16);
+  const int nmine = cid < P.nunits ? (P.nunits - 1 - cid) / ncl + 1 : 0;
+  const uint32_t copy_bytes = (uint32_t)((size_t)vlen * sizeof(DT));
+  const uint64_t pol = policy_evict_first();
+
   if (tid == 0) {
-    mbar_init(&W.mbar, 1);
+    for (int s = 0; s < P.NS; ++s) mbar_init(&S.full[s], 1);
     fence_mbar_init();
+    S.timeout = 0;
   }
+  for (int s = 0; s < P.NS; ++s) {
+    DT* sp = reinterpret_cast<DT*>(slots + (size_t)s * slot_bytes);
+    for (int l = vlen + tid; l < P.slot_elems; l += NT) sp[l] = neg_inf<DT>();
+  }
+  load_meta<MODE>(S, P, cid, ncl, nmine, 0, MR);
   __syncthreads();
-  int load_bad = 0;
-  if (P.bulk_ok) {
-    if (tid == 0) {
-      const uint32_t bytes = (uint32_t)(n * es);
-      mbar_arrive_expect_tx(&W.mbar, bytes * nrows);
-      const uint64_t pol = policy_evict_first();
-      for (int r = 0; r < nrows; ++r) {
-        const char* src = reinterpret_cast<const char*>((r == 0 ? g0 : g1) + v0);
-        char* dst = reinterpret_cast<char*>(smem + (r == 0 ? 0 : row_bytes));
-        for (uint32_t off = 0; off < bytes; off += 32768u) {
-          const uint32_t sz = min(32768u, bytes - off);
-          bulk_g2s(dst + off, src + off, sz, &W.mbar, pol);
-        }
-      }
-    }
-    if (!mbar_wait_bounded(&W.mbar, 0, WAIT_LIMIT_NS)) {
-      load_bad = 1;
-      if (tid == 0) atomicOr(P.ws_error, 1u);
-    }
-  } else {
-    DT* d0 = reinterpret_cast<DT*>(smem);
-    DT* d1 = reinterpret_cast<DT*>(smem + row_bytes);
-    for (int j = tid; j < n; j += NT) d0[j] = g0[v0 + j];
-    if (nrows == 2)
-      for (int j = tid; j < n; j += NT) d1[j] = g1[v0 + j];
-    __syncthreads();
-  }
-  SV_MARK(1);
-  const int j0 = tid * P.ept;
-  const int j1 = min(n, j0 + P.ept);
-  const int ept = P.ept;
 
-  // ------------------------------------------- pass A: max, argmax, NaN
-  const bool topk_on = topk > 0 && topk < V;
-  const int kk = topk_on ? topk : V;
-  float best[2] = {-INFINITY, -INFINITY};
-  int bidx[2] = {0x7fffffff, 0x7fffffff};
-  int bad[2] = {0, 0};
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    if (r < nrows) {
-      const unsigned char* rb = r == 0 ? rb0 : rb1;
-      float bb = -INFINITY;
-      int bi = 0x7fffffff, bd = 0;
-      for (int j = j0; j < j1; ++j) {
-        const float z = ld_logit<DT>(rb, j);
-        bd |= !(z <= 3.402823466e38f);        // NaN or +inf
-        if (z > bb) {
-          bb = z;
-          bi = j;
-        }
-      }
-      best[r] = bb;
-      bidx[r] = bi;
-      bad[r] = bd;
-    }
-  }
-  uint32_t kth[2] = {KEY_ALL, KEY_ALL};
-  if (!greedy && topk_on && kk <= NT) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-      if (r < nrows)
-        kth[r] = block_kth_largest(mkey(best[r], kmask), j1 > j0, kk, W.kthh[r], W.scan32, P.nlev);
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    for (int o = 16; o; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best[r], o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bidx[r], o);
-      if (ob > best[r] || (ob == best[r] && oi < bidx[r])) {
-        best[r] = ob;
-        bidx[r] = oi;
-      }
-      bad[r] |= __shfl_xor_sync(0xffffffffu, bad[r], o);
-    }
-  }
-  {
-    __shared__ float sbest[2][NWARP];
-    __shared__ int sidx[2][NWARP], sbad[2][NWARP];
-    if (lane_id() == 0)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        sbest[r][warp_id()] = best[r];
-        sidx[r][warp_id()] = bidx[r];
-        sbad[r][warp_id()] = bad[r];
-      }
-    __syncthreads();
-    if (tid < 2) {
-      const int r = tid;
-      float bb = -INFINITY;
-      int ii = 0x7fffffff, bd = load_bad;
-      for (int w = 0; w < NWARP; ++w) {
-        if (sbest[r][w] > bb || (sbest[r][w] == bb && sidx[r][w] < ii)) {
-          bb = sbest[r][w];
-          ii = sidx[r][w];
-        }
-        bd |= sbad[r][w];
-      }
-      W.xa[r].best = bb;
-      W.xa[r].best_id = (ii == 0x7fffffff) ? 0x7fffffff : v0 + ii;
-      W.xa[r].bad = bd;
-      W.xa[r].kth = r == 0 ? kth[0] : kth[1];
-    }
-  }
-  __syncthreads();
-  SV_MARK(2);
-  cluster_sync();  // X1
-  SV_MARK(3);
-  if (tid < 2) {
-    const int r = tid;
-    float bb = -INFINITY;
-    int ii = 0x7fffffff, bd = 0;
-    uint32_t kt = KEY_ALL;
-    for (uint32_t c = 0; c < C; ++c) {
-      const float pb = ld_peer_f32(&W.xa[r].best, c);
-      const int pi = (int)ld_peer_u32(&W.xa[r].best_id, c);
-      if (pb > bb || (pb == bb && pi < ii)) {
-        bb = pb;
-        ii = pi;
-      }
-      bd |= (int)ld_peer_u32(&W.xa[r].bad, c);
-      kt = max(kt, ld_peer_u32(&W.xa[r].kth, c));
-    }
-    RowK& rk = W.rk[r];
-    rk.w.m = bb;
-    rk.argmax = ii;
-    rk.bad = bd | (bb == -INFINITY ? 1 : 0);
-    rk.tau = kt;
-    rk.kk = kk;
-    rk.topp = topp;
-    rk.thr = KEY_ALL;
-    rk.tie = NO_TIE;
-    rk.ZL = 0;
-    rk.Z = 0;
-    rk.Zh = 0;
-    rk.above = 0;
-    rk.X = 0.0;
-    rk.lev = -1;
-    rk.q = 0;
-    rk.need = ND_DONE;
-    if (!greedy && !(bd | (bb == -INFINITY))) {
-      // per-row weight constants, once per CTA (double precision on one thread)
-      const double inv = 1.0 / (double)T;
-      const double c2 = 1.4426950408889634 * inv;
-      rk.w.c2 = (float)c2;
-      rk.w.c2_lo = (float)(c2 - (double)rk.w.c2);
-      rk.w.invT = (float)inv;
-      rk.w.zh = (float)((double)bb - (double)DHEAD * (double)T);
-      rk.mode = topk_on ? ((kk <= NT) ? RM_TOPK : -1) : (topp < 1.0f ? RM_TOPP : RM_FULL);
-    } else {
-      rk.mode = RM_FULL;
-    }
-  }
-  __syncthreads();
-  int xb = 0;            // next exchange buffer
-  const bool unit_err = param_bad || W.rk[0].bad || (nrows == 2 && W.rk[1].bad);
+  int next_j = 0, rows_issued = 0, rows_done = 0, xr = 0, lp = 0;
 
-  // --------------------------------------------------------- greedy / error
-  if (greedy || unit_err) {
-    const int am = W.rk[0].argmax;
-    if (MODE == MODE_SAMPLE && rank == 0 && tid == 0) P.out_tokens[unit] = unit_err ? -1 : am;
-    if (MODE == MODE_PROBS) {
-      float* out = P.out_probs + (size_t)unit * V + v0;
-      for (int j = tid; j < n; j += NT)
-        out[j] = unit_err ? __int_as_float(0x7fc00000) : ((v0 + j == am) ? 1.0f : 0.0f);
-    }
-    cluster_sync();  // peers may still read this CTA's exchange slots
-    if (MODE == MODE_VERIFY && rank == 0 && tid == 0)
-      publish_unit(P, unit, b, unit_err ? -1 : am, !unit_err && i < P.K && dtok == am, unit_err);
-    if (load_bad) mbar_wait_bounded(&W.mbar, 0, WAIT_LIMIT_NS);
-    return;
-  }
-
-  // ------------------------------------------------------- pass B
-  const RowW rw0 = W.rk[0].w, rw1 = W.rk[1].w;
-  const int mode0 = W.rk[0].mode, mode1 = W.rk[1].mode;
-  const uint32_t tau0 = W.rk[0].tau, tau1 = W.rk[1].tau;
-  const bool general_k = (mode0 < 0);      // top-k with k beyond the per-thread pool
-  if (tid < 2) W.lcnt[tid] = 0;
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    if (r >= nrows || general_k) continue;
-    const int mode = r == 0 ? mode0 : mode1;
-    unsigned long long zh = 0;
-    float zt = 0.f;
-    if (mode == RM_TOPP) {
-#pragma unroll
-      for (int bb = 0; bb < NBH; ++bb) {
-        W.u.ph.pmass[bb][tid] = 0.f;
-        W.u.ph.pcnt[bb][tid] = 0;
-      }
-    }
-    passB_row<DT>(r == 0 ? rb0 : rb1, j0, j1, ept, mode, r == 0 ? rw0 : rw1, r == 0 ? tau0 : tau1,
-                  kmask, fscale, &W.u.ph.pmass[0][tid], &W.u.ph.pcnt[0][tid], W.list[r],
-                  &W.lcnt[r], zh, zt);
-    __syncthreads();
-    XB& x = W.xb[xb][r];
-    const unsigned long long zhs = block_sum<unsigned long long>(zh, W.scan64);
-    const unsigned long long zts = block_sum<unsigned long long>(to_fixed(zt, fscale), W.scan64);
-    if (mode == RM_TOPP) {
-      // reduce the private histograms: warp w handles bins w, w + NWARP, ...
-      for (int bb = warp_id(); bb < NBH; bb += NWARP) {
-        unsigned long long m = 0;
-        unsigned int c = 0;
-        for (int t = lane_id(); t < NT; t += 32) {
-          m += to_fixed(W.u.ph.pmass[bb][t], fscale);
-          c += W.u.ph.pcnt[bb][t];
-        }
-        m = warp_sum(m);
-        c = warp_sum(c);
-        if (lane_id() == 0) {
-          x.hm[bb] = m;
-          x.hc[bb] = c;
-        }
-      }
-    }
-    if (tid == 0) {
-      x.zh = zhs;
-      x.zt = zts;
-      x.lcnt = W.lcnt[r];
-    }
-    __syncthreads();
-  }
-  SV_MARK(4);
-  cluster_sync();   // X2
-  SV_MARK(5);
-  // cluster totals and the next step of every row (thread r decides row r)
-  if (tid < nrows && !general_k) {
-    const int r = tid;
-    RowK& rk = W.rk[r];
-    unsigned long long zh = 0, zt = 0, hm[NBH];
-    unsigned int hc[NBH], lc = 0, lmax = 0;
-    for (int bb = 0; bb < NBH; ++bb) {
-      hm[bb] = 0;
-      hc[bb] = 0;
-    }
-    const XB* px = &W.xb[xb][r];
-    for (uint32_t c = 0; c < C; ++c) {
-      zh += ld_peer_u64(&px->zh, c);
-      zt += ld_peer_u64(&px->zt, c);
-      const unsigned int l = ld_peer_u32(&px->lcnt, c);
-      rk.rc[c] = l;
-      lc += l;
-      lmax = max(lmax, l);
-      if (rk.mode == RM_TOPP)
-        for (int bb = 0; bb < NBH; ++bb) {
-          hm[bb] += ld_peer_u64(&px->hm[bb], c);
-          hc[bb] += ld_peer_u32(&px->hc[bb], c);
-        }
-    }
-    rk.Zh = zh;
-    if (rk.mode == RM_FULL) {
-      rk.Z = zh + zt;
-      rk.ZL = rk.Z;
-      rk.need = ND_DONE;
-    } else if (rk.mode == RM_TOPK) {
-      rk.need = (lc > GCAP || lmax > LCAP || lc < (unsigned int)rk.kk) ? ND_GENERAL : ND_LIST;
-      rk.lev = -1;
-    } else {
-      unsigned long long z = zh;
-      for (int bb = 0; bb < NBH; ++bb) z += hm[bb];
-      rk.Z = z;
-      rk.X = (double)rk.topp * (double)z;
-      if ((double)zh >= rk.X) {            // the cut lies in the head
-        rk.lev = -1;
-        rk.above = 0;
-        rk.need = (lc > GCAP || lmax > LCAP) ? ND_GENERAL : ND_LIST;
-      } else {
-        // first bin (by distance) where the cumulative mass reaches X; the
-        // last non-empty bin if rounding keeps the total just below X
-        unsigned long long cum = zh, pick_above = zh;
-        int pick = -1;
-        for (int bb = 0; bb < NBH; ++bb) {
-          if (hc[bb] == 0) continue;
-          pick = bb;
-          pick_above = cum;
-          if ((double)(cum + hm[bb]) >= rk.X) break;
-          cum += hm[bb];
-        }
-        if (pick < 0 || pick == NB) {
-          rk.need = ND_GENERAL;
-        } else {
-          rk.lev = 0;
-          rk.q = pick;
-          rk.above = pick_above;
-          unsigned int cmax = 0;
-          for (uint32_t c = 0; c < C; ++c) {
-            const unsigned int cc = ld_peer_u32(&px->hc[pick], c);
-            rk.rc[c] = cc;
-            cmax = max(cmax, cc);
-          }
-          rk.need = (hc[pick] <= GCAP && cmax <= LCAP) ? ND_LIST : ND_REFINE;
-        }
-      }
-    }
-  }
-  xb ^= 1;
-  __syncthreads();
-#ifdef SV_TRACE
-  if (tid == 0 && rank == 0 && unit < 256)
-    g_trace[unit * 16 + 13] = (unsigned long long)W.rk[1].need | ((unsigned long long)(W.rk[1].lev + 1) << 8) |
-                              ((unsigned long long)W.rk[1].q << 16) | ((unsigned long long)W.rk[1].rc[0] << 32);
-#endif
-
-  // ------------------------------------------------- refinement of top-p cuts
-  for (int lev = 1; lev <= MAXLEV && !general_k; ++lev) {
-    bool any = false;
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-      if (r < nrows && W.rk[r].need == ND_REFINE) any = true;
-    if (!any) break;
-    const float sc_prev = pow16(lev - 1), sc_cur = pow16(lev);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      if (r >= nrows || W.rk[r].need != ND_REFINE) continue;
-      const int q = W.rk[r].q;
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb) {
-        W.u.ph.pmass[bb][tid] = 0.f;
-        W.u.ph.pcnt[bb][tid] = 0;
-      }
-      uint32_t kmn = 0xffffffffu, kmx = 0u;
-      refine_row<DT>(r == 0 ? rb0 : rb1, j0, j1, r == 0 ? rw0 : rw1, q, sc_prev, sc_cur, kmask,
-                     &W.u.ph.pmass[0][tid], &W.u.ph.pcnt[0][tid], kmn, kmx);
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, o));
-        kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, o));
-      }
-      if (lane_id() == 0) {                   // kthh is free after pass A: key-range scratch
-        W.kthh[0][warp_id()] = kmn;
-        W.kthh[1][warp_id()] = kmx;
-      }
+  for (int j = 0; j < nmine; ++j) {
+    if (j > 0 && (j % (MR / 2)) == 0) {
       __syncthreads();
-      XB& x = W.xb[xb][r];
+      load_meta<MODE>(S, P, cid, ncl, nmine, j + MR / 2, MR / 2);
+      __syncthreads();
+    }
+    // producer: row slices of the next units, as far as the slots allow
+    if (P.bulk_ok && !S.timeout) {
+      bool fenced = false;
+      while (next_j < nmine) {
+        int nb_, ni_;
+        decode_unit<MODE>(P, cid + next_j * ncl, &nb_, &ni_);
+        const int nr = unit_rows<MODE>(P, S.meta[next_j % MR], ni_);
+        if (rows_issued - rows_done + nr > P.NS) break;
+        if (tid == 0) {
+          if (!fenced) {
+            fence_proxy_async();
+            fenced = true;
+          }
+          for (int w = 0; w < nr; ++w) {
+            const int s = (rows_issued + w) % P.NS;
+            mbar_arrive_expect_tx(&S.full[s], copy_bytes);
+            if (copy_bytes)
+              bulk_g2s(slots + (size_t)s * slot_bytes, row_src<DT, MODE>(P, nb_, ni_, w) + base,
+                       copy_bytes, &S.full[s], pol);
+          }
+        }
+        rows_issued += nr;
+        ++next_j;
+      }
+    }
+    const int u = cid + j * ncl;
+    int b, i;
+    decode_unit<MODE>(P, u, &b, &i);
+    const Meta m = S.meta[j % MR];
+    SV_MARK(0);
+    const bool perr = param_error<MODE>(P, m, i);
+    const int nr = unit_rows<MODE>(P, m, i);
+    const void* sl[2] = {slots + (size_t)(rows_done % P.NS) * slot_bytes,
+                         slots + (size_t)((rows_done + 1) % P.NS) * slot_bytes};
+    // consumer: wait for (or, without bulk copies, load) the unit's rows
+    if (P.bulk_ok) {
+      if (!S.timeout) {
+        for (int w = 0; w < nr; ++w) {
+          const int ri = rows_done + w;
+          if (!mbar_wait_bounded(&S.full[ri % P.NS], (uint32_t)((ri / P.NS) & 1), WAIT_LIMIT_NS)) {
+            atomicOr(&S.timeout, 1u);
+            atomicOr(P.ws_error, 1u);
+          }
+        }
+      }
+    } else {
+      for (int w = 0; w < nr; ++w) {
+        DT* dst = reinterpret_cast<DT*>(const_cast<void*>(sl[w]));
+        const DT* src = row_src<DT, MODE>(P, b, i, w) + base;
+        for (int l = tid; l < vlen; l += NT) dst[l] = src[l];
+      }
+    }
+    __syncthreads();
+    const bool tmo = S.timeout != 0;
+    SV_MARK(1);
+
+    if (perr) {
+      // ------------------------------------------------ parameter error
+      if (MODE == MODE_VERIFY) {
+        if (rank == 0 && tid == 0) publish_unit(P, u, b, -1, false, true);
+      } else if (MODE == MODE_SAMPLE) {
+        if (rank == 0 && tid == 0) P.out_tokens[(size_t)b * P.K + i] = -1;
+      } else {
+        for (int l = tid; l < vlen; l += NT) P.out_probs[(size_t)b * P.V + base + l] = __int_as_float(0x7fc00000);
+      }
+    } else if (m.T == 0.0f) {
+      // ------------------------------------------------ greedy (T = 0)
+      X1Row& x = S.x1[xr & 1][0];
+      const float tm = thread_max<DT>(sl[0], nvec);
+      const float mx = block_max_nan(tm, S.redf);
+      uint32_t fi = UINT_MAX;
+      if (mx > -INFINITY && mx < INFINITY) fi = thread_first_index<DT>(sl[0], nvec, mx);
+      fi = block_min_u32(fi, S.redu);
       if (tid == 0) {
-        uint32_t a = 0xffffffffu, bmax = 0u;
-        for (int w = 0; w < NWARP; ++w) {
-          a = min(a, W.kthh[0][w]);
-          bmax = max(bmax, W.kthh[1][w]);
-        }
-        x.kmin = a;
-        x.kmax = bmax;
+        x.m = mx;
+        x.flags = ((isnan(mx) || tmo) ? F_NAN : 0u) | (mx == INFINITY ? F_PINF : 0u);
+        x.best = (fi < (uint32_t)vlen) ? (((unsigned long long)okey(mx) << 32) | (uint32_t)~(uint32_t)(base + (int)fi)) : 0ull;
       }
-      for (int bb = warp_id(); bb < NB; bb += NWARP) {
-        unsigned long long m = 0;
-        unsigned int c = 0;
-        for (int t = lane_id(); t < NT; t += 32) {
-          m += to_fixed(W.u.ph.pmass[bb][t], fscale);
-          c += W.u.ph.pcnt[bb][t];
+      cluster_sync();
+      if (warp_id() == 0) {
+        const int l = lane_id();
+        unsigned long long bst = 0;
+        uint32_t fl = 0;
+        float mm = -INFINITY;
+        if (l < C) {
+          bst = ld_peer_u64(&x.best, l);
+          fl = ld_peer_u32(&x.flags, l);
+          mm = ld_peer_f32(&x.m, l);
         }
-        m = warp_sum(m);
-        c = warp_sum(c);
-        if (lane_id() == 0) {
-          x.hm[bb] = m;
-          x.hc[bb] = c;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const unsigned long long ob = __shfl_xor_sync(0xffffffffu, bst, o);
+          bst = ob > bst ? ob : bst;
+          fl |= __shfl_xor_sync(0xffffffffu, fl, o);
+        }
+        mm = warp_max_nan(mm);
+        if (l == 0) {
+          S.res_i[0] = (fl & (F_NAN | F_PINF)) || !(mm > -INFINITY) || bst == 0ull;
+          S.res_i[1] = (int)~(uint32_t)bst;
         }
       }
       __syncthreads();
-    }
-    cluster_sync();   // X3..
-    if (tid < nrows && W.rk[tid].need == ND_REFINE) {
-      const int r = tid;
-      RowK& rk = W.rk[r];
-      unsigned long long hm[NB];
-      unsigned int hc[NB];
-      for (int bb = 0; bb < NB; ++bb) {
-        hm[bb] = 0;
-        hc[bb] = 0;
-      }
-      const XB* px = &W.xb[xb][r];
-      uint32_t kmn = 0xffffffffu, kmx = 0u;
-      for (uint32_t c = 0; c < C; ++c) {
-        for (int bb = 0; bb < NB; ++bb) {
-          hm[bb] += ld_peer_u64(&px->hm[bb], c);
-          hc[bb] += ld_peer_u32(&px->hc[bb], c);
-        }
-        kmn = min(kmn, ld_peer_u32(&px->kmin, c));
-        kmx = max(kmx, ld_peer_u32(&px->kmax, c));
-      }
-      if (kmn == kmx) {
-        // the range holds one logit value: keep the first j members (by id)
-        // whose exclusive mass stays below X
-        unsigned int cnt = 0;
-        for (int bb = 0; bb < NB; ++bb) cnt += hc[bb];
-        const unsigned long long Et = to_fixed(hweight(mkey_to_float(kmn, kmask), rk.w), fscale);
-        double jf = Et > 0 ? ceil((rk.X - (double)rk.above) / (double)Et) : (double)cnt;
-        jf = fmin(fmax(jf, 0.0), (double)cnt);
-        const unsigned int j = (unsigned int)jf;
-        rk.thr = kmn;
-        rk.jt = j;
-        rk.ZL = rk.above + (unsigned long long)j * Et;
-        rk.tie = j == 0 ? -1 : NO_TIE;
-        rk.need = (j == 0 || j == cnt) ? ND_DONE : ND_TIE;
+      const bool err = S.res_i[0] != 0;
+      const int amax = S.res_i[1];
+      if (MODE == MODE_VERIFY) {
+        if (rank == 0 && tid == 0) publish_unit(P, u, b, err ? -1 : amax, i < P.K && m.d == amax, err);
+      } else if (MODE == MODE_SAMPLE) {
+        if (rank == 0 && tid == 0) P.out_tokens[(size_t)b * P.K + i] = err ? -1 : amax;
       } else {
-        unsigned long long cum = rk.above, pick_above = rk.above;
-        int pick = -1;
-        for (int bb = 0; bb < NB; ++bb) {
-          if (hc[bb] == 0) continue;
-          pick = bb;
-          pick_above = cum;
-          if ((double)(cum + hm[bb]) >= rk.X) break;
-          cum += hm[bb];
+        for (int l = tid; l < vlen; l += NT)
+          P.out_probs[(size_t)b * P.V + base + l] =
+              err ? __int_as_float(0x7fc00000) : (base + l == amax ? 1.0f : 0.0f);
+      }
+      ++xr;
+    } else {
+      // ------------------------------------------------ sampling unit
+      const bool paired = nr == 2;
+      if (tid == 0) {
+        for (int rho = 0; rho < nr; ++rho) {
+          RowG& g = S.rg[rho];
+          g = RowG{};
+          g.c = __fdiv_rn(1.44269504088896341f, m.T);   // log2(e)/T
+          g.P = m.P;
+          const int kk = (m.k > 0 && m.k < P.V) ? m.k : P.V;
+          g.kk = kk;
+          g.mode = kk < P.V ? (kk <= KFAST ? RM_LIST : RM_GENERAL) : (m.P < 1.0f ? RM_TOPP : RM_ALL);
+          g.zt = -INFINITY;
+          g.idcut = INT_MAX;
+          g.Rl = -INFINITY;
         }
-        if (pick < 0) {
-          rk.need = ND_GENERAL;
-        } else {
-          rk.lev = lev;
-          rk.q = rk.q * NB + pick;
-          rk.above = pick_above;
-          unsigned int cmax = 0;
-          for (uint32_t c = 0; c < C; ++c) {
-            const unsigned int cc = ld_peer_u32(&px->hc[pick], c);
-            rk.rc[c] = cc;
-            cmax = max(cmax, cc);
+      }
+      __syncthreads();
+      // pass A and pass B (or the top-k candidate list) of each row
+      X1Row* X = S.x1[xr & 1];
+      for (int rho = 0; rho < nr; ++rho) {
+        RowG& g = S.rg[rho];
+        const float tm = thread_max<DT>(sl[rho], nvec);
+        const float mx = block_max_nan(tm, S.redf);
+        const bool fin = mx > -INFINITY && mx < INFINITY;
+        bool ext = false;
+        float R = -INFINITY;
+        if (fin) {
+          const float mc = mx * g.c;
+          if (!(fabsf(mc) < 4194304.0f)) ext = true;
+          else R = 2.0f * ceilf(mc * 0.5f);
+        }
+        if (tid == 0) {
+          X[rho].m = mx;
+          X[rho].flags = ((isnan(mx) || tmo) ? F_NAN : 0u) | (mx == INFINITY ? F_PINF : 0u) |
+                         (ext ? F_EXTREME : 0u);
+          X[rho].R = R;
+          X[rho].ncand = 0;
+          g.Rl = R;
+          S.list_n[rho] = 0;
+        }
+        if (tid < NB) {
+          X[rho].bins[tid] = 0ull;
+          X[rho].cnts[tid] = 0u;
+        }
+        __syncthreads();
+        if (g.mode == RM_LIST) {
+          if (fin) {
+            const uint32_t t16 = block_kth_prefix16(tm, g.kk, reinterpret_cast<uint32_t*>(Gr),
+                                                    reinterpret_cast<uint32_t*>(S.res_i));
+            const float zt = t16 <= 0x007Fu ? -INFINITY : key_to_float(t16 << 16);
+            pass_list<DT>(sl[rho], nvec, vlen, zt, base, lists + rho * LC, &S.list_n[rho]);
+            __syncthreads();
+            if (tid == 0) {
+              X[rho].ncand = min(S.list_n[rho], (uint32_t)LC);
+              if (S.list_n[rho] > (uint32_t)LC) X[rho].flags |= F_OVER;
+            }
           }
-          if (hc[pick] <= GCAP && cmax <= LCAP) rk.need = ND_LIST;
-          else if (lev == MAXLEV) rk.need = ND_GENERAL;
+        } else if (fin && !ext) {
+          if (g.mode == RM_GENERAL) pass_bins<DT, true>(sl[rho], nvec, vlen, g, hist, hcnt, X[rho]);
+          else pass_bins<DT, false>(sl[rho], nvec, vlen, g, hist, hcnt, X[rho]);
+        }
+        __syncthreads();
+        if (rho == 0) SV_MARK(11);
+      }
+      SV_MARK(2);
+      cluster_sync();                                              // S1
+      SV_MARK(3);
+      // cluster maxima, frames, flags
+      if (warp_id() == 0) {
+        for (int rho = 0; rho < nr; ++rho) {
+          bool e, ex, ov;
+          uint32_t ntot;
+          merge_head(S, S.rg[rho], &X[rho], rho, C, rank, &e, &ex, &ov, &ntot);
+          if (lane_id() == 0) {
+            RowG& g = S.rg[rho];
+            g.err = e;
+            g.extreme = ex;
+            g.sh = ex ? 0 : (g.Rl > -INFINITY ? (int)fminf(g.Rg - g.Rl, 4096.0f) : 4096);
+            S.res_i[2 + rho] = ov ? -1 : (int)ntot;
+          }
+        }
+      }
+      __syncthreads();
+      ++xr;
+      bool uerr = S.rg[0].err || (paired && S.rg[1].err);
+      if (!uerr) {
+        // rows that need bins: merge them; rows whose bins must be (re)computed
+        // in the cluster frame (extreme) or with counts (overflowing lists) get
+        // one more exchange round
+        // (both rows of a unit share their parameters, so both list or neither;
+        // if either list overflowed, both rows take the general path and no CTA
+        // reads another's lists)
+        const bool lists_over = S.rg[0].mode == RM_LIST &&
+                                (S.res_i[2] < 0 || (paired && S.res_i[3] < 0));
+        bool redo = false;
+        for (int rho = 0; rho < nr; ++rho) {
+          RowG& g = S.rg[rho];
+          const bool was_list = g.mode == RM_LIST;
+          __syncthreads();
+          if (tid == 0) S.res_i[2 + rho] = (was_list && lists_over) ? -1 : S.res_i[2 + rho];
+          if (tid == 0 && was_list && lists_over) g.mode = RM_GENERAL;
+          __syncthreads();
+          if (g.mode == RM_LIST) continue;
+          if (g.extreme || (was_list && lists_over)) redo = true;
+          else merge_bins(S, &X[rho], rho, C, false, gbuf, reinterpret_cast<uint32_t*>(gbuf + 16 * NB));
+        }
+        if (redo) {
+          X1Row* X2_ = S.x1[xr & 1];
+          for (int rho = 0; rho < nr; ++rho) {
+            RowG& g = S.rg[rho];
+            const bool need = g.mode != RM_LIST && (g.extreme || S.res_i[2 + rho] < 0);
+            if (tid < NB) {
+              X2_[rho].bins[tid] = 0ull;
+              X2_[rho].cnts[tid] = 0u;
+            }
+            if (tid == 0) {
+              X2_[rho].m = g.mg;
+              X2_[rho].flags = 0;
+              X2_[rho].R = g.Rl;
+              X2_[rho].ncand = 0;
+            }
+            __syncthreads();
+            if (need && (g.extreme || g.Rl > -INFINITY)) {
+              if (g.mode == RM_GENERAL) pass_bins<DT, true>(sl[rho], nvec, vlen, g, hist, hcnt, X2_[rho]);
+              else pass_bins<DT, false>(sl[rho], nvec, vlen, g, hist, hcnt, X2_[rho]);
+            }
+            __syncthreads();
+          }
+          cluster_sync();                                          // S1b
+          for (int rho = 0; rho < nr; ++rho) {
+            RowG& g = S.rg[rho];
+            const bool need = g.mode != RM_LIST && (g.extreme || S.res_i[2 + rho] < 0);
+            if (need)
+              merge_bins(S, &X2_[rho], rho, C, g.extreme != 0, gbuf,
+                         reinterpret_cast<uint32_t*>(gbuf + 16 * NB));
+          }
+          ++xr;
+        }
+        // selection set-up
+        for (int rho = 0; rho < nr; ++rho) {
+          RowG& g = S.rg[rho];
+          if (g.mode == RM_LIST) {
+            list_select<DT>(S, g, rho, lists, C, (uint32_t)S.res_i[2 + rho], P.slice, gbuf);
+            continue;
+          }
+          if (tid == 0) {
+            unsigned long long Z = 0;
+            for (int q = 0; q < NB; ++q) Z += S.gb[rho][q];
+            g.Z = Z;
+            if (g.mode == RM_ALL) {
+              g.zt = -INFINITY;
+              g.idcut = INT_MAX;
+              g.Zk = Z;
+              g.stage = ST_DONE;
+            } else if (g.mode == RM_TOPP) {
+              g.tkind = T_MASS;
+              g.Y = mass_threshold(g.P, Z);
+              ebin_pick<DT>(S, g, rho);
+            } else {
+              g.tkind = T_COUNT;
+              g.need = (unsigned long long)g.kk;
+              g.then_mass = g.P < 1.0f;
+              ebin_pick<DT>(S, g, rho);
+            }
+          }
+          __syncthreads();
+        }
+        SV_MARK(4);
+        // refinement levels (one cluster barrier each)
+        while (true) {
+          const bool k0 = S.rg[0].stage == ST_KEYS && !S.rg[0].err;
+          const bool k1 = paired && S.rg[1].stage == ST_KEYS && !S.rg[1].err;
+          if (!k0 && !k1) break;
+          X2Row* xl = x2 + (lp & 1) * 2;
+          for (int rho = 0; rho < nr; ++rho) {
+            if (rho == 0 ? !k0 : !k1) continue;
+            for (int q = tid; q < NSUB; q += NT) {
+              xl[rho].cnt[q] = 0u;
+              xl[rho].mass[q] = 0ull;
+            }
+          }
+          if (tid < 2) S.list_n[tid] = 0u;
+          __syncthreads();
+          for (int rho = 0; rho < nr; ++rho) {
+            if (rho == 0 ? !k0 : !k1) continue;
+            pass_level<DT>(sl[rho], nvec, vlen, S.rg[rho], &xl[rho], Gr + (size_t)rho * (G_BYTES / 2),
+                           &S.list_n[rho], (int)(G_BYTES / 2));
+          }
+          __syncthreads();
+          // single-key sub-bins: mass = count * this CTA's weight of that key
+          for (int rho = 0; rho < nr; ++rho) {
+            if (rho == 0 ? !k0 : !k1) continue;
+            const RowG& g = S.rg[rho];
+            if (g.kshift == 0 && tid < g.nsub) {
+              const uint32_t n = xl[rho].cnt[tid];
+              if (n) {
+                const float zk = Lg<DT>::key_float(g.klo + (uint32_t)tid);
+                xl[rho].mass[tid] = (unsigned long long)n * fix_of(zk, g, g.Rl);
+              }
+            }
+          }
+          SV_MARK(13);
+          cluster_sync();                                          // S2 (per level)
+          SV_MARK(14);
+          for (int rho = 0; rho < nr; ++rho) {
+            if (rho == 0 ? !k0 : !k1) continue;
+            level_pick<DT>(S, S.rg[rho], rho, &xl[rho], C, rank, Gr);
+          }
+          ++lp;
+#ifdef SV_TRACE
+          if (cid == 0 && rank == 0 && threadIdx.x == 0 && j < 64) g_trace[j * 16 + 10] = (unsigned long long)lp;
+#endif
+        }
+        uerr = S.rg[0].err || (paired && S.rg[1].err);
+        SV_MARK(5);
+      }
+      if (uerr) {
+        if (MODE == MODE_VERIFY) {
+          if (rank == 0 && tid == 0) publish_unit(P, u, b, -1, false, true);
+        } else if (MODE == MODE_SAMPLE) {
+          if (rank == 0 && tid == 0) P.out_tokens[(size_t)b * P.K + i] = -1;
+        } else {
+          for (int l = tid; l < vlen; l += NT) P.out_probs[(size_t)b * P.V + base + l] = __int_as_float(0x7fc00000);
+        }
+        cluster_sync();                                            // end of unit
+      } else {
+        // ---------------------------------------------- phase D
+        if (tid == 0) {
+          for (int rho = 0; rho < nr; ++rho) {
+            RowG& g = S.rg[rho];
+            g.invZ = __fdiv_rn(17592186044416.0f, (float)(g.Zk ? g.Zk : 1ull));   // 2^44 / Zk
+          }
+        }
+        __syncthreads();
+        for (int rho = 0; rho < nr; ++rho)
+          if (S.rg[rho].partial) tie_pass<DT>(S, S.rg[rho], sl[rho], P.ept, vlen, base);
+        __syncthreads();
+        SV_MARK(12);
+        const RowG& g0 = S.rg[0];
+        const RowG& g1 = S.rg[paired ? 1 : 0];
+        if (MODE == MODE_PROBS) {
+          write_probs<DT>(sl[0], g0, vlen, base, P.out_probs + (size_t)b * P.V);
+          cluster_sync();                                          // end of unit
+        } else {
+          uint32_t ku, kv;
+          philox_uniform_bits(P.seed, P.offset, (uint32_t)b, (uint32_t)i, &ku, &kv);
+          if (tid == 0) {
+            uint32_t flag = 0;
+            if (paired && m.d / P.slice == (int)rank) {
+              const int l = m.d - base;
+              const float zp = Lg<DT>::at(sl[0], l), zq = Lg<DT>::at(sl[1], l);
+              const float p = kept(zp, m.d, g0.zt, g0.idcut) ? __fmul_rn(wacc(zp, g0), g0.invZ) : 0.0f;
+              const float q = kept(zq, m.d, g1.zt, g1.idcut) ? __fmul_rn(wacc(zq, g1), g1.invZ) : 0.0f;
+              flag = __fmul_rn((float)ku * 5.9604644775390625e-08f, q) < p ? 1u : 0u;
+            }
+            S.x3.flag = flag;
+          }
+          const int l0 = min(tid * P.ept, vlen), l1 = min(l0 + P.ept, vlen);
+          unsigned long long Rt, Pt;
+          sample_range<DT>(sl[0], sl[1], paired, g0, g1, l0, l1, base, &Rt, &Pt);
+          __syncthreads();
+          SV_MARK(15);
+          unsigned long long totR, totP;
+          const unsigned long long exR = block_excl_scan<unsigned long long>(Rt, S.scan64, &totR);
+          const unsigned long long exP = block_excl_scan<unsigned long long>(Pt, S.scan64b, &totP);
+          if (tid == 0) {
+            S.x3.R = totR;
+            S.x3.P = totP;
+          }
+          SV_MARK(6);
+          cluster_sync();                                          // S3
+          SV_MARK(7);
+          if (warp_id() == 0) {
+            const int l = lane_id();
+            unsigned long long r = 0, p = 0;
+            if (l < C) {
+              r = ld_peer_u64(&S.x3.R, l);
+              p = ld_peer_u64(&S.x3.P, l);
+            }
+            unsigned long long ir = r, ip = p;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const unsigned long long a = __shfl_up_sync(0xffffffffu, ir, o);
+              const unsigned long long c2 = __shfl_up_sync(0xffffffffu, ip, o);
+              if (l >= o) {
+                ir += a;
+                ip += c2;
+              }
+            }
+            const unsigned long long SR = __shfl_sync(0xffffffffu, ir, 31);
+            const unsigned long long SP = __shfl_sync(0xffffffffu, ip, 31);
+            const bool useR = SR > 0ull;
+            const unsigned long long Stot = useR ? SR : SP;
+            const unsigned long long inc = useR ? ir : ip, own = useR ? r : p;
+            const bool cross = l < C && mul_gt(inc, 1ull << 24, kv, Stot) &&
+                               !mul_gt(inc - own, 1ull << 24, kv, Stot);
+            const uint32_t bal = __ballot_sync(0xffffffffu, cross);
+            const int cs = bal ? __ffs(bal) - 1 : C - 1;
+            if (l == cs) {
+              S.res_i[4] = cs;
+              S.res_i[5] = useR;
+              S.res_i[6] = bal ? 1 : 0;
+              S.res_u[0] = inc - own;
+              S.res_u[1] = Stot;
+            }
+          }
+          __syncthreads();
+          if (S.res_i[4] == (int)rank) {
+            const bool useR = S.res_i[5] != 0;
+            const unsigned long long Stot = S.res_u[1];
+            const unsigned long long ex = S.res_u[0] + (useR ? exR : exP);
+            const unsigned long long own = useR ? Rt : Pt;
+            const bool mine = S.res_i[6] && mul_gt(ex + own, 1ull << 24, kv, Stot) &&
+                              !mul_gt(ex, 1ull << 24, kv, Stot);
+            if (tid == 0) S.res_i[7] = -1;
+            __syncthreads();
+            if (mine) {
+              S.res_i[7] = tid;
+              S.res_u[2] = ex;
+            }
+            __syncthreads();
+            const int ts = S.res_i[7];
+            if (warp_id() == 0) {
+              int tok = -1;
+              if (ts >= 0) {
+                const int a0 = min(ts * P.ept, vlen), a1 = min(a0 + P.ept, vlen);
+                tok = warp_sample_find<DT>(sl[0], sl[1], paired, g0, g1, a0, a1, base, S.res_u[2],
+                                           useR, kv, Stot);
+              }
+              if (tid == 0) {
+                if (MODE == MODE_VERIFY) {
+                  bool flag = false;
+                  if (paired) flag = ld_peer_u32(&S.x3.flag, (uint32_t)(m.d / P.slice)) != 0u;
+                  publish_unit(P, u, b, tok, flag, tok < 0);
+                } else {
+                  P.out_tokens[(size_t)b * P.K + i] = tok;
+                }
+              }
+            }
+          }
+          // X3 is read by peers until their next cluster barrier; it is written
+          // again only after the next unit's first barrier
         }
       }
     }
-    xb ^= 1;
     __syncthreads();
-  }
-
-  // ------------------------------------- single-value ranges: split by id
-  {
-    bool want[2] = {false, false};
-    uint32_t tthr[2] = {0, 0};
-    unsigned int tgt[2] = {0, 0};
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      want[r] = r < nrows && W.rk[r].need == ND_TIE;
-      tthr[r] = W.rk[r].thr;
-      tgt[r] = W.rk[r].jt - 1;
-    }
-    if (want[0] || want[1]) {
-      int found[2];
-      tie_split<DT>(want, tthr, tgt, rb0, rb1, j0, j1, v0, kmask, W, xb, C, rank, found);
-      if (tid < 2 && want[tid]) {
-        W.rk[tid].tie = found[tid];
-        W.rk[tid].need = ND_DONE;
-      }
-      __syncthreads();
-    }
-  }
-
-  // ---------------------------------------------- lists -> selecting CTA
-  bool general = general_k;
-#pragma unroll
-  for (int r = 0; r < 2; ++r)
-    if (r < nrows && (W.rk[r].need == ND_GENERAL || W.rk[r].need == ND_REFINE)) general = true;
-  if (!general) {
-    // list the range of rows whose cut lies in a tail range
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      if (r >= nrows || W.rk[r].need != ND_LIST || W.rk[r].lev < 0) continue;
-      if (tid == 0) W.lcnt[r] = 0;
-      __syncthreads();
-      list_range_row<DT>(r == 0 ? rb0 : rb1, j0, j1, ept, r == 0 ? rw0 : rw1, W.rk[r].q,
-                         pow16(W.rk[r].lev), W.list[r], &W.lcnt[r]);
-    }
-    __syncthreads();
-    // push the entries into CTA 0's gather buffer (the union is free there:
-    // CTA 0 finished its histograms before the last cluster barrier)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      if (r >= nrows || W.rk[r].need != ND_LIST) continue;
-      unsigned int off = 0;
-      for (uint32_t c = 0; c < rank; ++c) off += W.rk[r].rc[c];
-      const unsigned int cnt = min(W.rk[r].rc[rank], (unsigned int)LCAP);
-      const unsigned char* rb = r == 0 ? rb0 : rb1;
-      for (unsigned int t = tid; t < cnt; t += NT) {
-        const int j = W.list[r][t];
-        const uint32_t key = mkey(ld_logit<DT>(rb, j), kmask);
-        const uint32_t id = (uint32_t)(v0 + j);
-        st_peer_u64(&W.u.g[r][off + t], 0, ((unsigned long long)key << 32) | (unsigned long long)(~id));
-      }
-    }
-    cluster_sync();   // entries in place
-    if (rank == 0) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        if (r >= nrows || W.rk[r].need != ND_LIST) continue;
-        unsigned int tot = 0;
-        for (uint32_t c = 0; c < C; ++c) tot += W.rk[r].rc[c];
-        local_select(W.u.g[r], (int)tot, W.rk[r], fscale, kmask, W.scan64, &W.res_thr[r],
-                     &W.res_tie[r], &W.res_zl[r], &W.res_fail[r]);
-      }
-    }
-    cluster_sync();   // results in place at CTA 0
-    if (tid < nrows && W.rk[tid].need == ND_LIST) {
-      const int r = tid;
-      RowK& rk = W.rk[r];
-      rk.thr = ld_peer_u32(&W.res_thr[r], 0);
-      rk.tie = (int)ld_peer_u32(&W.res_tie[r], 0);
-      rk.ZL = ld_peer_u64(&W.res_zl[r], 0);
-      rk.need = ld_peer_u32(&W.res_fail[r], 0) ? ND_GENERAL : ND_DONE;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-      if (r < nrows && W.rk[r].need == ND_GENERAL) general = true;
-  }
-  SV_MARK(6);
+    rows_done += nr;
+    SV_MARK(8);
 #ifdef SV_TRACE
-  if (tid == 0 && rank == 0 && unit < 256) {
-    g_trace[unit * 16 + 10] = (unsigned long long)W.rk[0].need | ((unsigned long long)(W.rk[0].lev + 1) << 8) |
-                              ((unsigned long long)W.rk[0].q << 16);
-    g_trace[unit * 16 + 11] = (unsigned long long)W.rk[1].need | ((unsigned long long)(W.rk[1].lev + 1) << 8) |
-                              ((unsigned long long)W.rk[1].q << 16);
-    g_trace[unit * 16 + 12] = (unsigned long long)W.rk[1].mode | ((unsigned long long)W.rk[0].mode << 8);
+    if (cid == 0 && rank == 0 && threadIdx.x == 0 && j < 64) g_trace[j * 16 + 9] = (unsigned long long)nr;
+#endif
+  }
+#ifdef SV_TRACE
+  if (cid == 0 && rank == 0 && threadIdx.x == 0) {
+    g_trace[64 * 16] = (unsigned long long)ncl;
+    g_trace[64 * 16 + 1] = (unsigned long long)nmine;
   }
 #endif
-
-  // ------------------------------------------------- general selection path
-  if (general) {
-    const bool topp_on = topp < 1.0f;
-    const bool any_sel = topk_on || topp_on;
-    uint32_t gtau[2] = {KEY_ALL, KEY_ALL};
-    if (topk_on) {
-      if (kk <= NT) {
-        gtau[0] = W.rk[0].tau;
-        gtau[1] = W.rk[1].tau;
-      }
-    } else if (topp_on) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        // eligibility: within ln(V/(1-top_p)) + 0.05 nats of the maximum
-        const float taud = logf((float)V / (1.0f - topp)) + 0.05f;
-        const float zt = (r == 0 ? rw0.m : rw1.m) - taud * T;
-        gtau[r] = isfinite(zt) ? mkey(zt, kmask) : KEY_ALL;
-      }
+  // copies still in flight after a timeout: wait (bounded) before leaving
+  if (tid == 0 && S.timeout && P.bulk_ok) {
+    for (int s = 0; s < P.NS && s < rows_issued; ++s) {
+      const int last = s + ((rows_issued - 1 - s) / P.NS) * P.NS;   // last fill of slot s
+      mbar_wait_bounded(&S.full[s], (uint32_t)((last / P.NS) & 1), WAIT_LIMIT_NS);
     }
-    uint32_t tk[2] = {0, 0};
-    unsigned int jk[2] = {0, 0};
-    unsigned long long Etk[2] = {0, 0};
-    double Z1[2] = {0, 0};
-    uint32_t thr[2] = {KEY_ALL, KEY_ALL};
-    unsigned int jt[2] = {0, 0}, neq_all[2] = {0, 0};
-    unsigned long long ZL[2] = {0, 0};
-    for (int stage = 0; stage < 2 && any_sel; ++stage) {
-      const bool by_mass = (stage == 1);
-      if (stage == 0 && !topk_on) continue;
-      if (stage == 1 && !topp_on) continue;
-      uint32_t prefix[2] = {0, 0}, pmask = 0;
-      unsigned int cabove[2] = {0, 0};
-      unsigned long long mabove[2] = {0, 0};
-      double need_m[2] = {0, 0};
-      unsigned int lastcnt[2] = {0, 0};
-      for (int lev = 0; lev < P.nlev; ++lev) {
-        const int shift = 24 - 8 * lev;
-        const int buf = xb;
-        xb ^= 1;
-        for (int t = tid; t < 2 * 256; t += NT) {
-          W.u.gp.hcnt[buf][t >> 8][t & 255] = 0;
-          W.u.gp.hmass[buf][t >> 8][t & 255] = 0;
-        }
-        __syncthreads();
-        float zfar[2] = {0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          if (r >= nrows) continue;
-          const unsigned char* rb = r == 0 ? rb0 : rb1;
-          const RowW w = r == 0 ? rw0 : rw1;
-          for (int j = j0; j < j1; ++j) {
-            const float z = ld_logit<DT>(rb, j);
-            const uint32_t key = mkey(z, kmask);
-            bool in;
-            if (stage == 0) {
-              in = key >= gtau[r];
-            } else if (topk_on) {
-              in = key > tk[r];                   // the tie group at tk enters as one pseudo token
-            } else {
-              in = key >= gtau[r];
-              if (!in && lev == 0) zfar[r] += hweight(z, w);
-            }
-            if (in && (key & pmask) == prefix[r]) {
-              const unsigned int dg = (key >> shift) & 255u;
-              atomicAdd(&W.u.gp.hcnt[buf][r][dg], 1u);
-              const unsigned long long E = to_fixed(hweight(z, w), fscale);
-              if (E) atomicAdd(&W.u.gp.hmass[buf][r][dg], E);
-            }
-          }
-        }
-        if (stage == 1 && topk_on && rank == 0 && tid == 0) {
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-            if (r < nrows && (tk[r] & pmask) == prefix[r]) {
-              const unsigned int dg = (tk[r] >> shift) & 255u;
-              atomicAdd(&W.u.gp.hcnt[buf][r][dg], jk[r]);
-              atomicAdd(&W.u.gp.hmass[buf][r][dg], (unsigned long long)jk[r] * Etk[r]);
-            }
-        }
-        if (stage == 1 && !topk_on && lev == 0) {
-          const unsigned long long zf0 = block_sum<unsigned long long>(to_fixed(zfar[0], fscale), W.scan64);
-          const unsigned long long zf1 = block_sum<unsigned long long>(to_fixed(zfar[1], fscale), W.scan64);
-          if (tid == 0) {
-            W.xs[buf][0] = zf0;
-            W.xs[buf][1] = zf1;
-          }
-        }
-        __syncthreads();
-        cluster_sync();
-        for (int t = tid; t < 2 * 256; t += NT) {
-          const int r = t >> 8, dg = t & 255;
-          if (r < nrows) {
-            unsigned int c = 0;
-            unsigned long long w = 0;
-            for (uint32_t q = 0; q < C; ++q) {
-              c += ld_peer_u32(&W.u.gp.hcnt[buf][r][dg], q);
-              w += ld_peer_u64(&W.u.gp.hmass[buf][r][dg], q);
-            }
-            W.u.gp.gcnt[r][dg] = c;
-            W.u.gp.gmass[r][dg] = w;
-          }
-        }
-        if (stage == 1 && !topk_on && lev == 0 && tid < nrows) {
-          unsigned long long zf = 0;
-          for (uint32_t q = 0; q < C; ++q) zf += ld_peer_u64(&W.xs[buf][tid], q);
-          W.bu[2 + tid] = zf;
-        }
-        __syncthreads();
-        if (stage == 1 && lev == 0) {
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            if (r >= nrows) continue;
-            if (!topk_on) {
-              unsigned long long s = 0;
-              for (int dg = 0; dg < 256; ++dg) s += W.u.gp.gmass[r][dg];
-              Z1[r] = (double)(s + W.bu[2 + r]);
-            }
-            need_m[r] = (double)topp * Z1[r];
-          }
-        }
-        if (warp_id() < nrows) {
-          const int r = warp_id();
-          const unsigned int need_c =
-              stage == 0 ? (unsigned int)kk - (r == 0 ? cabove[0] : cabove[1]) : 0u;
-          const double need_mr =
-              r == 0 ? need_m[0] - (double)mabove[0] : need_m[1] - (double)mabove[1];
-          const DigitPick pk =
-              pick_digit(W.u.gp.gcnt[r], W.u.gp.gmass[r], by_mass, need_c, need_mr);
-          if (lane_id() == 0) {
-            W.bi[r] = pk.digit;
-            W.bi[2 + r] = (int)pk.cnt_above;
-            W.bu[r] = pk.mass_above;
-            W.bi[4 + r] = (int)W.u.gp.gcnt[r][pk.digit];
-          }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          if (r >= nrows) continue;
-          prefix[r] |= (uint32_t)W.bi[r] << shift;
-          cabove[r] += (unsigned int)W.bi[2 + r];
-          mabove[r] += W.bu[r];
-          lastcnt[r] = (unsigned int)W.bi[4 + r];
-        }
-        pmask |= 255u << shift;
-        __syncthreads();
-      }
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        if (r >= nrows) continue;
-        const unsigned long long Et =
-            to_fixed(hweight(mkey_to_float(prefix[r], kmask), r == 0 ? rw0 : rw1), fscale);
-        if (stage == 0) {
-          tk[r] = prefix[r];
-          jk[r] = (unsigned int)kk - cabove[r];
-          Etk[r] = Et;
-          Z1[r] = (double)(mabove[r] + (unsigned long long)jk[r] * Et);
-          thr[r] = tk[r];
-          jt[r] = jk[r];
-          neq_all[r] = lastcnt[r];
-          ZL[r] = mabove[r] + (unsigned long long)jk[r] * Et;
-        } else {
-          const double gap = need_m[r] - (double)mabove[r];
-          const double jf = Et > 0 ? ceil(gap / (double)Et) : 1.0;
-          const unsigned int j = (unsigned int)fmax(1.0, fmin(jf, (double)lastcnt[r]));
-          thr[r] = prefix[r];
-          jt[r] = j;
-          neq_all[r] = (topk_on && prefix[r] == tk[r]) ? neq_all[r] : lastcnt[r];
-          ZL[r] = mabove[r] + (unsigned long long)j * Et;
-        }
-      }
-    }
-    // tie split by token id
-    bool need_tie[2] = {false, false};
-#pragma unroll
-    for (int r = 0; r < 2; ++r) need_tie[r] = r < nrows && any_sel && jt[r] < neq_all[r];
-    int tie_res[2] = {NO_TIE, NO_TIE};
-    if (need_tie[0] || need_tie[1]) {
-      const unsigned int tgt[2] = {jt[0] - 1, jt[1] - 1};
-      tie_split<DT>(need_tie, thr, tgt, rb0, rb1, j0, j1, v0, kmask, W, xb, C, rank, tie_res);
-    }
-    __syncthreads();
-    if (tid < nrows) {
-      const int r = tid;
-      RowK& rk = W.rk[r];
-      if (any_sel) {
-        rk.thr = r == 0 ? thr[0] : thr[1];
-        rk.ZL = r == 0 ? ZL[0] : ZL[1];
-        rk.tie = (r == 0 ? need_tie[0] : need_tie[1]) ? (r == 0 ? tie_res[0] : tie_res[1]) : NO_TIE;
-      } else {
-        rk.thr = KEY_ALL;
-        rk.tie = NO_TIE;
-      }
-    }
-    __syncthreads();
   }
-  SV_MARK(7);
-
-  uint32_t thr[2];
-  int tie[2];
-  unsigned long long ZL[2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    thr[r] = W.rk[r].thr;
-    tie[r] = W.rk[r].tie;
-    ZL[r] = W.rk[r].ZL;
-  }
-  auto kept = [&](int r, float z, int id) -> bool {
-    const uint32_t key = mkey(z, kmask);
-    const uint32_t t = r == 0 ? thr[0] : thr[1];
-    const int ti = r == 0 ? tie[0] : tie[1];
-    return key > t || (key == t && id <= ti);
-  };
-
-  // --------------------------------------------------- probabilities hook
-  if (MODE == MODE_PROBS) {
-    float* out = P.out_probs + (size_t)unit * V + v0;
-    if (tid == 0) W.bu[0] = __double_as_longlong(1.0 / (double)ZL[0]);
-    __syncthreads();
-    const double inv = __longlong_as_double((long long)W.bu[0]);
-    for (int j = tid; j < n; j += NT) {
-      const float z = ld_logit<DT>(rb0, j);
-      float pr = 0.0f;
-      if (kept(0, z, v0 + j)) pr = (float)((double)to_fixed(hweight(z, rw0), fscale) * inv);
-      out[j] = pr;
-    }
-    cluster_sync();
-    return;
-  }
-
-  // ------------------------------------------------------------ acceptance
-  bool flag = false;
-  uint32_t ku, kv;
-  philox_uniform_bits(P.seed, P.offset, (uint32_t)b, (uint32_t)i, &ku, &kv);
-  const bool residual = (MODE == MODE_VERIFY && i < P.K);
-  if (residual) {
-    if (tid == 0) {
-      const uint32_t owner = (uint32_t)(dtok / P.slice);
-      const int jj = dtok - (int)owner * P.slice;
-      double pq[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const float z = ld_peer_logit<DT>(r == 0 ? sb0 : sb1, jj, owner);
-        pq[r] = kept(r, z, dtok)
-                    ? (double)to_fixed(hweight(z, r == 0 ? rw0 : rw1), fscale) /
-                          (double)(r == 0 ? ZL[0] : ZL[1])
-                    : 0.0;
-      }
-      W.bi[0] = ((double)ku * 5.9604644775390625e-08 * pq[1] < pq[0]) ? 1 : 0;
-      W.bu[0] = __float_as_uint((float)((double)fscale / (double)ZL[0]));
-      W.bu[1] = __float_as_uint((float)((double)fscale / (double)ZL[1]));
-    }
-    __syncthreads();
-    flag = W.bi[0] != 0;
-  }
-  const float sp = residual ? __uint_as_float((uint32_t)W.bu[0]) : 0.f;
-  const float sq = residual ? __uint_as_float((uint32_t)W.bu[1]) : 0.f;
-
-  // ------------------------------------------- inverse-CDF in token-id order
-  auto wgt = [&](int j, bool res) -> unsigned long long {
-    const float z = ld_logit<DT>(rb0, j);
-    if (!kept(0, z, v0 + j)) return 0ull;
-    const float ep = hweight(z, rw0);
-    if (!res) return to_fixed(ep, fscale);
-    const float zq = ld_logit<DT>(rb1, j);
-    // rounded products and difference (no FMA contraction): identical rows give d == 0
-    const float q = kept(1, zq, v0 + j) ? __fmul_rn(hweight(zq, rw1), sq) : 0.0f;
-    const float d = __fsub_rn(__fmul_rn(ep, sp), q);
-    return d > 0.0f ? __float2ull_rz(d * 4611686018427387904.0f) : 0ull;
-  };
-  bool use_res = residual;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    unsigned long long s = 0;
-    for (int j = j0; j < j1; ++j) s += wgt(j, use_res);
-    unsigned long long ctot;
-    const unsigned long long texcl = block_excl_scan<unsigned long long>(s, W.scan64, &ctot);
-    const int buf = xb;
-    xb ^= 1;
-    if (tid == 0) W.xs[buf][0] = ctot;
-    __syncthreads();
-    cluster_sync();
-    unsigned long long off = 0, S = 0;
-    for (uint32_t q = 0; q < C; ++q) {
-      const unsigned long long t = ld_peer_u64(&W.xs[buf][0], q);
-      if (q < rank) off += t;
-      S += t;
-    }
-    if (S == 0 && use_res) {       // (p - q)+ has no mass: sample from p
-      use_res = false;
-      continue;
-    }
-    const unsigned long long lo = off + texcl, hi = lo + s;
-    const unsigned long long kvs = (unsigned long long)kv;
-    if (s > 0 && !mul_gt(lo, 1ull << 24, kvs, S) && mul_gt(hi, 1ull << 24, kvs, S)) {
-      unsigned long long run = lo;
-      int tok = v0 + j1 - 1;
-      for (int j = j0; j < j1; ++j) {
-        run += wgt(j, use_res);
-        if (mul_gt(run, 1ull << 24, kvs, S)) {
-          tok = v0 + j;
-          break;
-        }
-      }
-      if (MODE == MODE_SAMPLE) P.out_tokens[unit] = tok;
-      else publish_unit(P, unit, b, tok, flag, false);
-    }
-    break;
-  }
-  SV_MARK(8);
-  cluster_sync();   // keep this CTA's shared memory alive until every peer is done
-  SV_MARK(9);
+  __syncthreads();
+  cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
 
 __global__ void philox_kernel(uint64_t seed, uint64_t offset, int B, int K1, uint32_t* out) {
@@ -1562,70 +1669,82 @@ __global__ void philox_kernel(uint64_t seed, uint64_t offset, int B, int K1, uin
 }
 
 // ------------------------------------------------------------------ host
-template <typename DT, int MODE>
-cudaError_t launch(const Params& p, int C, size_t smem, cudaStream_t st) {
-  auto kern = sv_kernel<DT, MODE>;
-  static size_t configured = 0;      // largest dynamic shared memory set so far
-  static bool nonportable = false;
-  cudaError_t e;
-  if (smem > configured) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
+struct Geometry {
+  int C, slice, ept, slot_elems, NS;
+  size_t smem;
+};
+
+// Cluster size: the smallest C (1..16) whose row slice fits a ~20 KB slot, else
+// 16. Four slots (two paired units) when two CTAs fit an SM, else as many as
+// fit one CTA per SM.
+static Geometry geometry(int V, int es) {
+  Geometry g{};
+  const size_t fixed = SHARED_BYTES + H_BYTES + G_BYTES;
+  for (int C = 1; C <= 16; ++C) {
+    int slice = (V + C - 1) / C;
+    slice = (slice + 7) & ~7;
+    if ((long long)(C - 1) * slice >= V) continue;
+    int per = (slice + NT - 1) / NT;
+    int words = (per * es + 3) / 4;
+    words |= 1;                                   // odd word stride: no bank conflicts
+    const int ept = words * 4 / es;
+    const size_t slot = (size_t)NT * ept * es;
+    g.C = C;
+    g.slice = slice;
+    g.ept = ept;
+    g.slot_elems = NT * ept;
+    if (slot <= 20 * 1024 || C == 16) break;
   }
-  if (C > 8 && !nonportable) {
+  const size_t slot = (size_t)g.slot_elems * es;
+  g.NS = NSMAX;
+  while (g.NS > 2 && fixed + g.NS * slot > 227 * 1024) --g.NS;
+  g.smem = fixed + (size_t)g.NS * slot;
+  if (g.smem > 227 * 1024 || g.ept > 255) g.smem = 0;
+  return g;
+}
+
+template <typename DT, int MODE>
+static cudaError_t launch(const Params& p, const Geometry& g, cudaStream_t st) {
+  auto kern = sv_kernel<DT, MODE>;
+  static size_t configured = 0;
+  static int cached_C = 0;
+  static size_t cached_smem = 0;
+  static int cached_dev = -1;
+  static int max_clusters = 0;
+  cudaError_t e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (g.smem > configured) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    nonportable = true;
+    configured = g.smem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.nunits * C), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = g.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.x = (unsigned)g.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
-struct Geometry {
-  int C, slice, ept;
-  size_t smem;
-};
-
-// Smallest cluster (1..16 CTAs) whose per-CTA share of two rows keeps the
-// footprint near 72 KB (three CTAs per SM), else the largest that fits.
-static Geometry geometry(int V, int es) {
-  Geometry g{};
-  const size_t target = 72 * 1024, hard = 227 * 1024;
-  for (int C = 1; C <= 16; C *= 2) {
-    int slice = (V + C - 1) / C;
-    slice = (slice + 15) & ~15;
-    const size_t rb = ((size_t)slice * es + 15) & ~(size_t)15;
-    const size_t smem = 2 * rb + sizeof(Work);
-    g.C = C;
-    g.slice = slice;
-    g.smem = smem;
-    if (smem <= target) break;
-    if (C == 16 && smem > hard) g.smem = 0;   // does not fit: reported as a shape error
+  if (cached_C != g.C || cached_smem != g.smem || cached_dev != dev) {
+    cfg.gridDim = dim3((unsigned)g.C, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = n > 0 ? n : 1;
+    cached_C = g.C;
+    cached_smem = g.smem;
+    cached_dev = dev;
   }
-  // contiguous per-thread ranges with an odd number of 32-bit words (bank spread)
-  int per = (g.slice + NT - 1) / NT;
-  int words = (per * es + 3) / 4;
-  words |= 1;
-  g.ept = words * 4 / es;
-  return g;
-}
-
-static int fix_scale_shift(int V) {
-  int lg = 0;
-  while ((1ll << lg) < (long long)V) ++lg;
-  return 63 - lg;
+  const int ncl = min(max_clusters, p.nunits);
+  cfg.gridDim = dim3((unsigned)(ncl * g.C), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace sv
@@ -1642,24 +1761,24 @@ static bool fill_geometry(Params& p, int V, sv_dtype dt, Geometry* g) {
   const int es = dt == SV_BF16 ? 2 : 4;
   *g = geometry(V, es);
   p.V = V;
+  p.C = g->C;
   p.slice = g->slice;
   p.ept = g->ept;
-  p.nlev = dt == SV_BF16 ? 2 : 4;
-  p.keymask = dt == SV_BF16 ? 0xFFFF0000u : 0xFFFFFFFFu;
-  p.fix_scale = ldexpf(1.0f, fix_scale_shift(V));
+  p.slot_elems = g->slot_elems;
+  p.NS = g->NS;
   return g->smem != 0;
 }
 
 static sv_status do_launch(int mode, sv_dtype dt, const Params& p, const Geometry& g, cudaStream_t st) {
   cudaError_t e;
   if (dt == SV_BF16) {
-    if (mode == MODE_VERIFY) e = launch<__nv_bfloat16, MODE_VERIFY>(p, g.C, g.smem, st);
-    else if (mode == MODE_PROBS) e = launch<__nv_bfloat16, MODE_PROBS>(p, g.C, g.smem, st);
-    else e = launch<__nv_bfloat16, MODE_SAMPLE>(p, g.C, g.smem, st);
+    if (mode == MODE_VERIFY) e = launch<__nv_bfloat16, MODE_VERIFY>(p, g, st);
+    else if (mode == MODE_PROBS) e = launch<__nv_bfloat16, MODE_PROBS>(p, g, st);
+    else e = launch<__nv_bfloat16, MODE_SAMPLE>(p, g, st);
   } else {
-    if (mode == MODE_VERIFY) e = launch<float, MODE_VERIFY>(p, g.C, g.smem, st);
-    else if (mode == MODE_PROBS) e = launch<float, MODE_PROBS>(p, g.C, g.smem, st);
-    else e = launch<float, MODE_SAMPLE>(p, g.C, g.smem, st);
+    if (mode == MODE_VERIFY) e = launch<float, MODE_VERIFY>(p, g, st);
+    else if (mode == MODE_PROBS) e = launch<float, MODE_PROBS>(p, g, st);
+    else e = launch<float, MODE_SAMPLE>(p, g, st);
   }
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
@@ -1795,11 +1914,16 @@ const char* sv_status_string(sv_status status) {
   return "unknown status";
 }
 
-int sv_version(void) { return 200; }
+int sv_version(void) { return 300; }
 
 #ifdef SV_TRACE
+int sv_trace_reset(void) {
+  static unsigned long long zero[64 * 16 + 16];
+  return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
+}
 int sv_trace_copy(unsigned long long* host, size_t n) {
-  return (int)cudaMemcpyFromSymbol(host, sv::g_trace, n * sizeof(unsigned long long));
+  if (n > 64 * 16 + 16) n = 64 * 16 + 16;
+  return cudaMemcpyFromSymbol(host, g_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
 }
 #endif
 

@@ -2,8 +2,8 @@
 //
 // Thread-block clusters and distributed shared memory (DSMEM), mbarrier-tracked
 // bulk copies (the non-tensor TMA path) with bounded waits, Philox4x32-10,
-// order-preserving logit keys, fixed-point weights, and deterministic
-// block-level reductions and scans.
+// order-preserving logit keys, the exponent-binned softmax weights, exact
+// fixed-point comparisons, and deterministic block-level reductions and scans.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -20,9 +20,14 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ uint32_t cluster_size() {
+__device__ __forceinline__ uint32_t cluster_id_x() {
   uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
   return r;
 }
 // Full cluster barrier with release/acquire semantics on shared::cluster memory.
@@ -52,11 +57,6 @@ __device__ __forceinline__ uint64_t ld_peer_u64(const void* p, uint32_t rank) {
 __device__ __forceinline__ float ld_peer_f32(const void* p, uint32_t rank) {
   return __uint_as_float(ld_peer_u32(p, rank));
 }
-__device__ __forceinline__ uint16_t ld_peer_u16(const void* p, uint32_t rank) {
-  uint16_t v;
-  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(peer_addr(p, rank)) : "memory");
-  return v;
-}
 
 // ---------------------------------------------------------- mbarrier + bulk
 __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
@@ -64,6 +64,10 @@ __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t coun
 }
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Orders this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
@@ -153,82 +157,52 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-template <typename DT>
-__device__ __forceinline__ float to_f32(DT v);
-template <>
-__device__ __forceinline__ float to_f32<float>(float v) {
-  return v;
-}
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
-  return __bfloat162float(v);
-}
-
-// ---------------------------------------------------------------- weights
+// ------------------------------------------------------------ arithmetic
 __device__ __forceinline__ float ex2_approx(float y) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
   return r;
 }
-
-// Per-row constants of the temperature-scaled softmax weights
-//   e(z) = exp((z - m)/T) = 2^((z - m) * log2(e)/T).
-// Tokens within `head` nats of the maximum (z >= zh) get the argument carried
-// to ~2^-48 relative error (z - m as an exact two-term sum, log2(e)/T as a
-// two-term product) and e = 2^y_hi * (1 + y_lo * ln 2), about 2.5e-7 relative
-// error overall. Tokens further out (each weighing less than e^-head of the
-// maximum) use 2^((z - m) * log2(e)/T) directly.
-struct RowW {
-  float m;       // row maximum (raw logit)
-  float c2;      // log2(e)/T, rounded
-  float c2_lo;   // log2(e)/T - c2
-  float zh;      // accurate-weight threshold
-  float invT;    // 1/T, rounded (distance bins)
-};
-
-__device__ __forceinline__ float hweight(float z, const RowW& w) {
-  const float dz = z - w.m;
-  if (z >= w.zh) {
-    const float bb = dz - z;
-    const float dz_lo = (z - (dz - bb)) + (-w.m - bb);
-    const float y = dz * w.c2;
-    const float y_lo = fmaf(dz, w.c2, -y) + fmaf(dz, w.c2_lo, dz_lo * w.c2);
-    const float e = ex2_approx(y);
-    return fmaf(e, y_lo * 0.69314718055994531f, e);
-  }
-  return ex2_approx(dz * w.c2);   // z = -inf gives 0
+// max that returns NaN if either input is NaN
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
-
-// Fixed-point weight: floor(e * 2^shift), e in [0, 1]. Integer sums of these are
-// exact and independent of summation order.
-__device__ __forceinline__ uint64_t to_fixed(float e, float scale_pow2) {
-  return __float2ull_rz(e * scale_pow2);
+// 2^k as a float for integer k (0 below the normal range)
+__device__ __forceinline__ float pow2i(int k) {
+  return k < -126 ? 0.0f : (k > 127 ? __int_as_float(0x7f800000) : __int_as_float((k + 127) << 23));
 }
-
-// ------------------------------------------------------------ shared loads
+// floor(x * 2^k) for finite x >= 0 (0 for x below the normal range), built from
+// the float's bits with integer shifts; exact (truncation toward zero). The
+// result must fit 64 bits (x * 2^k < 2^64).
+__device__ __forceinline__ unsigned long long fix_pow2(float x, int k) {
+  const uint32_t b = __float_as_uint(x);
+  const int E = (int)((b >> 23) & 0xFFu);
+  if (E == 0 || (b >> 31)) return 0ull;
+  const unsigned long long M = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
+  const int sh = E - 150 + k;                     // x * 2^k = M * 2^sh
+  if (sh >= 0) return M << sh;
+  if (sh <= -24) return 0ull;
+  return M >> (-sh);
+}
+// 16- and 32-bit loads from shared memory by shared-window address.
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
 __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
-// Logit j of a row slice whose shared-memory byte address is `base`.
-template <typename DT>
-__device__ __forceinline__ float lds_logit(uint32_t base, int j);
-template <>
-__device__ __forceinline__ float lds_logit<float>(uint32_t base, int j) {
-  return __uint_as_float(lds_u32(base + 4u * (uint32_t)j));
-}
-template <>
-__device__ __forceinline__ float lds_logit<__nv_bfloat16>(uint32_t base, int j) {
-  return __uint_as_float(((uint32_t)lds_u16(base + 2u * (uint32_t)j)) << 16);
-}
-__device__ __forceinline__ void st_peer_u64(void* p, uint32_t rank, uint64_t v) {
-  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(peer_addr(p, rank)), "l"(v) : "memory");
+
+// 128-bit product compare: a*b > c*d for 64-bit unsigned operands.
+__device__ __forceinline__ bool mul_gt(uint64_t a, uint64_t b, uint64_t c, uint64_t d) {
+  const uint64_t ah = __umul64hi(a, b), al = a * b;
+  const uint64_t ch = __umul64hi(c, d), cl = c * d;
+  return ah > ch || (ah == ch && al > cl);
 }
 
 // ---------------------------------------------------- block-level helpers
@@ -239,6 +213,11 @@ template <typename T>
 __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 // Exclusive scan over the CTA in thread order; `scratch` holds NWARP entries.
@@ -264,36 +243,6 @@ __device__ __forceinline__ T block_excl_scan(T v, T* scratch, T* total) {
   }
   *total = tot;
   return off + incl - v;
-}
-template <typename T>
-__device__ __forceinline__ T block_sum(T v, T* scratch) {
-  T tot;
-  block_excl_scan<T>(v, scratch, &tot);
-  return tot;
-}
-
-// 128-bit product compare: a*b > c*d for 64-bit unsigned operands.
-__device__ __forceinline__ bool mul_gt(uint64_t a, uint64_t b, uint64_t c, uint64_t d) {
-  const uint64_t ah = __umul64hi(a, b), al = a * b;
-  const uint64_t ch = __umul64hi(c, d), cl = c * d;
-  return ah > ch || (ah == ch && al > cl);
-}
-
-// Warp-aggregated append of index j to a shared list when pred holds; every
-// lane of the warp must call it. Entries beyond cap are counted but dropped.
-__device__ __forceinline__ void list_push(bool pred, uint16_t j, uint16_t* list, unsigned int* cnt,
-                                          unsigned int cap) {
-  const unsigned int mk = __ballot_sync(0xffffffffu, pred);
-  if (mk == 0u) return;
-  const int lane = lane_id();
-  const int leader = __ffs(mk) - 1;
-  unsigned int base = 0;
-  if (lane == leader) base = atomicAdd(cnt, (unsigned int)__popc(mk));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (pred) {
-    const unsigned int pos = base + (unsigned int)__popc(mk & ((1u << lane) - 1u));
-    if (pos < cap) list[pos] = j;
-  }
 }
 
 }  // namespace sv
