@@ -30,7 +30,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_NAME = "sv_kernel"
+KERNEL_NAME = "sv_kernel"          # dominant kernel of sampling workloads
+GREEDY_KERNEL = "greedy_kernel"    # dominant kernel of temperature-0 workloads
 
 
 def dist_env():
@@ -59,9 +60,13 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def dominant_kernel(workload: str) -> str:
+    return GREEDY_KERNEL if workload == "greedy" else KERNEL_NAME
+
+
 def profiled_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{dominant_kernel(workload)}_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -250,8 +255,13 @@ def bench_gpu(args):
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                      "alg_bytes_per_launch": alg_bytes,
-                     "launch_ms": per_launch_ms, "kernel": KERNEL_NAME},
-        "gpu_launches": args.steps,
+                     "launch_ms": per_launch_ms, "kernel": dominant_kernel(w.name),
+                     "timing": "CUDA events around each spec_verify call (all kernels of "
+                               "the call), so the dominant kernel's own fraction is at "
+                               "least this"},
+        # per call: greedy_kernel (temperature-0 rows), greedy_finalize, sv_kernel
+        # (clusters); rows are 16-byte aligned here, so all three launch
+        "gpu_launches": 3 * args.steps,
         "e2e": e2e,
         "clocks": clk.summary(),
     }

@@ -82,11 +82,19 @@ struct Params {
   unsigned long long* ws_units; // per unit: bits 0..31 token, bit 32 flag, bit 33 error
   unsigned int* ws_tickets;     // per sequence
   unsigned int* ws_error;       // sticky: bit 0 = a bulk copy did not complete in time
+  unsigned long long* ws_best;  // greedy rows: (okey(max) << 32) | ~argmax
+  unsigned int* ws_rcnt;        // greedy rows: chunks done
+  unsigned int* ws_rflag;       // greedy rows: NaN / +inf seen
+  unsigned int* ws_work;        // set by greedy_kernel when other units exist
+  unsigned int* ws_done;        // cluster-kernel CTAs finished (resets ws_work)
+  int greedy_split;             // temperature-0 verify units go to greedy_kernel
 };
 
 struct Meta {
   float T, P;
   int k, d;
+  int g;                        // the unit's sequence is on the greedy path
+  int pad[3];
 };
 
 // Exchanged through DSMEM after the first cluster barrier of a unit.
@@ -218,6 +226,9 @@ struct Lg<float> {
   __device__ static __forceinline__ uint32_t key(float z) { return okey(z); }
   __device__ static __forceinline__ float key_float(uint32_t k) { return key_to_float(k); }
 };
+
+__device__ __forceinline__ float to_float_dt(float v) { return v; }
+__device__ __forceinline__ float to_float_dt(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // Calls f(z, l) for every logit of the slot in coalesced 16-byte vectors
 // (thread t takes vectors t, t + NT, ...; l is the index in the slice).
@@ -358,7 +369,7 @@ __device__ __forceinline__ float thread_max(const void* slot, int nvec) {
 
 // Lowest slice index holding the value m in this thread's vectors (UINT_MAX if none).
 template <typename DT>
-__device__ __forceinline__ uint32_t thread_first_index(const void* slot, int nvec, float m) {
+__device__ __noinline__ uint32_t thread_first_index(const void* slot, int nvec, float m) {
   const uint4* v = reinterpret_cast<const uint4*>(slot);
   constexpr int PV = 16 / sizeof(DT);
   for (int q = threadIdx.x; q < nvec; q += NT) {
@@ -380,7 +391,7 @@ __device__ __forceinline__ uint32_t thread_first_index(const void* slot, int nve
 // Pass B: per-thread bin masses (and counts) of the slot's weights, then the
 // CTA's fixed-point bin masses in the CTA frame, written to x.bins / x.cnts.
 template <typename DT, bool COUNTS>
-__device__ void pass_bins(const void* slot, int nvec, int vlen, const RowG& g, float* hist,
+__device__ __noinline__ void pass_bins(const void* slot, int nvec, int vlen, const RowG& g, float* hist,
                           uint8_t* hcnt, X1Row& x) {
   const int tid = threadIdx.x;
 #pragma unroll
@@ -430,7 +441,7 @@ __device__ void pass_bins(const void* slot, int nvec, int vlen, const RowG& g, f
 
 // Top-k rows: the 16-bit key prefix of the CTA's k-th largest per-thread maximum
 // (k <= NT), by two rounds of 256-bin counting over the thread maxima.
-__device__ uint32_t block_kth_prefix16(float tmax, int k, uint32_t* h, uint32_t* res) {
+__device__ __noinline__ uint32_t block_kth_prefix16(float tmax, int k, uint32_t* h, uint32_t* res) {
   const int tid = threadIdx.x;
   const uint32_t key = okey(tmax) >> 16;
   uint32_t above = 0, prefix = 0;
@@ -478,7 +489,7 @@ __device__ uint32_t block_kth_prefix16(float tmax, int k, uint32_t* h, uint32_t*
 
 // Top-k rows: lists (okey << 32 | ~id) of the slot's logits >= zt (cap LC).
 template <typename DT>
-__device__ void pass_list(const void* slot, int nvec, int vlen, float zt, int base,
+__device__ __noinline__ void pass_list(const void* slot, int nvec, int vlen, float zt, int base,
                           unsigned long long* list, uint32_t* count) {
   for_each_logit<DT>(slot, nvec, [&](float z, int l) {
     const bool pred = z >= zt && l < vlen;
@@ -502,7 +513,7 @@ __device__ void pass_list(const void* slot, int nvec, int vlen, float zt, int ba
 // 32 listed indices and adds each run with one atomic. Entries beyond the list
 // capacity are counted directly.
 template <typename DT>
-__device__ void pass_level(const void* slot, int nvec, int vlen, const RowG& gs, X2Row* x,
+__device__ __noinline__ void pass_level(const void* slot, int nvec, int vlen, const RowG& gs, X2Row* x,
                            uint8_t* list, uint32_t* list_n, int cap) {
   // row constants in registers (the loop stores to shared memory, which would
   // otherwise force reloads of the shared row state)
@@ -572,7 +583,7 @@ __device__ void pass_level(const void* slot, int nvec, int vlen, const RowG& gs,
 // -------------------------------------------------------- cluster merges
 // Warp 0 after an exchange barrier: cluster maximum, flags, frames and list
 // sizes of row `rho` (lanes 0..C-1 read CTA lane's X1).
-__device__ void merge_head(Shared& S, RowG& g, const X1Row* x1p, int rho, int C, uint32_t rank,
+__device__ __noinline__ void merge_head(Shared& S, RowG& g, const X1Row* x1p, int rho, int C, uint32_t rank,
                            bool* err, bool* extreme, bool* over, uint32_t* ncand_total) {
   const int l = lane_id();
   float m = -INFINITY, R = -INFINITY;
@@ -615,7 +626,7 @@ __device__ void merge_head(Shared& S, RowG& g, const X1Row* x1p, int rho, int C,
 // Thread (r, j) shifts CTA r's bin j into cluster bin min(j + h_r, NB-1); the
 // half-warp of CTA r folds the bins that land in the last bin; then thread j
 // sums cluster bin j over the CTAs.
-__device__ void merge_bins(Shared& S, const X1Row* x1p, int rho, int C, bool extreme,
+__device__ __noinline__ void merge_bins(Shared& S, const X1Row* x1p, int rho, int C, bool extreme,
                            unsigned long long* tmpb, uint32_t* tmpc) {
   const int t = threadIdx.x, r = t >> 4, j = t & 15;
   unsigned long long v = 0;
@@ -670,7 +681,7 @@ __device__ void merge_bins(Shared& S, const X1Row* x1p, int rho, int C, bool ext
 
 // The weight bin a cut lies in, and the key range of that bin (thread 0).
 template <typename DT>
-__device__ void ebin_pick(Shared& S, RowG& g, int rho) {
+__device__ __noinline__ void ebin_pick(Shared& S, RowG& g, int rho) {
   unsigned long long cm = g.above_m, cc = g.above_c;
   int j = 0;
   for (; j < NB - 1; ++j) {
@@ -711,7 +722,7 @@ __device__ void ebin_pick(Shared& S, RowG& g, int rho) {
 // After a refinement level: merge the sub-bins of row rho, pick the one holding
 // the cut; resolve the run of equal logits when a sub-bin is a single key.
 template <typename DT>
-__device__ void level_pick(Shared& S, RowG& g, int rho, const X2Row* xp, int C, uint32_t rank,
+__device__ __noinline__ void level_pick(Shared& S, RowG& g, int rho, const X2Row* xp, int C, uint32_t rank,
                            unsigned char* Gr) {
   const int t = threadIdx.x;
   const int s = g.nsub - 1 - t;             // thread order = descending keys
@@ -841,7 +852,7 @@ __device__ void level_pick(Shared& S, RowG& g, int rho, const X2Row* xp, int C, 
 
 // Sorts n composites (okey << 32 | ~id) in descending order (logit desc, id asc).
 // n <= NT: rank sort into out; otherwise bitonic in place (out = in).
-__device__ unsigned long long* sort_desc(unsigned long long* in, int n, unsigned long long* out) {
+__device__ __noinline__ unsigned long long* sort_desc(unsigned long long* in, int n, unsigned long long* out) {
   const int t = threadIdx.x;
   if (n <= NT) {
     if (t < n) {
@@ -879,7 +890,7 @@ __device__ unsigned long long* sort_desc(unsigned long long* in, int n, unsigned
 // Top-k rows: gather the listed candidates of every CTA, sort them, keep the
 // first k, then the top-p prefix of those. Sets zt / idcut (global id) / Zk.
 template <typename DT>
-__device__ void list_select(Shared& S, RowG& g, int rho, const unsigned long long* lists, int C,
+__device__ __noinline__ void list_select(Shared& S, RowG& g, int rho, const unsigned long long* lists, int C,
                             uint32_t n, int slice, unsigned long long* gbuf) {
   const int t = threadIdx.x;
   for (uint32_t idx = t; idx < n; idx += NT) {
@@ -922,7 +933,7 @@ __device__ void list_select(Shared& S, RowG& g, int rho, const unsigned long lon
 // (token-id order): per-thread counts over contiguous id ranges, a block scan,
 // then the thread holding that member scans its range.
 template <typename DT>
-__device__ void tie_pass(Shared& S, RowG& g, const void* slot, int ept, int vlen, int base) {
+__device__ __noinline__ void tie_pass(Shared& S, RowG& g, const void* slot, int ept, int vlen, int base) {
   const int t = threadIdx.x;
   const int l0 = t * ept, l1 = min(l0 + ept, vlen);
   const float zt = g.zt;
@@ -966,7 +977,7 @@ __device__ __forceinline__ void elem_w(const void* s0, const void* s1, bool pair
 
 // Residual and target mass over a contiguous id range, as fixed-point sums (2^-40).
 template <typename DT>
-__device__ __forceinline__ void sample_range(const void* s0, const void* s1, bool paired,
+__device__ __noinline__ void sample_range(const void* s0, const void* s1, bool paired,
                                              const RowG& g0s, const RowG& g1s, int l0, int l1,
                                              int base, unsigned long long* R,
                                              unsigned long long* Pm) {
@@ -987,7 +998,7 @@ __device__ __forceinline__ void sample_range(const void* s0, const void* s1, boo
 // Warp: the first id in [a0, a1) at which the running sum (from acc) times 2^24
 // exceeds kv * S; `useR` selects the residual or p. -1 if none.
 template <typename DT>
-__device__ int warp_sample_find(const void* s0, const void* s1, bool paired, const RowG& g0,
+__device__ __noinline__ int warp_sample_find(const void* s0, const void* s1, bool paired, const RowG& g0,
                                 const RowG& g1, int a0, int a1, int base, unsigned long long acc,
                                 bool useR, uint32_t kv, unsigned long long S) {
   const int ln = lane_id();
@@ -1015,7 +1026,7 @@ __device__ int warp_sample_find(const void* s0, const void* s1, bool paired, con
 
 // Probabilities of a row slice (truncated-probabilities mode).
 template <typename DT>
-__device__ void write_probs(const void* slot, const RowG& gs, int vlen, int base, float* out) {
+__device__ __noinline__ void write_probs(const void* slot, const RowG& gs, int vlen, int base, float* out) {
   const RowG g = gs;
   for (int l = threadIdx.x; l < vlen; l += NT) {
     const float z = Lg<DT>::at(slot, l);
@@ -1025,7 +1036,7 @@ __device__ void write_probs(const void* slot, const RowG& gs, int vlen, int base
 
 // Publishes one unit's result; the last of the K+1 units of sequence b writes
 // the sequence's outputs and re-arms the ticket (leaving the workspace zeroed).
-__device__ void publish_unit(const Params& P, int unit, int b, int token, bool flag, bool err) {
+__device__ __noinline__ void publish_unit(const Params& P, int unit, int b, int token, bool flag, bool err) {
   P.ws_units[unit] = (unsigned long long)(uint32_t)token | ((unsigned long long)flag << 32) |
                      ((unsigned long long)err << 33);
   __threadfence();
@@ -1088,6 +1099,7 @@ __device__ __forceinline__ bool param_error(const Params& P, const Meta& m, int 
 template <int MODE>
 __device__ __forceinline__ int unit_rows(const Params& P, const Meta& m, int i) {
   if (param_error<MODE>(P, m, i)) return 0;
+  if (MODE == MODE_VERIFY && P.greedy_split && m.g) return 0;   // greedy path
   if (MODE == MODE_VERIFY && i < P.K && m.T > 0.0f) return 2;
   return 1;
 }
@@ -1103,8 +1115,20 @@ __device__ __forceinline__ const DT* row_src(const Params& P, int b, int i, int 
   return r0 + ((size_t)b * P.K + i) * P.V;
 }
 
+// A sequence served by the greedy path: temperature 0 with valid parameters and
+// every drafted token in range (any other sequence goes to the cluster kernel,
+// which also reports parameter errors).
+__device__ __forceinline__ bool greedy_seq(const Params& P, int b) {
+  if (!(P.temp[b] == 0.0f) || !(P.topp[b] > 0.0f) || P.topk[b] < 0) return false;
+  for (int q = 0; q < P.K; ++q) {
+    const int d = P.dtok[(size_t)b * P.K + q];
+    if (d < 0 || d >= P.V) return false;
+  }
+  return true;
+}
+
 template <int MODE>
-__device__ void load_meta(Shared& S, const Params& P, int cid, int ncl, int nmine, int j0, int cnt) {
+__device__ __noinline__ void load_meta(Shared& S, const Params& P, int cid, int ncl, int nmine, int j0, int cnt) {
   for (int t = threadIdx.x; t < cnt; t += NT) {
     const int j = j0 + t;
     if (j >= nmine) break;
@@ -1115,6 +1139,7 @@ __device__ void load_meta(Shared& S, const Params& P, int cid, int ncl, int nmin
     m.P = P.topp[b];
     m.k = P.topk[b];
     m.d = (MODE == MODE_VERIFY && i < P.K) ? P.dtok[(size_t)b * P.K + i] : 0;
+    m.g = (MODE == MODE_VERIFY && P.greedy_split) ? (int)greedy_seq(P, b) : 0;
     S.meta[j % MR] = m;
   }
 }
@@ -1151,7 +1176,10 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
   const int base = (int)rank * P.slice;
   const int vlen = max(0, min(P.slice, P.V - base));
   const int nvec = (int)(slot_bytes / 16);
-  const int nmine = cid < P.nunits ? (P.nunits - 1 - cid) / ncl + 1 : 0;
+  int nmine = cid < P.nunits ? (P.nunits - 1 - cid) / ncl + 1 : 0;
+  // verify batches whose units are all temperature 0: nothing to do here
+  if (MODE == MODE_VERIFY && P.greedy_split && *reinterpret_cast<volatile unsigned int*>(P.ws_work) == 0u)
+    nmine = 0;
   const uint32_t copy_bytes = (uint32_t)((size_t)vlen * sizeof(DT));
   const uint64_t pol = policy_evict_first();
 
@@ -1178,7 +1206,10 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
     // producer: row slices of the next units, as far as the slots allow
     if (P.bulk_ok && !S.timeout) {
       bool fenced = false;
-      while (next_j < nmine) {
+      // only units whose metadata is loaded (the ring holds units j .. j+MR/2-1
+      // at least)
+      const int jlim = min(nmine, j + MR / 2);
+      while (next_j < jlim) {
         int nb_, ni_;
         decode_unit<MODE>(P, cid + next_j * ncl, &nb_, &ni_);
         const int nr = unit_rows<MODE>(P, S.meta[next_j % MR], ni_);
@@ -1240,6 +1271,8 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
       } else {
         for (int l = tid; l < vlen; l += NT) P.out_probs[(size_t)b * P.V + base + l] = __int_as_float(0x7fc00000);
       }
+    } else if (MODE == MODE_VERIFY && P.greedy_split && m.g) {
+      // units of greedy sequences are served by greedy_kernel + greedy_finalize
     } else if (m.T == 0.0f) {
       // ------------------------------------------------ greedy (T = 0)
       X1Row& x = S.x1[xr & 1][0];
@@ -1657,6 +1690,169 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
   }
   __syncthreads();
   cluster_sync();   // no CTA leaves while another may still read its shared memory
+  if (MODE == MODE_VERIFY && tid == 0) {
+    // the last CTA to finish re-arms the work flag for the next call (every CTA
+    // read it at its start)
+    __threadfence();
+    if (atomicAdd(P.ws_done, 1u) == gridDim.x - 1u) {
+      *P.ws_work = 0u;
+      *P.ws_done = 0u;
+    }
+  }
+}
+
+// ------------------------------------------------------- greedy streaming
+// Temperature-0 sequences of spec_verify: each target row is split into G chunks
+// (items). A persistent grid walks the items; a CTA holds its next item's
+// 16-byte vector loads in registers while it reduces the current one, so HBM
+// reads stay in flight. Per item: the maximum (packed bf16x2) and the lowest
+// index holding it, merged into the row's slot as (okey(max) << 32 | ~index)
+// with a 64-bit atomicMax that needs no reply (the largest logit, then the
+// lowest id); NaN / +inf set the row's flag. greedy_finalize then writes the
+// sequences' outputs. Items of other sequences raise the cluster kernel's work
+// flag.
+constexpr int GV = 6;          // 16-byte vectors per thread and item (at most)
+
+template <typename DT>
+__device__ __forceinline__ void greedy_load(const Params& P, int item, int G, int chunk, uint4* w,
+                                            int* row_out, bool* ok_out) {
+  const int row = item / G, c = item - row * G;
+  const int b = row / (P.K + 1);
+  const bool ok = greedy_seq(P, b);
+  *row_out = row;
+  *ok_out = ok;
+  constexpr uint32_t NEG = sizeof(DT) == 2 ? 0xFF80FF80u : 0xFF800000u;
+  const int l0 = c * chunk, l1 = min(l0 + chunk, P.V);
+  constexpr int PV = 16 / (int)sizeof(DT);
+  const uint4* v = reinterpret_cast<const uint4*>(static_cast<const DT*>(P.rows0) + (size_t)row * P.V) + l0 / PV;
+  const int nv = ok ? (l1 - l0) / PV : 0;
+#pragma unroll
+  for (int q = 0; q < GV; ++q) {
+    const int vi = (int)threadIdx.x + q * NT;
+    if (vi < nv) {
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[q].x), "=r"(w[q].y), "=r"(w[q].z), "=r"(w[q].w)
+                   : "l"(v + vi));
+    } else {
+      w[q] = make_uint4(NEG, NEG, NEG, NEG);
+    }
+  }
+}
+
+template <typename DT>
+__global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int chunk, int nitems,
+                                                     unsigned long long* best,
+                                                     unsigned int* rflag) {
+  const int tid = threadIdx.x;
+  constexpr int PV = 16 / (int)sizeof(DT);
+  __shared__ unsigned long long red[NWARP];
+  uint4 cur[GV], nxt[GV];
+  int item = blockIdx.x, row = 0, nrow = 0;
+  bool ok = false, nok = false;
+  if (item < nitems) greedy_load<DT>(P, item, G, chunk, cur, &row, &ok);
+  while (item < nitems) {
+    const int next = item + (int)gridDim.x;
+    if (next < nitems) greedy_load<DT>(P, next, G, chunk, nxt, &nrow, &nok);
+    if (!ok) {
+      if (tid == 0 && item - row * G == 0 &&
+          *reinterpret_cast<volatile unsigned int*>(P.ws_work) == 0u)
+        atomicOr(P.ws_work, 1u);
+    } else {
+      const int l0 = (item - row * G) * chunk;
+      float m;
+      if constexpr (sizeof(DT) == 2) {
+        __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll
+        for (int q = 0; q < GV; ++q) {
+          __nv_bfloat162 a, bb, cc, dd;
+          memcpy(&a, &cur[q].x, 4);
+          memcpy(&bb, &cur[q].y, 4);
+          memcpy(&cc, &cur[q].z, 4);
+          memcpy(&dd, &cur[q].w, 4);
+          m2 = __hmax2_nan(__hmax2_nan(m2, a), __hmax2_nan(__hmax2_nan(bb, cc), dd));
+        }
+        m = fmax_nan(__low2float(m2), __high2float(m2));
+      } else {
+        m = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < GV; ++q)
+          m = fmax_nan(fmax_nan(m, __uint_as_float(cur[q].x)),
+                       fmax_nan(__uint_as_float(cur[q].y),
+                                fmax_nan(__uint_as_float(cur[q].z), __uint_as_float(cur[q].w))));
+      }
+      uint32_t idx = UINT_MAX;
+      if (m > -INFINITY && m < INFINITY) {
+#pragma unroll
+        for (int q = GV - 1; q >= 0; --q) {       // backwards: the last hit is the lowest index
+          const uint32_t ws[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
+          const uint32_t base = (uint32_t)(l0 + (tid + q * NT) * PV);
+#pragma unroll
+          for (int h = 3; h >= 0; --h) {
+            if constexpr (sizeof(DT) == 2) {
+              if (__uint_as_float(ws[h] & 0xFFFF0000u) == m) idx = base + 2 * h + 1;
+              if (__uint_as_float(ws[h] << 16) == m) idx = base + 2 * h;
+            } else {
+              if (__uint_as_float(ws[h]) == m) idx = base + h;
+            }
+          }
+        }
+      }
+      const bool bad = (m != m) || m == INFINITY;
+      unsigned long long key = idx != UINT_MAX ? (((unsigned long long)okey(m) << 32) | (uint32_t)~idx) : 0ull;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const unsigned long long o2 = __shfl_xor_sync(0xffffffffu, key, o);
+        key = o2 > key ? o2 : key;
+      }
+      if (lane_id() == 0) red[warp_id()] = key;
+      const int anyb = __syncthreads_or(bad ? 1 : 0);
+      if (tid == 0) {
+        unsigned long long kb = red[0];
+        for (int q = 1; q < NWARP; ++q) kb = red[q] > kb ? red[q] : kb;
+        // results are not needed here: reductions without a round trip
+        if (anyb) atomicOr(&rflag[row], 1u);
+        else if (kb) atomicMax(&best[row], kb);
+      }
+      __syncthreads();                           // red[] is reused by the next item
+    }
+#pragma unroll
+    for (int q = 0; q < GV; ++q) cur[q] = nxt[q];
+    row = nrow;
+    ok = nok;
+    item = next;
+  }
+}
+
+// Greedy sequences after greedy_kernel: one thread per sequence reads the K+1
+// rows' (max, argmax) slots, writes the accepted prefix and the token, and
+// clears the slots for the next call.
+__global__ void greedy_finalize(const Params P, unsigned long long* best, unsigned int* rflag) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= P.B || !greedy_seq(P, b)) return;
+  const int K = P.K;
+  int nacc = K, last = -1;
+  bool err = false;
+  int32_t* ot = P.out_tokens + (size_t)b * (K + 1);
+  for (int q = 0; q <= K; ++q) {
+    const size_t r = (size_t)b * (K + 1) + q;
+    const unsigned long long fb = best[r];
+    const unsigned int ff = rflag[r];
+    best[r] = 0ull;
+    rflag[r] = 0u;
+    err |= ff != 0u || fb == 0ull;
+    const int amax = (int)~(uint32_t)fb;
+    if (q <= nacc && nacc == K) {
+      if (q < K && P.dtok[(size_t)b * K + q] != amax) {
+        nacc = q;
+        last = amax;
+      } else if (q == K) {
+        last = amax;
+      }
+    }
+  }
+  for (int q = 0; q <= K; ++q)
+    ot[q] = err ? -1 : (q < nacc ? P.dtok[(size_t)b * K + q] : (q == nacc ? last : -1));
+  P.out_n[b] = err ? -1 : nacc;
 }
 
 __global__ void philox_kernel(uint64_t seed, uint64_t offset, int B, int K1, uint32_t* out) {
@@ -1787,11 +1983,14 @@ static bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 
 
 extern "C" {
 
+// Workspace layout: [units u64 x B(K+1)][tickets u32 x B, padded to 16][error u32,
+// padded to 16][greedy best u64 x B(K+1)][greedy chunk counters u32 x B(K+1)]
+// [greedy flags u32 x B(K+1)]; all of it zero between calls.
 size_t spec_verify_workspace_bytes(int B, int K) {
   if (B < 1 || K < 1) return 0;
-  const size_t units = (size_t)B * (K + 1) * sizeof(unsigned long long);
+  const size_t rows = (size_t)B * (K + 1);
   const size_t tickets = ((size_t)B * sizeof(unsigned int) + 15) & ~(size_t)15;
-  return units + tickets + 16;
+  return rows * 8 + tickets + 16 + rows * 8 + rows * 4 + rows * 4;
 }
 
 sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
@@ -1833,9 +2032,43 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
   char* ws = static_cast<char*>(workspace);
   p.ws_units = reinterpret_cast<unsigned long long*>(ws);
   p.ws_tickets = reinterpret_cast<unsigned int*>(ws + (size_t)p.nunits * 8);
-  p.ws_error = reinterpret_cast<unsigned int*>(
-      ws + (size_t)p.nunits * 8 + (((size_t)B * 4 + 15) & ~(size_t)15));
-  return do_launch(MODE_VERIFY, dtype, p, g, static_cast<cudaStream_t>(stream));
+  const size_t rows = (size_t)p.nunits;
+  char* w2 = ws + rows * 8 + (((size_t)B * 4 + 15) & ~(size_t)15);
+  p.ws_error = reinterpret_cast<unsigned int*>(w2);
+  p.ws_work = reinterpret_cast<unsigned int*>(w2 + 4);
+  p.ws_done = reinterpret_cast<unsigned int*>(w2 + 8);
+  p.ws_best = reinterpret_cast<unsigned long long*>(w2 + 16);
+  p.ws_rcnt = reinterpret_cast<unsigned int*>(w2 + 16 + rows * 8);
+  p.ws_rflag = reinterpret_cast<unsigned int*>(w2 + 16 + rows * 12);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // temperature-0 units: streaming reduction; the cluster kernel takes the rest
+  // (unaligned rows: the cluster kernel serves every unit)
+  if (p.bulk_ok) {
+    const int PV = 16 / (int)es;
+    const int cmax = GV * NT * PV;
+    const int G = (V + cmax - 1) / cmax;
+    int chunk = (V + G - 1) / G;
+    chunk = (chunk + PV - 1) / PV * PV;
+    const long long nitems = (long long)rows * G;
+    static int gblocks = 0;
+    if (!gblocks) {
+      int dev = 0, sms = 0, per = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, greedy_kernel<__nv_bfloat16>, NT, 0);
+      gblocks = max(1, sms * max(1, per));
+    }
+    const unsigned grid = (unsigned)(nitems < (long long)gblocks ? nitems : (long long)gblocks);
+    if (dtype == SV_BF16)
+      greedy_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(p, G, chunk, (int)nitems, p.ws_best, p.ws_rflag);
+    else
+      greedy_kernel<float><<<grid, NT, 0, st>>>(p, G, chunk, (int)nitems, p.ws_best, p.ws_rflag);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    p.greedy_split = 1;
+    greedy_finalize<<<(unsigned)((B + NT - 1) / NT), NT, 0, st>>>(p, p.ws_best, p.ws_rflag);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  }
+  return do_launch(MODE_VERIFY, dtype, p, g, st);
 }
 
 sv_status spec_truncated_probs(const void* logits, sv_dtype dtype, int R, int V,
