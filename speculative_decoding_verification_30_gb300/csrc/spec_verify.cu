@@ -83,11 +83,12 @@ struct Params {
   unsigned int* ws_tickets;     // per sequence
   unsigned int* ws_error;       // sticky: bit 0 = a bulk copy did not complete in time
   unsigned long long* ws_best;  // greedy rows: (okey(max) << 32) | ~argmax
-  unsigned int* ws_rcnt;        // greedy rows: chunks done
+  unsigned int* ws_rcnt;        // [0]: greedy_kernel CTAs finished
   unsigned int* ws_rflag;       // greedy rows: NaN / +inf seen
   unsigned int* ws_work;        // set by greedy_kernel when other units exist
   unsigned int* ws_done;        // cluster-kernel CTAs finished (resets ws_work)
   int greedy_split;             // temperature-0 verify units go to greedy_kernel
+  int greedy_only;              // no draft logits: greedy_kernel serves the whole batch
 };
 
 struct Meta {
@@ -1272,7 +1273,7 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
         for (int l = tid; l < vlen; l += NT) P.out_probs[(size_t)b * P.V + base + l] = __int_as_float(0x7fc00000);
       }
     } else if (MODE == MODE_VERIFY && P.greedy_split && m.g) {
-      // units of greedy sequences are served by greedy_kernel + greedy_finalize
+      // units of greedy sequences are served by greedy_kernel
     } else if (m.T == 0.0f) {
       // ------------------------------------------------ greedy (T = 0)
       X1Row& x = S.x1[xr & 1][0];
@@ -1708,17 +1709,46 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
 // reads stay in flight. Per item: the maximum (packed bf16x2) and the lowest
 // index holding it, merged into the row's slot as (okey(max) << 32 | ~index)
 // with a 64-bit atomicMax that needs no reply (the largest logit, then the
-// lowest id); NaN / +inf set the row's flag. greedy_finalize then writes the
+// lowest id); NaN / +inf set the row's flag. The last CTA to finish writes the
 // sequences' outputs. Items of other sequences raise the cluster kernel's work
 // flag.
 constexpr int GV = 6;          // 16-byte vectors per thread and item (at most)
+
+// A greedy sequence once all its rows are reduced: the accepted prefix and the
+// token from the K+1 rows' (max, argmax) slots, which are cleared for the next call.
+__device__ void greedy_finalize_seq(const Params& P, int b, unsigned long long* best,
+                                    unsigned int* rflag) {
+  const int K = P.K;
+  int nacc = K, last = -1;
+  bool err = false;
+  for (int q = 0; q <= K; ++q) {
+    const size_t r = (size_t)b * (K + 1) + q;
+    const unsigned long long fb = best[r];
+    const unsigned int ff = rflag[r];
+    best[r] = 0ull;
+    rflag[r] = 0u;
+    err |= ff != 0u || fb == 0ull;
+    const int amax = (int)~(uint32_t)fb;
+    if (nacc == K) {
+      if (q < K && P.dtok[(size_t)b * K + q] != amax) {
+        nacc = q;
+        last = amax;
+      } else if (q == K) {
+        last = amax;
+      }
+    }
+  }
+  int32_t* ot = P.out_tokens + (size_t)b * (K + 1);
+  for (int q = 0; q <= K; ++q)
+    ot[q] = err ? -1 : (q < nacc ? P.dtok[(size_t)b * K + q] : (q == nacc ? last : -1));
+  P.out_n[b] = err ? -1 : nacc;
+}
 
 template <typename DT>
 __device__ __forceinline__ void greedy_load(const Params& P, int item, int G, int chunk, uint4* w,
                                             int* row_out, bool* ok_out) {
   const int row = item / G, c = item - row * G;
-  const int b = row / (P.K + 1);
-  const bool ok = greedy_seq(P, b);
+  const bool ok = greedy_seq(P, row / (P.K + 1));
   *row_out = row;
   *ok_out = ok;
   constexpr uint32_t NEG = sizeof(DT) == 2 ? 0xFF80FF80u : 0xFF800000u;
@@ -1742,7 +1772,7 @@ __device__ __forceinline__ void greedy_load(const Params& P, int item, int G, in
 template <typename DT>
 __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int chunk, int nitems,
                                                      unsigned long long* best,
-                                                     unsigned int* rflag) {
+                                                     unsigned int* rflag, unsigned int* done) {
   const int tid = threadIdx.x;
   constexpr int PV = 16 / (int)sizeof(DT);
   __shared__ unsigned long long red[NWARP];
@@ -1754,46 +1784,50 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
     const int next = item + (int)gridDim.x;
     if (next < nitems) greedy_load<DT>(P, next, G, chunk, nxt, &nrow, &nok);
     if (!ok) {
-      if (tid == 0 && item - row * G == 0 &&
+      if (!P.greedy_only && tid == 0 && item - row * G == 0 &&
           *reinterpret_cast<volatile unsigned int*>(P.ws_work) == 0u)
         atomicOr(P.ws_work, 1u);
     } else {
       const int l0 = (item - row * G) * chunk;
-      float m;
-      if constexpr (sizeof(DT) == 2) {
-        __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+      // per-vector maxima, then the thread maximum; the lowest index holding it
+      // is looked up only in the first vector whose maximum equals it
+      float vm[GV];
+      float m = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < GV; ++q) {
+      for (int q = 0; q < GV; ++q) {
+        if constexpr (sizeof(DT) == 2) {
           __nv_bfloat162 a, bb, cc, dd;
           memcpy(&a, &cur[q].x, 4);
           memcpy(&bb, &cur[q].y, 4);
           memcpy(&cc, &cur[q].z, 4);
           memcpy(&dd, &cur[q].w, 4);
-          m2 = __hmax2_nan(__hmax2_nan(m2, a), __hmax2_nan(__hmax2_nan(bb, cc), dd));
+          const __nv_bfloat162 v2 = __hmax2_nan(__hmax2_nan(a, bb), __hmax2_nan(cc, dd));
+          vm[q] = fmax_nan(__low2float(v2), __high2float(v2));
+        } else {
+          vm[q] = fmax_nan(fmax_nan(__uint_as_float(cur[q].x), __uint_as_float(cur[q].y)),
+                           fmax_nan(__uint_as_float(cur[q].z), __uint_as_float(cur[q].w)));
         }
-        m = fmax_nan(__low2float(m2), __high2float(m2));
-      } else {
-        m = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < GV; ++q)
-          m = fmax_nan(fmax_nan(m, __uint_as_float(cur[q].x)),
-                       fmax_nan(__uint_as_float(cur[q].y),
-                                fmax_nan(__uint_as_float(cur[q].z), __uint_as_float(cur[q].w))));
+        m = fmax_nan(m, vm[q]);
       }
       uint32_t idx = UINT_MAX;
       if (m > -INFINITY && m < INFINITY) {
+        int qf = GV;
 #pragma unroll
-        for (int q = GV - 1; q >= 0; --q) {       // backwards: the last hit is the lowest index
-          const uint32_t ws[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
-          const uint32_t base = (uint32_t)(l0 + (tid + q * NT) * PV);
+        for (int q = GV - 1; q >= 0; --q)
+          if (vm[q] == m) qf = q;
+        uint4 w = cur[0];
 #pragma unroll
-          for (int h = 3; h >= 0; --h) {
-            if constexpr (sizeof(DT) == 2) {
-              if (__uint_as_float(ws[h] & 0xFFFF0000u) == m) idx = base + 2 * h + 1;
-              if (__uint_as_float(ws[h] << 16) == m) idx = base + 2 * h;
-            } else {
-              if (__uint_as_float(ws[h]) == m) idx = base + h;
-            }
+        for (int q = 1; q < GV; ++q)
+          if (q == qf) w = cur[q];
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t base = (uint32_t)(l0 + (tid + qf * NT) * PV);
+#pragma unroll
+        for (int h = 3; h >= 0; --h) {
+          if constexpr (sizeof(DT) == 2) {
+            if (__uint_as_float(ws[h] & 0xFFFF0000u) == m) idx = base + 2 * h + 1;
+            if (__uint_as_float(ws[h] << 16) == m) idx = base + 2 * h;
+          } else {
+            if (__uint_as_float(ws[h]) == m) idx = base + h;
           }
         }
       }
@@ -1809,7 +1843,7 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
       if (tid == 0) {
         unsigned long long kb = red[0];
         for (int q = 1; q < NWARP; ++q) kb = red[q] > kb ? red[q] : kb;
-        // results are not needed here: reductions without a round trip
+        // one merge per item, without a reply (the row's slot takes the largest key)
         if (anyb) atomicOr(&rflag[row], 1u);
         else if (kb) atomicMax(&best[row], kb);
       }
@@ -1821,39 +1855,29 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
     ok = nok;
     item = next;
   }
-}
-
-// Greedy sequences after greedy_kernel: one thread per sequence reads the K+1
-// rows' (max, argmax) slots, writes the accepted prefix and the token, and
-// clears the slots for the next call.
-__global__ void greedy_finalize(const Params P, unsigned long long* best, unsigned int* rflag) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= P.B || !greedy_seq(P, b)) return;
-  const int K = P.K;
-  int nacc = K, last = -1;
-  bool err = false;
-  int32_t* ot = P.out_tokens + (size_t)b * (K + 1);
-  for (int q = 0; q <= K; ++q) {
-    const size_t r = (size_t)b * (K + 1) + q;
-    const unsigned long long fb = best[r];
-    const unsigned int ff = rflag[r];
-    best[r] = 0ull;
-    rflag[r] = 0u;
-    err |= ff != 0u || fb == 0ull;
-    const int amax = (int)~(uint32_t)fb;
-    if (q <= nacc && nacc == K) {
-      if (q < K && P.dtok[(size_t)b * K + q] != amax) {
-        nacc = q;
-        last = amax;
-      } else if (q == K) {
-        last = amax;
+  // the last CTA to finish writes the greedy sequences' outputs
+  __shared__ int last_cta;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    last_cta = atomicAdd(done, 1u) == gridDim.x - 1u;
+  }
+  __syncthreads();
+  if (last_cta) {
+    __threadfence();
+    for (int b = tid; b < P.B; b += NT) {
+      if (greedy_seq(P, b)) {
+        greedy_finalize_seq(P, b, best, rflag);
+      } else if (P.greedy_only) {
+        // no draft logits: a sequence off the greedy path is a data error
+        for (int q = 0; q <= P.K; ++q) P.out_tokens[(size_t)b * (P.K + 1) + q] = -1;
+        P.out_n[b] = -1;
       }
     }
+    if (tid == 0) *done = 0u;
   }
-  for (int q = 0; q <= K; ++q)
-    ot[q] = err ? -1 : (q < nacc ? P.dtok[(size_t)b * K + q] : (q == nacc ? last : -1));
-  P.out_n[b] = err ? -1 : nacc;
 }
+
 
 __global__ void philox_kernel(uint64_t seed, uint64_t offset, int B, int K1, uint32_t* out) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -2044,6 +2068,9 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
   // temperature-0 units: streaming reduction; the cluster kernel takes the rest
   // (unaligned rows: the cluster kernel serves every unit)
   if (p.bulk_ok) {
+    // without draft logits every sequence must be greedy (others are data
+    // errors), so the greedy kernel alone serves the batch
+    p.greedy_only = draft_logits == nullptr ? 1 : 0;
     const int PV = 16 / (int)es;
     const int cmax = GV * NT * PV;
     const int G = (V + cmax - 1) / cmax;
@@ -2060,13 +2087,12 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
     }
     const unsigned grid = (unsigned)(nitems < (long long)gblocks ? nitems : (long long)gblocks);
     if (dtype == SV_BF16)
-      greedy_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(p, G, chunk, (int)nitems, p.ws_best, p.ws_rflag);
+      greedy_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(p, G, chunk, (int)nitems, p.ws_best, p.ws_rflag, p.ws_rcnt);
     else
-      greedy_kernel<float><<<grid, NT, 0, st>>>(p, G, chunk, (int)nitems, p.ws_best, p.ws_rflag);
+      greedy_kernel<float><<<grid, NT, 0, st>>>(p, G, chunk, (int)nitems, p.ws_best, p.ws_rflag, p.ws_rcnt);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     p.greedy_split = 1;
-    greedy_finalize<<<(unsigned)((B + NT - 1) / NT), NT, 0, st>>>(p, p.ws_best, p.ws_rflag);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    if (p.greedy_only) return SV_OK;
   }
   return do_launch(MODE_VERIFY, dtype, p, g, st);
 }
