@@ -190,11 +190,11 @@ constexpr size_t SHARED_BYTES = (sizeof(Shared) + 127) & ~(size_t)127;
 
 #ifdef SV_TRACE
 // Phase timestamps of the first 64 units of CTA 0 of cluster 0 (trace builds).
-__device__ unsigned long long g_trace[64 * 16 + 16];
+__device__ unsigned long long g_trace[64 * 32 + 16];
 #define SV_MARK(k)                                                         \
   do {                                                                     \
     if (cid == 0 && rank == 0 && threadIdx.x == 0 && j < 64)               \
-      g_trace[j * 16 + (k)] = global_timer_ns();                           \
+      g_trace[j * 32 + (k)] = global_timer_ns();                           \
   } while (0)
 #else
 #define SV_MARK(k) \
@@ -288,6 +288,31 @@ __device__ __forceinline__ float wacc(float z, const RowG& g) {
   if (g.extreme) return wext(z, g.mg, g.c);
   const float t = z * g.c;
   if (!(t > -1.0e9f)) return 0.0f;               // -inf logit, or 2^(very negative)
+  const float tl = fmaf(z, g.c, -t);
+  const float n = rintf(t);
+  const float f = (t - n) + tl;
+  return ex2_approx(f) * pow2i((int)(n - g.Rg));
+}
+// The row constants of the sampling phase, passed by value (registers).
+struct WP {
+  float zt, invZ, c, Rg, mg;
+  int idcut, extreme;
+};
+__device__ __forceinline__ WP wp_of(const RowG& g) {
+  WP w;
+  w.zt = g.zt;
+  w.invZ = g.invZ;
+  w.c = g.c;
+  w.Rg = g.Rg;
+  w.mg = g.mg;
+  w.idcut = g.idcut;
+  w.extreme = g.extreme;
+  return w;
+}
+__device__ __forceinline__ float wacc_v(float z, WP g) {
+  if (g.extreme) return wext(z, g.mg, g.c);
+  const float t = z * g.c;
+  if (!(t > -1.0e9f)) return 0.0f;
   const float tl = fmaf(z, g.c, -t);
   const float n = rintf(t);
   const float f = (t - n) + tl;
@@ -523,44 +548,53 @@ __device__ __noinline__ void pass_level(const void* slot, int nvec, int vlen, co
   const int hsh = gs.sh >> 1, fsh = extreme ? 0 : gs.sh, ebin = gs.ebin, kshift = gs.kshift;
   const uint32_t klo = gs.klo, nsub = (uint32_t)gs.nsub;
   const bool listed = kshift == 0 && nsub <= 255u;
-  // per-warp list segment, fill count kept in a register (warp-uniform)
-  const uint32_t wcap = (uint32_t)cap / NWARP;
-  uint8_t* wl = list + (size_t)warp_id() * wcap;
-  uint32_t wn = 0;
+  // per-thread hit buffers (TB entries each, interleaved so that entry r of the
+  // 32 lanes of a warp is one 32-byte row); the count stays in a register and
+  // no warp-wide operation runs per logit
+  constexpr int TB = 32;
+  static_assert(NT * TB <= (int)G_BYTES, "hit buffers exceed their region");
+  const int tid = threadIdx.x, lane = lane_id();
+  uint8_t* tb = list + (size_t)warp_id() * 32 * TB;           // [TB][32] per warp
+  uint32_t n = 0;
   (void)list_n;
-  for_each_logit<DT>(slot, nvec, [&](float z, int l) {
-    uint32_t sub = 0xFFFFFFFFu;
-    float e = 0.0f;
-    if (z >= lo && z <= hi && l < vlen) {
-      e = extreme ? wext(z, mg, c) : wloc(z, c, negR);
-      const int b = extreme ? wbin(e) : min(wbin(e) + hsh, NB - 1);
-      if (b == ebin) {
-        const uint32_t sb = (Lg<DT>::key(z) - klo) >> kshift;
-        if (sb < nsub) sub = sb;
+  (void)cap;
+  const uint4* vv = reinterpret_cast<const uint4*>(slot);
+  constexpr int PV = 16 / (int)sizeof(DT);
+  for (int q = tid; q < nvec; q += NT) {
+    const uint4 w4 = vv[q];
+    const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int h = 0; h < PV; ++h) {
+      float z;
+      if constexpr (sizeof(DT) == 2) z = __uint_as_float((h & 1) ? (ws[h >> 1] & 0xFFFF0000u) : (ws[h >> 1] << 16));
+      else z = __uint_as_float(ws[h]);
+      const int l = q * PV + h;
+      if (z >= lo && z <= hi && l < vlen) {
+        const float e = extreme ? wext(z, mg, c) : wloc(z, c, negR);
+        const int b = extreme ? wbin(e) : min(wbin(e) + hsh, NB - 1);
+        if (b == ebin) {
+          const uint32_t sub = (Lg<DT>::key(z) - klo) >> kshift;
+          if (sub < nsub) {
+            if (listed && n < (uint32_t)TB) {
+              tb[n * 32 + lane] = (uint8_t)sub;
+              ++n;
+            } else {
+              atomicAdd(&x->cnt[sub], 1u);
+              if (kshift > 0) atomicAdd(&x->mass[sub], fixg(e, fsh));
+            }
+          }
+        }
       }
     }
-    const bool hit = sub != 0xFFFFFFFFu;
-    if (!listed) {
-      if (hit) {
-        atomicAdd(&x->cnt[sub], 1u);
-        if (kshift > 0) atomicAdd(&x->mass[sub], fixg(e, fsh));
-      }
-      return;
-    }
-    const uint32_t mk = __ballot_sync(0xffffffffu, hit);
-    if (hit) {
-      const uint32_t pos = wn + (uint32_t)__popc(mk & ((1u << lane_id()) - 1u));
-      if (pos < wcap) wl[pos] = (uint8_t)sub;
-      else atomicAdd(&x->cnt[sub], 1u);
-    }
-    wn += (uint32_t)__popc(mk);
-  });
+  }
   if (!listed) return;
-  // each warp counts its own segment: sort 32 entries, one atomic per run
-  const uint32_t n = min(wn, wcap);
-  const int lane = lane_id();
-  for (uint32_t b0 = 0; b0 < n; b0 += 32) {
-    uint32_t v = b0 + lane < n ? wl[b0 + lane] : 0xFFu;
+  // each warp counts its buffers: round r sorts entry r of its 32 lanes and adds
+  // each run of equal sub-bins with one atomic
+  uint32_t rounds = n;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) rounds = max(rounds, __shfl_xor_sync(0xffffffffu, rounds, o));
+  for (uint32_t r = 0; r < rounds; ++r) {
+    uint32_t v = r < n ? tb[r * 32 + lane] : 0xFFu;
 #pragma unroll
     for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
@@ -730,19 +764,14 @@ __device__ __noinline__ void level_pick(Shared& S, RowG& g, int rho, const X2Row
   unsigned long long mass = 0;
   uint32_t cnt = 0;
   uint32_t* pc = reinterpret_cast<uint32_t*>(Gr);          // [16] counts of the picked key
-  uint32_t nn[16];
-#pragma unroll
-  for (int r = 0; r < 16; ++r) nn[r] = 0u;
   if (s >= 0) {
+    // all peers' loads issued together (no dependency between them)
+    uint32_t nn[16];
     unsigned long long mm[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      if (r < C) {
-        nn[r] = ld_peer_u32(&xp->cnt[s], r);
-        mm[r] = ld_peer_u64(&xp->mass[s], r);
-      } else {
-        mm[r] = 0ull;
-      }
+      nn[r] = r < C ? ld_peer_u32(&xp->cnt[s], r) : 0u;
+      mm[r] = r < C ? ld_peer_u64(&xp->mass[s], r) : 0ull;
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -764,8 +793,7 @@ __device__ __noinline__ void level_pick(Shared& S, RowG& g, int rho, const X2Row
       S.res_i[0] = s;
       S.res_u[0] = em;
       S.res_u[1] = ec;
-#pragma unroll
-      for (int r = 0; r < 16; ++r) pc[r] = nn[r];
+      for (int r = 0; r < 16; ++r) pc[r] = r < C ? ld_peer_u32(&xp->cnt[s], r) : 0u;
     }
   }
   __syncthreads();
@@ -957,19 +985,18 @@ __device__ __noinline__ void tie_pass(Shared& S, RowG& g, const void* slot, int 
 // Sampling weight of slice index l: the residual (p - q)+ (paired units) or p,
 // and p itself (both 0 outside the target's kept set).
 template <typename DT>
-__device__ __forceinline__ void elem_w(const void* s0, const void* s1, bool paired,
-                                       const RowG& g0, const RowG& g1, int l, int base,
-                                       float* r, float* p) {
+__device__ __forceinline__ void elem_w(const void* s0, const void* s1, bool paired, WP g0, WP g1,
+                                       int l, int base, float* r, float* p) {
   const float zp = Lg<DT>::at(s0, l);
   const int gid = base + l;
   *r = 0.0f;
   *p = 0.0f;
   if (kept(zp, gid, g0.zt, g0.idcut)) {
-    const float pp = __fmul_rn(wacc(zp, g0), g0.invZ);
+    const float pp = __fmul_rn(wacc_v(zp, g0), g0.invZ);
     float q = 0.0f;
     if (paired) {
       const float zq = Lg<DT>::at(s1, l);
-      if (kept(zq, gid, g1.zt, g1.idcut)) q = __fmul_rn(wacc(zq, g1), g1.invZ);
+      if (kept(zq, gid, g1.zt, g1.idcut)) q = __fmul_rn(wacc_v(zq, g1), g1.invZ);
     }
     *r = fmaxf(__fsub_rn(pp, q), 0.0f);
     *p = pp;
@@ -978,11 +1005,9 @@ __device__ __forceinline__ void elem_w(const void* s0, const void* s1, bool pair
 
 // Residual and target mass over a contiguous id range, as fixed-point sums (2^-40).
 template <typename DT>
-__device__ __noinline__ void sample_range(const void* s0, const void* s1, bool paired,
-                                             const RowG& g0s, const RowG& g1s, int l0, int l1,
-                                             int base, unsigned long long* R,
-                                             unsigned long long* Pm) {
-  const RowG g0 = g0s, g1 = g1s;            // row constants in registers
+__device__ __noinline__ void sample_range(const void* s0, const void* s1, bool paired, WP g0,
+                                          WP g1, int l0, int l1, int base, unsigned long long* R,
+                                          unsigned long long* Pm) {
   unsigned long long ra = 0, pa = 0;
   for (int l = l0; l < l1; ++l) {
     const float zp = Lg<DT>::at(s0, l);
@@ -999,8 +1024,8 @@ __device__ __noinline__ void sample_range(const void* s0, const void* s1, bool p
 // Warp: the first id in [a0, a1) at which the running sum (from acc) times 2^24
 // exceeds kv * S; `useR` selects the residual or p. -1 if none.
 template <typename DT>
-__device__ __noinline__ int warp_sample_find(const void* s0, const void* s1, bool paired, const RowG& g0,
-                                const RowG& g1, int a0, int a1, int base, unsigned long long acc,
+__device__ __noinline__ int warp_sample_find(const void* s0, const void* s1, bool paired, WP g0,
+                                WP g1, int a0, int a1, int base, unsigned long long acc,
                                 bool useR, uint32_t kv, unsigned long long S) {
   const int ln = lane_id();
   for (int c0 = a0; c0 < a1; c0 += 32) {
@@ -1027,11 +1052,10 @@ __device__ __noinline__ int warp_sample_find(const void* s0, const void* s1, boo
 
 // Probabilities of a row slice (truncated-probabilities mode).
 template <typename DT>
-__device__ __noinline__ void write_probs(const void* slot, const RowG& gs, int vlen, int base, float* out) {
-  const RowG g = gs;
+__device__ __noinline__ void write_probs(const void* slot, WP g, int vlen, int base, float* out) {
   for (int l = threadIdx.x; l < vlen; l += NT) {
     const float z = Lg<DT>::at(slot, l);
-    out[base + l] = kept(z, base + l, g.zt, g.idcut) ? __fmul_rn(wacc(z, g), g.invZ) : 0.0f;
+    out[base + l] = kept(z, base + l, g.zt, g.idcut) ? __fmul_rn(wacc_v(z, g), g.invZ) : 0.0f;
   }
 }
 
@@ -1407,6 +1431,7 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
         }
       }
       __syncthreads();
+      SV_MARK(22);
       ++xr;
       bool uerr = S.rg[0].err || (paired && S.rg[1].err);
       if (!uerr) {
@@ -1462,6 +1487,7 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
           }
           ++xr;
         }
+        SV_MARK(23);
         // selection set-up
         for (int rho = 0; rho < nr; ++rho) {
           RowG& g = S.rg[rho];
@@ -1507,12 +1533,15 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
           }
           if (tid < 2) S.list_n[tid] = 0u;
           __syncthreads();
+          SV_MARK(16);
           for (int rho = 0; rho < nr; ++rho) {
             if (rho == 0 ? !k0 : !k1) continue;
-            pass_level<DT>(sl[rho], nvec, vlen, S.rg[rho], &xl[rho], Gr + (size_t)rho * (G_BYTES / 2),
-                           &S.list_n[rho], (int)(G_BYTES / 2));
+            // the hit buffers (8 KB) are consumed inside the call, so rows share them
+            pass_level<DT>(sl[rho], nvec, vlen, S.rg[rho], &xl[rho], Gr, &S.list_n[rho], (int)G_BYTES);
+            SV_MARK(17 + rho);
           }
           __syncthreads();
+          SV_MARK(19);
           // single-key sub-bins: mass = count * this CTA's weight of that key
           for (int rho = 0; rho < nr; ++rho) {
             if (rho == 0 ? !k0 : !k1) continue;
@@ -1531,10 +1560,11 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
           for (int rho = 0; rho < nr; ++rho) {
             if (rho == 0 ? !k0 : !k1) continue;
             level_pick<DT>(S, S.rg[rho], rho, &xl[rho], C, rank, Gr);
+            SV_MARK(20 + rho);
           }
           ++lp;
 #ifdef SV_TRACE
-          if (cid == 0 && rank == 0 && threadIdx.x == 0 && j < 64) g_trace[j * 16 + 10] = (unsigned long long)lp;
+          if (cid == 0 && rank == 0 && threadIdx.x == 0 && j < 64) g_trace[j * 32 + 10] = (unsigned long long)lp;
 #endif
         }
         uerr = S.rg[0].err || (paired && S.rg[1].err);
@@ -1562,8 +1592,8 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
           if (S.rg[rho].partial) tie_pass<DT>(S, S.rg[rho], sl[rho], P.ept, vlen, base);
         __syncthreads();
         SV_MARK(12);
-        const RowG& g0 = S.rg[0];
-        const RowG& g1 = S.rg[paired ? 1 : 0];
+        const WP g0 = wp_of(S.rg[0]);
+        const WP g1 = wp_of(S.rg[paired ? 1 : 0]);
         if (MODE == MODE_PROBS) {
           write_probs<DT>(sl[0], g0, vlen, base, P.out_probs + (size_t)b * P.V);
           cluster_sync();                                          // end of unit
@@ -1575,8 +1605,8 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
             if (paired && m.d / P.slice == (int)rank) {
               const int l = m.d - base;
               const float zp = Lg<DT>::at(sl[0], l), zq = Lg<DT>::at(sl[1], l);
-              const float p = kept(zp, m.d, g0.zt, g0.idcut) ? __fmul_rn(wacc(zp, g0), g0.invZ) : 0.0f;
-              const float q = kept(zq, m.d, g1.zt, g1.idcut) ? __fmul_rn(wacc(zq, g1), g1.invZ) : 0.0f;
+              const float p = kept(zp, m.d, g0.zt, g0.idcut) ? __fmul_rn(wacc_v(zp, g0), g0.invZ) : 0.0f;
+              const float q = kept(zq, m.d, g1.zt, g1.idcut) ? __fmul_rn(wacc_v(zq, g1), g1.invZ) : 0.0f;
               flag = __fmul_rn((float)ku * 5.9604644775390625e-08f, q) < p ? 1u : 0u;
             }
             S.x3.flag = flag;
@@ -1673,13 +1703,13 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
     rows_done += nr;
     SV_MARK(8);
 #ifdef SV_TRACE
-    if (cid == 0 && rank == 0 && threadIdx.x == 0 && j < 64) g_trace[j * 16 + 9] = (unsigned long long)nr;
+    if (cid == 0 && rank == 0 && threadIdx.x == 0 && j < 64) g_trace[j * 32 + 9] = (unsigned long long)nr;
 #endif
   }
 #ifdef SV_TRACE
   if (cid == 0 && rank == 0 && threadIdx.x == 0) {
-    g_trace[64 * 16] = (unsigned long long)ncl;
-    g_trace[64 * 16 + 1] = (unsigned long long)nmine;
+    g_trace[64 * 32] = (unsigned long long)ncl;
+    g_trace[64 * 32 + 1] = (unsigned long long)nmine;
   }
 #endif
   // copies still in flight after a timeout: wait (bounded) before leaving
@@ -2177,11 +2207,11 @@ int sv_version(void) { return 300; }
 
 #ifdef SV_TRACE
 int sv_trace_reset(void) {
-  static unsigned long long zero[64 * 16 + 16];
+  static unsigned long long zero[64 * 32 + 16];
   return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
 }
 int sv_trace_copy(unsigned long long* host, size_t n) {
-  if (n > 64 * 16 + 16) n = 64 * 16 + 16;
+  if (n > 64 * 32 + 16) n = 64 * 32 + 16;
   return cudaMemcpyFromSymbol(host, g_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
 }
 #endif

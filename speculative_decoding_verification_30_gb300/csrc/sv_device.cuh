@@ -41,17 +41,20 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 // Address of the same shared variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
   uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
   return r;
 }
+// Loads from a peer CTA's shared memory. They are ordered after cluster barriers
+// (which are compiler memory barriers); no clobber here, so independent peer
+// loads can be issued back to back.
 __device__ __forceinline__ uint32_t ld_peer_u32(const void* p, uint32_t rank) {
   uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(peer_addr(p, rank)) : "memory");
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(peer_addr(p, rank)));
   return v;
 }
 __device__ __forceinline__ uint64_t ld_peer_u64(const void* p, uint32_t rank) {
   uint64_t v;
-  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(peer_addr(p, rank)) : "memory");
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(peer_addr(p, rank)));
   return v;
 }
 __device__ __forceinline__ float ld_peer_f32(const void* p, uint32_t rank) {
