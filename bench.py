@@ -130,6 +130,28 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def job_throughput(total_ms: float, steps: int, rows_per_step: int, ws: int, dev):
+    """Whole-job throughput of `ws` independent replicas.
+
+    Every rank processes `rows_per_step` rows per step on its own inputs; the job
+    time is the slowest rank's timed region (max over ranks), and the value is
+    the rows all ranks processed divided by that time. Returns (ms_per_step,
+    rows/s)."""
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        tt = torch.tensor([float(total_ms)], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / steps
+    return ms_per_step, rows_per_step * ws * steps / (total_ms / 1e3)
+
+
+def replica_input_step(rank: int, s: int) -> int:
+    """Seed index of input set `s` on `rank`: replicas never share inputs."""
+    return 1000 * rank + s
+
+
 def bench_gpu(args):
     import torch
     import torch.distributed as dist
@@ -152,7 +174,7 @@ def bench_gpu(args):
     nsets = min(nsets, 64)
     sets = []
     for s in range(nsets):
-        b = make_batch(w, 1000 * rank + s, device=dev)
+        b = make_batch(w, replica_input_step(rank, s), device=dev)
         T, k, P = b.temperature.to(dev), b.top_k.to(dev), b.top_p.to(dev)
         # drafted tokens: the library's own draft-side sampler (d ~ q), not timed
         dtok = sv.spec_sample(b.draft, T, k, P, seed=4242, offset=10_000 + s)
@@ -191,13 +213,8 @@ def bench_gpu(args):
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
     per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    ms_per_step = total_ms / args.steps
     rows_per_step = w.rows_per_step()
-    value = rows_per_step * ws / (ms_per_step / 1e3)
+    ms_per_step, value = job_throughput(total_ms, args.steps, rows_per_step, ws, dev)
 
     # end to end through the public call with host buffers: H2D inputs, verify, D2H outputs
     e2e = None
