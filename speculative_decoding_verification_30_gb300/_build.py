@@ -8,7 +8,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libspec_verify.so")
 SOURCES = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "spec_verify_noalloc.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"),
+DEPS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(CSRC, "keyhist.cuh"),
                   os.path.join(os.path.dirname(HERE), "include", "spec_verify.h")]
 
 NVCC_FLAGS = [

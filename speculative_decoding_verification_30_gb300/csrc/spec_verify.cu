@@ -65,6 +65,8 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 // X1 row flags
 constexpr uint32_t F_NAN = 1u, F_PINF = 2u, F_EXTREME = 4u, F_OVER = 8u;
 
+struct KhRow;
+
 struct Params {
   const void* rows0;            // target [B][K+1][V] | probs rows [R][V] | draft [B][K][V]
   const void* rows1;            // draft [B][K][V] (verify)
@@ -89,6 +91,11 @@ struct Params {
   unsigned int* ws_done;        // cluster-kernel CTAs finished (resets ws_work)
   int greedy_split;             // temperature-0 verify units go to greedy_kernel
   int greedy_only;              // no draft logits: greedy_kernel serves the whole batch
+  int fast_split;               // sampled bf16 sequences go to keyhist_kernel
+  KhRow* ws_rowres;             // keyhist_kernel: per-row results [B][2K+1]
+  unsigned int* ws_fb;          // keyhist_kernel: 1 = sequence handed to the cluster kernel
+  unsigned int* ws_fnext;       // keyhist_kernel: work counter
+  unsigned int* ws_fdone;       // keyhist_kernel: CTAs finished
 };
 
 struct Meta {
@@ -341,6 +348,10 @@ __device__ __forceinline__ unsigned long long mass_threshold(float P, unsigned l
   if (s >= 64) return hi >> (s - 64);
   return (hi << (64 - s)) | (lo >> s);
 }
+
+}  // namespace sv
+#include "keyhist.cuh"
+namespace sv {
 
 // --------------------------------------------------------- block helpers
 __device__ __forceinline__ float block_max_nan(float v, float* red) {
@@ -1087,6 +1098,7 @@ __device__ __noinline__ void publish_unit(const Params& P, int unit, int b, int 
   for (int q = 0; q <= P.K; ++q)
     P.ws_units[q < P.K ? (size_t)b * P.K + q : (size_t)P.B * P.K + b] = 0ull;
   P.ws_tickets[b] = 0u;
+  if (P.fast_split) P.ws_fb[b] = 0u;             // a sequence keyhist_kernel handed back
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1164,7 +1176,10 @@ __device__ __noinline__ void load_meta(Shared& S, const Params& P, int cid, int 
     m.P = P.topp[b];
     m.k = P.topk[b];
     m.d = (MODE == MODE_VERIFY && i < P.K) ? P.dtok[(size_t)b * P.K + i] : 0;
-    m.g = (MODE == MODE_VERIFY && P.greedy_split) ? (int)greedy_seq(P, b) : 0;
+    // sequences served by greedy_kernel or, unless handed back, keyhist_kernel
+    m.g = (MODE == MODE_VERIFY && P.greedy_split)
+              ? (int)(greedy_seq(P, b) || (P.fast_split && fast_seq(P, b) && P.ws_fb[b] == 0u))
+              : 0;
     S.meta[j % MR] = m;
   }
 }
@@ -1814,7 +1829,10 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
     const int next = item + (int)gridDim.x;
     if (next < nitems) greedy_load<DT>(P, next, G, chunk, nxt, &nrow, &nok);
     if (!ok) {
+      // rows of sampled sequences: the cluster kernel has work unless they all
+      // go to keyhist_kernel (which raises the flag itself when it hands one back)
       if (!P.greedy_only && tid == 0 && item - row * G == 0 &&
+          !(P.fast_split && fast_seq(P, row / (P.K + 1))) &&
           *reinterpret_cast<volatile unsigned int*>(P.ws_work) == 0u)
         atomicOr(P.ws_work, 1u);
     } else {
@@ -2044,7 +2062,9 @@ size_t spec_verify_workspace_bytes(int B, int K) {
   if (B < 1 || K < 1) return 0;
   const size_t rows = (size_t)B * (K + 1);
   const size_t tickets = ((size_t)B * sizeof(unsigned int) + 15) & ~(size_t)15;
-  return rows * 8 + tickets + 16 + rows * 8 + rows * 4 + rows * 4;
+  const size_t head = rows * 8 + tickets + 16 + rows * 8 + rows * 4 + rows * 4;
+  // keyhist_kernel: hand-back flags, row results, work counter
+  return ((head + 15) & ~(size_t)15) + tickets + (size_t)B * (2 * K + 1) * sizeof(KhRow) + 16;
 }
 
 sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
@@ -2094,6 +2114,16 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
   p.ws_best = reinterpret_cast<unsigned long long*>(w2 + 16);
   p.ws_rcnt = reinterpret_cast<unsigned int*>(w2 + 16 + rows * 8);
   p.ws_rflag = reinterpret_cast<unsigned int*>(w2 + 16 + rows * 12);
+  {
+    const size_t tickets = ((size_t)B * sizeof(unsigned int) + 15) & ~(size_t)15;
+    const size_t head = rows * 8 + tickets + 16 + rows * 8 + rows * 4 + rows * 4;
+    char* w3 = ws + ((head + 15) & ~(size_t)15);
+    p.ws_fb = reinterpret_cast<unsigned int*>(w3);
+    p.ws_rowres = reinterpret_cast<KhRow*>(w3 + tickets);
+    char* w4 = w3 + tickets + (size_t)B * (2 * K + 1) * sizeof(KhRow);
+    p.ws_fnext = reinterpret_cast<unsigned int*>(w4);
+    p.ws_fdone = reinterpret_cast<unsigned int*>(w4 + 4);
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // temperature-0 units: streaming reduction; the cluster kernel takes the rest
   // (unaligned rows: the cluster kernel serves every unit)
@@ -2101,6 +2131,8 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
     // without draft logits every sequence must be greedy (others are data
     // errors), so the greedy kernel alone serves the batch
     p.greedy_only = draft_logits == nullptr ? 1 : 0;
+    // sampled bf16 sequences: one-pass key-histogram kernel
+    p.fast_split = (dtype == SV_BF16 && draft_logits != nullptr) ? 1 : 0;
     const int PV = 16 / (int)es;
     const int cmax = GV * NT * PV;
     const int G = (V + cmax - 1) / cmax;
@@ -2123,6 +2155,23 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     p.greedy_split = 1;
     if (p.greedy_only) return SV_OK;
+    if (p.fast_split) {
+      static int kblocks = 0;
+      if (!kblocks) {
+        int dev = 0, sms = 0, per = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaFuncSetAttribute(keyhist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)KH_SMEM) != cudaSuccess)
+          return SV_ERR_CUDA;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, keyhist_kernel, KT, KH_SMEM);
+        kblocks = max(1, sms * max(1, per));
+      }
+      const int kitems = B * (2 * K + 1);
+      const int kgrid = kitems < kblocks ? kitems : kblocks;
+      keyhist_kernel<<<kgrid, KT, KH_SMEM, st>>>(p, kitems);
+      if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    }
   }
   return do_launch(MODE_VERIFY, dtype, p, g, st);
 }
