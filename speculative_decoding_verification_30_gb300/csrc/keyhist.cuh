@@ -34,10 +34,46 @@ constexpr int KH_WPT = (KH_NW + KT - 1) / KT;             // words swept per thr
 constexpr int KH_NINF = KH_OFF - (0x7F80 - (int)KH_TSPLIT + 1);   // bin of -inf
 constexpr int KH_PINF = KH_OFF + (0x7F80 - (int)KH_TSPLIT + 1);   // bin of +inf
 constexpr int KH_PF = 4;                                  // 16-byte loads in flight per thread
-constexpr size_t KH_SMEM = (size_t)KH_NW * 4;
+constexpr int KH_MAXBLK = 64;                             // 32-vector blocks per warp range (V <= 262144)
+constexpr size_t KH_HIST_BYTES = ((size_t)KH_NW * 4 + 15) & ~(size_t)15;
+constexpr size_t KH_SMEM = KH_HIST_BYTES + 2 * (size_t)KWARP * KH_MAXBLK * 8;
 constexpr float KH_LOG2E = 1.44269504088896341f;
 
 constexpr uint32_t KH_ERR = 1u, KH_BAIL = 2u;
+constexpr int KH_LCAP = 1024;                             // listed kept tokens per target row
+constexpr uint32_t KH_NOLIST = 0xFFFFFFFFu;
+constexpr float KH_LIST_BITS = 12.0f;                     // listed: weight >= 2^-12 of the maximum
+
+#ifdef SV_TRACE
+// Phase timestamps per row item (trace builds): 0 fetched, 1 streamed, 2 swept,
+// 3 cut found, 4 row done, 5 finalize start, 6 finalize end, 7 SM id.
+__device__ unsigned long long g_khtrace[4096 * 8];
+#define KH_MARK(item, k)                                                   \
+  do {                                                                     \
+    if (threadIdx.x == 0 && (item) < 4096) g_khtrace[(item) * 8 + (k)] = global_timer_ns(); \
+  } while (0)
+// Per-sequence finalize timestamps: 0 start, 1 acceptance done, 2 first sampling
+// pass done, 3 end; 4 = redo, 5 = n.
+__device__ unsigned long long g_kftrace[1024 * 8];
+#define KF_MARK(b, k)                                                      \
+  do {                                                                     \
+    if (threadIdx.x == 0 && (b) < 1024) g_kftrace[(b) * 8 + (k)] = global_timer_ns(); \
+  } while (0)
+#define KF_SET(b, k, v)                                                    \
+  do {                                                                     \
+    if (threadIdx.x == 0 && (b) < 1024) g_kftrace[(b) * 8 + (k)] = (v);   \
+  } while (0)
+#else
+#define KF_MARK(b, k) \
+  do {                \
+  } while (0)
+#define KF_SET(b, k, v) \
+  do {                  \
+  } while (0)
+#define KH_MARK(item, k) \
+  do {                   \
+  } while (0)
+#endif
 
 // Per-row result, written by the row's CTA and read by the sequence's finalizer.
 struct KhRow {
@@ -49,6 +85,21 @@ struct KhRow {
   uint32_t flags;  // KH_ERR (NaN, +inf or no finite logit), KH_BAIL
   uint32_t pad[2];
 };
+
+// The row constants the sampling phase needs, passed by value (registers).
+struct KhW {
+  float zt, invZ, m, c;
+  int idcut;
+};
+__device__ __forceinline__ KhW kh_wof(const KhRow& r) {
+  KhW w;
+  w.zt = r.zt;
+  w.invZ = r.invZ;
+  w.m = r.m;
+  w.c = r.c;
+  w.idcut = r.idcut;
+  return w;
+}
 
 // Bin of a bf16 bit pattern; increasing in the logit's value.
 __device__ __forceinline__ uint32_t kh_bin(uint32_t h) {
@@ -106,7 +157,13 @@ struct KhShared {
   unsigned long long Mk, Wk;
   int item, last, flags, idcut, wq, rq;
   int nacc, tok, useR;
-  uint32_t flag[64];
+  uint32_t need;                       // positions whose acceptance waits for a draft id split
+  uint32_t cmax;                       // collection: running block maximum (order-preserving key)
+  uint32_t ccount;                     // collection: candidates pushed
+  uint32_t gcount;                     // collection: kept tokens written out
+  uint32_t flag[16];
+  float pz[16], qz[16];                // p(d), and q(d) if d is kept
+  uint32_t ku[16];
 };
 
 // Exclusive sums in descending thread order (thread KT-1 first) and the total.
@@ -142,8 +199,8 @@ __device__ __forceinline__ uint4 kh_ld(const uint4* p) {
 }
 __device__ __forceinline__ uint4 kh_ld_l2(const uint4* p) { return __ldcg(p); }
 
-// Counts the 8 logits of one vector and folds them into the running maximum.
-__device__ __forceinline__ void kh_count8(uint32_t* hist, const uint4& w, __nv_bfloat162& m2) {
+// Counts the 8 logits of one vector; returns their packed maximum.
+__device__ __forceinline__ __nv_bfloat162 kh_count8(uint32_t* hist, const uint4& w) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -156,21 +213,75 @@ __device__ __forceinline__ void kh_count8(uint32_t* hist, const uint4& w, __nv_b
   memcpy(&b, &w.y, 4);
   memcpy(&c, &w.z, 4);
   memcpy(&d, &w.w, 4);
-  m2 = __hmax2(__hmax2(m2, a), __hmax2(__hmax2(b, c), d));
+  return __hmax2(__hmax2(a, b), __hmax2(c, d));
+}
+
+// Candidate list of a target row: every token within D of the running block
+// maximum at the time it is read. The running maximum never exceeds the row
+// maximum m, so the list holds every token with z >= m - D unless it overflowed.
+__device__ __forceinline__ void kh_collect(const uint4& w, int v, __nv_bfloat162 vm2, float D,
+                                           float* theta, KhShared& S, unsigned long long* list) {
+  const float vm = fmaxf(__low2float(vm2), __high2float(vm2));
+  if (!(vm >= *theta)) return;
+  float smax = key_to_float(*reinterpret_cast<volatile uint32_t*>(&S.cmax));
+  if (vm > smax) {
+    atomicMax(&S.cmax, okey(vm));
+    smax = vm;
+  }
+  *theta = smax - D;
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t bits = (e & 1) ? ws[e >> 1] >> 16 : ws[e >> 1] & 0xFFFFu;
+    if (__uint_as_float(bits << 16) >= *theta) {
+      const uint32_t slot = atomicAdd(&S.ccount, 1u);
+      if (slot < (uint32_t)KH_LCAP) list[slot] = (unsigned long long)(v * 8 + e) | ((unsigned long long)bits << 32);
+    }
+  }
 }
 
 // Streams one row (nv 16-byte vectors) into the histogram; returns this
 // thread's maximum (NaN is ignored here: NaN bins are checked afterwards).
-__device__ __forceinline__ float kh_stream(const uint4* src, int nv, uint32_t* hist) {
+// COLLECT: also lists the candidates of kh_collect (threshold seeded by the
+// block maximum of the first load wave).
+template <bool COLLECT>
+__device__ __forceinline__ float kh_stream(const uint4* src, int nv, uint32_t* hist, float D,
+                                           KhShared& S, unsigned long long* list) {
   const int tid = threadIdx.x;
   uint4 buf[KH_PF];
+  const uint32_t NEG2 = 0xFF80FF80u;
 #pragma unroll
   for (int p = 0; p < KH_PF; ++p) {
     const int q = tid + p * KT;
-    if (q < nv) buf[p] = kh_ld(src + q);
+    buf[p] = q < nv ? kh_ld(src + q) : make_uint4(NEG2, NEG2, NEG2, NEG2);
   }
   __nv_bfloat162 m2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0xFF80u),
                                          __ushort_as_bfloat16((unsigned short)0xFF80u));
+  float theta = -INFINITY;
+  if (COLLECT) {
+    __nv_bfloat162 f2 = m2;
+#pragma unroll
+    for (int p = 0; p < KH_PF; ++p) {
+      __nv_bfloat162 a, b, c, d;
+      memcpy(&a, &buf[p].x, 4);
+      memcpy(&b, &buf[p].y, 4);
+      memcpy(&c, &buf[p].z, 4);
+      memcpy(&d, &buf[p].w, 4);
+      f2 = __hmax2(f2, __hmax2(__hmax2(a, b), __hmax2(c, d)));
+    }
+    float fm = fmaxf(__low2float(f2), __high2float(f2));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, o));
+    if (tid == 0) {
+      S.cmax = okey(-INFINITY);
+      S.ccount = 0u;
+      S.gcount = 0u;
+    }
+    __syncthreads();
+    if (lane_id() == 0) atomicMax(&S.cmax, okey(fm));
+    __syncthreads();
+    theta = key_to_float(S.cmax) - D;
+  }
   for (int q0 = tid; q0 < nv; q0 += KH_PF * KT) {
 #pragma unroll
     for (int p = 0; p < KH_PF; ++p) {
@@ -179,7 +290,9 @@ __device__ __forceinline__ float kh_stream(const uint4* src, int nv, uint32_t* h
         const uint4 w = buf[p];
         const int qn = q + KH_PF * KT;
         if (qn < nv) buf[p] = kh_ld(src + qn);
-        kh_count8(hist, w, m2);
+        const __nv_bfloat162 vm2 = kh_count8(hist, w);
+        m2 = __hmax2(m2, vm2);
+        if (COLLECT) kh_collect(w, q, vm2, D, &theta, S, list);
       }
     }
   }
@@ -198,60 +311,101 @@ __device__ __forceinline__ uint32_t kh_match8(const uint4& w, uint32_t hb) {
   return mk;
 }
 
+extern __shared__ __align__(16) uint32_t kh_dyn[];
+// Per-(warp, block) partial results after the histogram: block j of warp w
+// covers vectors [a0(w) + 32 j, a0(w) + 32 j + 32).
+__device__ __forceinline__ unsigned long long* kh_blk0() {
+  return reinterpret_cast<unsigned long long*>(reinterpret_cast<unsigned char*>(kh_dyn) + KH_HIST_BYTES);
+}
+__device__ __forceinline__ unsigned long long* kh_blk1() { return kh_blk0() + KWARP * KH_MAXBLK; }
+
 // The id of the q-th (1-based) token, in id order, whose logit pattern is hb.
-// Each warp counts a contiguous id range; the warp holding the q-th match
-// locates it with a lane-order scan. -1 if there are fewer than q matches.
+// Every warp counts matches per 32-vector block of its contiguous id range;
+// warp 0 then locates the block holding the q-th match with two lane-parallel
+// scans and finds the token in it. -1 if there are fewer than q matches.
 __device__ __noinline__ int kh_tie(const uint4* src, int nv, uint32_t hb, int q, KhShared& S) {
   const int w = warp_id(), l = lane_id();
   const int cw = (nv + KWARP - 1) / KWARP;
+  const int nb = (cw + 31) / 32;
   const int a0 = min(w * cw, nv), a1 = min(a0 + cw, nv);
-  uint32_t n = 0;
-  for (int v = a0 + l; v < a1; v += 32) n += __popc(kh_match8(kh_ld_l2(src + v), hb));
-  n = warp_sum(n);
-  if (l == 0) S.s32[w] = n;
-  if (threadIdx.x == 0) S.idcut = -1;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t acc = 0;
-    S.wq = -1;
-    for (int i = 0; i < KWARP; ++i) {
-      if (acc + S.s32[i] >= (uint32_t)q) {
-        S.wq = i;
-        S.rq = q - (int)acc;
-        break;
-      }
-      acc += S.s32[i];
+  uint32_t* blk = reinterpret_cast<uint32_t*>(kh_blk0());
+  uint32_t tot = 0;
+  for (int j = 0; j < nb; j += 4) {
+    uint4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = a0 + (j + u) * 32 + l;
+      x[u] = (j + u < nb && v < a1) ? kh_ld_l2(src + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = a0 + (j + u) * 32 + l;
+      const uint32_t c = warp_sum((uint32_t)__popc((j + u < nb && v < a1) ? kh_match8(x[u], hb) : 0u));
+      if (l == 0 && j + u < nb) blk[w * KH_MAXBLK + j + u] = c;
+      tot += c;
     }
   }
+  if (l == 0) S.s32[w] = tot;
   __syncthreads();
-  if (w == S.wq) {
-    int r = S.rq;
-    for (int v0 = a0; v0 < a1; v0 += 32) {
-      const int v = v0 + l;
-      const uint32_t mk = v < a1 ? kh_match8(kh_ld_l2(src + v), hb) : 0u;
-      const int cnt = __popc(mk);
-      int incl = cnt;
+  if (w == 0) {
+    // the warp range, then the block, holding the q-th match
+    const uint32_t own = l < KWARP ? S.s32[l] : 0u;
+    uint32_t incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (l >= o) incl += t;
+    }
+    const uint32_t bw = __ballot_sync(0xffffffffu, l < KWARP && incl >= (uint32_t)q);
+    int id = -1;
+    if (bw) {
+      const int ww = __ffs(bw) - 1;
+      uint32_t r = (uint32_t)q - (__shfl_sync(0xffffffffu, incl, ww) - __shfl_sync(0xffffffffu, own, ww));
+      const int wa0 = min(ww * cw, nv), wa1 = min(wa0 + cw, nv);
+      // blocks of warp ww: lane l holds blocks 2l and 2l+1
+      const uint32_t b0 = 2 * l < nb ? blk[ww * KH_MAXBLK + 2 * l] : 0u;
+      const uint32_t b1 = 2 * l + 1 < nb ? blk[ww * KH_MAXBLK + 2 * l + 1] : 0u;
+      uint32_t bi = b0 + b1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (l >= o) incl += t;
+        const uint32_t t = __shfl_up_sync(0xffffffffu, bi, o);
+        if (l >= o) bi += t;
       }
-      const int excl = incl - cnt;
-      const uint32_t bal = __ballot_sync(0xffffffffu, excl < r && r <= incl);
-      if (bal) {
-        if (l == __ffs(bal) - 1) {
-          int need = r - excl;
+      const uint32_t bl = __ballot_sync(0xffffffffu, bi >= r);
+      if (bl) {
+        const int lb = __ffs(bl) - 1;
+        const uint32_t before = __shfl_sync(0xffffffffu, bi - b0 - b1, lb);
+        const uint32_t lb0 = __shfl_sync(0xffffffffu, b0, lb);
+        int jb = 2 * lb;
+        r -= before;
+        if (r > lb0) {
+          r -= lb0;
+          ++jb;
+        }
+        // the block: one vector per lane, in id order
+        const int v = wa0 + jb * 32 + l;
+        const uint32_t mk = v < wa1 ? kh_match8(kh_ld_l2(src + v), hb) : 0u;
+        const uint32_t cnt = __popc(mk);
+        uint32_t ci = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_up_sync(0xffffffffu, ci, o);
+          if (l >= o) ci += t;
+        }
+        const uint32_t hit = __ballot_sync(0xffffffffu, ci >= r && ci - cnt < r);
+        if (hit && l == __ffs(hit) - 1) {
+          uint32_t need = r - (ci - cnt);
           for (int e = 0; e < 8; ++e)
             if ((mk >> e) & 1u)
-              if (--need == 0) {
-                S.idcut = v * 8 + e;
+              if (--need == 0u) {
+                id = v * 8 + e;
                 break;
               }
         }
-        break;
+        id = __reduce_max_sync(0xffffffffu, id);
       }
-      r -= __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (l == 0) S.idcut = id;
   }
   __syncthreads();
   return S.idcut;
@@ -262,46 +416,116 @@ __device__ __forceinline__ unsigned long long kh_binw(int idx, float m, float c)
   return idx > KH_NINF ? kh_fix(kh_value(idx), m, c) : 0ull;
 }
 
-// One row: histogram, maximum, normaliser, top-k / top-p cut and the id split of
-// a partial cut bin. Leaves the histogram zeroed. The result is returned in
-// every thread.
+constexpr int KH_DEFER = -2;       // idcut of a partial cut bin not yet split by id
+
+// Warp 0: walks the bins of thread range t (words [t*WPT, ...)) in descending
+// order from the running count acc / mass M before the range, and stops at the
+// first bin where the count reaches k (by_mass false) or the mass exceeds Y.
+// Publishes the bin, its count and weight, and the count and mass before it.
+__device__ __forceinline__ void kh_walk(const uint32_t* hist, int t, uint32_t acc,
+                                        unsigned long long M, bool by_mass, uint32_t k,
+                                        unsigned long long Y, float m, float c, KhShared& S) {
+  const int l = lane_id();
+  const int w0 = min(t * KH_WPT, KH_NW), w1 = min(w0 + KH_WPT, KH_NW);
+  const int n = w1 - w0;
+  for (int base = 0; base < n; base += 32) {
+    const int pos = base + l;
+    const int wd = w1 - 1 - pos;
+    const uint32_t x = pos < n ? hist[wd] : 0u;
+    const uint32_t chi = x >> 16, clo = x & 0xFFFFu;
+    const unsigned long long Whi = chi ? kh_binw(2 * wd + 1, m, c) : 0ull;
+    const unsigned long long Wlo = clo ? kh_binw(2 * wd, m, c) : 0ull;
+    const uint32_t cw = chi + clo;
+    const unsigned long long mw = chi * Whi + clo * Wlo;
+    uint32_t ic = cw;
+    unsigned long long im = mw;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t tc = __shfl_up_sync(0xffffffffu, ic, o);
+      const unsigned long long tm = __shfl_up_sync(0xffffffffu, im, o);
+      if (l >= o) {
+        ic += tc;
+        im += tm;
+      }
+    }
+    const bool cross = pos < n && (by_mass ? (M + im > Y) : (acc + ic >= k));
+    const uint32_t bal = __ballot_sync(0xffffffffu, cross);
+    if (bal) {
+      if (l == __ffs(bal) - 1) {
+        uint32_t a2 = acc + ic - cw;
+        unsigned long long M2 = M + im - mw;
+        const bool in_hi = chi != 0u && (by_mass ? (M2 + chi * Whi > Y) : (a2 + chi >= k));
+        if (!in_hi) {
+          a2 += chi;
+          M2 += chi * Whi;
+        }
+        S.cbin = 2 * wd + (in_hi ? 1 : 0);
+        S.ccnt = (int)(in_hi ? chi : clo);
+        S.Wcut = in_hi ? Whi : Wlo;
+        S.Mcut = M2;
+        S.kq = (int)a2;                 // count before the bin
+      }
+      return;
+    }
+    acc += __shfl_sync(0xffffffffu, ic, 31);
+    M += __shfl_sync(0xffffffffu, im, 31);
+  }
+}
+
+// One row: histogram, maximum, normaliser, top-k / top-p cut and (target rows)
+// the id split of a partial cut bin; a draft row's split is left to the
+// sequence's finalizer, which needs it only for tokens on the cut value.
+// Leaves the histogram zeroed. The result is returned in every thread.
 __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, int k, float topP,
-                                     uint32_t* hist, KhShared& S) {
+                                     bool target, uint32_t* hist, KhShared& S, uint32_t* glist,
+                                     int item) {
   const int tid = threadIdx.x, l = lane_id(), w = warp_id();
   const int nv = V / 8;
+  const bool defer_tie = !target;
   const uint4* src = reinterpret_cast<const uint4*>(row);
-  float mt = kh_stream(src, nv, hist);
+  uint32_t* rcnt = reinterpret_cast<uint32_t*>(kh_blk0());      // per thread range
+  unsigned long long* rmass =
+      reinterpret_cast<unsigned long long*>(reinterpret_cast<unsigned char*>(kh_blk0()) + KT * 4);
+  unsigned long long* clist = kh_blk1();                         // candidates (id | bits << 32)
+  rcnt[tid] = 0u;
+  rmass[tid] = 0ull;
+  const float c = __fdiv_rn(KH_LOG2E, T);
+  const float D = __fdiv_rn(KH_LIST_BITS, c);                    // z >= m - D: weight >= 2^-12
+  float mt = target ? kh_stream<true>(src, nv, hist, D, S, clist)
+                    : kh_stream<false>(src, nv, hist, D, S, clist);
 #pragma unroll
   for (int o = 16; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
   if (l == 0) S.fmax[w] = mt;
   __syncthreads();                              // the histogram is complete
+  KH_MARK(item, 1);
   float m = S.fmax[0];
 #pragma unroll
   for (int i = 1; i < KWARP; ++i) m = fmaxf(m, S.fmax[i]);
-  const float c = __fdiv_rn(KH_LOG2E, T);
 
-  // sweep: counts and fixed-point masses of this thread's bins
-  const int w0 = min(tid * KH_WPT, KH_NW), w1 = min(w0 + KH_WPT, KH_NW);
-  uint32_t cnt = 0, bad = 0;
-  unsigned long long mass = 0;
-  for (int wd = w0; wd < w1; ++wd) {
+  // sweep, words interleaved over the threads (occupied bins cluster in a few
+  // value ranges): counts and fixed-point masses, added to the word's thread range
+  uint32_t bad = 0;
+  for (int wd = tid; wd < KH_NW; wd += KT) {
     const uint32_t x = hist[wd];
     if (x == 0u) continue;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t cb = h ? x >> 16 : x & 0xFFFFu;
-      if (cb == 0u) continue;
-      const int idx = 2 * wd + h;
-      cnt += cb;
-      if (idx < KH_NINF || idx >= KH_PINF) bad = 1u;
-      else mass += (unsigned long long)cb * kh_binw(idx, m, c);
-    }
+    const uint32_t chi = x >> 16, clo = x & 0xFFFFu;
+    const int i0 = 2 * wd;
+    if ((clo && (i0 < KH_NINF || i0 >= KH_PINF)) || (chi && (i0 + 1 < KH_NINF || i0 + 1 >= KH_PINF)))
+      bad = 1u;
+    const unsigned long long mw = (clo ? clo * kh_binw(i0, m, c) : 0ull) +
+                                  (chi ? chi * kh_binw(i0 + 1, m, c) : 0ull);
+    const int r = wd / KH_WPT;
+    atomicAdd(&rcnt[r], chi + clo);
+    if (mw) atomicAdd(&rmass[r], mw);
   }
   const int anyb = __syncthreads_or((int)bad);
+  const uint32_t cnt = rcnt[tid];
+  const unsigned long long mass = bad ? 0ull : rmass[tid];
   uint32_t ctot;
   const uint32_t cab = kh_above<uint32_t>(cnt, S.s32, &ctot);
   unsigned long long Ztot;
   const unsigned long long mab = kh_above<unsigned long long>(mass, S.s64, &Ztot);
+  KH_MARK(item, 2);
 
   KhRow res;
   res.m = m;
@@ -310,91 +534,58 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   res.idcut = V;
   res.invZ = 0.0f;
   res.flags = 0u;
-  res.pad[0] = res.pad[1] = 0u;
+  res.pad[0] = 0u;
+  res.pad[1] = KH_NOLIST;
   if (anyb || !(m > -INFINITY)) res.flags = KH_ERR;
   else if (ctot != (uint32_t)V) res.flags = KH_BAIL;
   const bool topk = k > 0 && k < V;
   const bool topp = topP < 1.0f;
+  unsigned long long ZL1 = Ztot;
   if (res.flags == 0u && topk) {
     // the bin holding the k-th token in (logit desc, id asc) order
     if (cab < (uint32_t)k && (uint32_t)k <= cab + cnt) {
-      uint32_t acc = cab;
-      unsigned long long M = mab;
-      for (int wd = w1 - 1; wd >= w0; --wd) {
-        const uint32_t x = hist[wd];
-        if (x == 0u) continue;
-        bool done = false;
-#pragma unroll
-        for (int h = 1; h >= 0; --h) {
-          const uint32_t cb = h ? x >> 16 : x & 0xFFFFu;
-          if (cb == 0u || done) continue;
-          const int idx = 2 * wd + h;
-          const unsigned long long W = kh_binw(idx, m, c);
-          if (acc + cb >= (uint32_t)k) {
-            S.kbin = idx;
-            S.kq = k - (int)acc;
-            S.Mk = M;
-            S.Wk = W;
-            S.ccnt = (int)cb;
-            done = true;
-          } else {
-            acc += cb;
-            M += (unsigned long long)cb * W;
-          }
-        }
-        if (done) break;
-      }
+      S.wq = tid;
+      S.acc = mab;
+      S.rq = (int)cab;
     }
     __syncthreads();
+    if (w == 0) kh_walk(hist, S.wq, (uint32_t)S.rq, S.acc, false, (uint32_t)k, 0ull, m, c, S);
+    __syncthreads();
+    ZL1 = S.Mcut + (unsigned long long)(k - S.kq) * S.Wcut;
+    if (!topp && tid == 0) S.cq = k - S.kq;   // tokens of the bin inside the top k
   }
-  if (res.flags == 0u && (topk || topp)) {
-    const unsigned long long ZL1 = topk ? S.Mk + (unsigned long long)S.kq * S.Wk : Ztot;
-    if (topp) {
-      // the bin where the exclusive mass first exceeds Y = the largest integer
-      // below P * Z(L1); tokens with exclusive mass <= Y are kept
-      const unsigned long long Y = mass_threshold(topP, ZL1);
-      if (mab <= Y && Y < mab + mass) {
-        unsigned long long M = mab;
-        for (int wd = w1 - 1; wd >= w0; --wd) {
-          const uint32_t x = hist[wd];
-          if (x == 0u) continue;
-          bool done = false;
-#pragma unroll
-          for (int h = 1; h >= 0; --h) {
-            const uint32_t cb = h ? x >> 16 : x & 0xFFFFu;
-            if (cb == 0u || done) continue;
-            const int idx = 2 * wd + h;
-            const unsigned long long W = kh_binw(idx, m, c);
-            if (M + (unsigned long long)cb * W > Y) {
-              S.cbin = idx;
-              S.cq = (int)((Y - M) / W) + 1;
-              S.Mcut = M;
-              S.Wcut = W;
-              S.ccnt = (int)cb;
-              done = true;
-            } else {
-              M += (unsigned long long)cb * W;
-            }
-          }
-          if (done) break;
-        }
-      }
-    } else if (tid == 0) {
-      S.cbin = S.kbin;
-      S.cq = S.kq;
-      S.Mcut = S.Mk;
-      S.Wcut = S.Wk;
+  if (res.flags == 0u && topp) {
+    // the bin where the exclusive mass first exceeds Y = the largest integer
+    // below P * Z(L1); tokens with exclusive mass <= Y are kept
+    const unsigned long long Y = mass_threshold(topP, ZL1);
+    __syncthreads();
+    if (mab <= Y && Y < mab + mass) {
+      S.wq = tid;
+      S.acc = mab;
+      S.rq = (int)cab;
+    }
+    __syncthreads();
+    if (w == 0) {
+      kh_walk(hist, S.wq, (uint32_t)S.rq, S.acc, true, 0u, Y, m, c, S);
+      __syncwarp();
+      if (l == 0) S.cq = (int)((Y - S.Mcut) / S.Wcut) + 1;
     }
     __syncthreads();
   }
   // the histogram is not read again for this row
-  for (int wd = w0; wd < w1; ++wd) hist[wd] = 0u;
+  for (int wd = tid; wd < KH_NW; wd += KT) hist[wd] = 0u;
+  KH_MARK(item, 3);
   if (res.flags != 0u) return res;
 
   unsigned long long Zk = Ztot;
+  // a target row's candidate list holds every kept token when the cut lies
+  // within D of the maximum and the list did not overflow
+  const uint32_t ncand = target ? S.ccount : 0u;
+  bool listed = false;
   if (topk || topp) {
     const int cbin = S.cbin, q = S.cq, ccnt = S.ccnt;
     Zk = S.Mcut + (unsigned long long)q * S.Wcut;
+    listed = target && ncand <= (uint32_t)KH_LCAP && cbin != KH_OFF && kh_value(cbin) >= m - D;
     if (q >= ccnt || S.Wcut == 0ull) {
       // the whole bin is kept (zero-weight tokens have p = 0 either way)
       if (cbin == KH_OFF) {
@@ -408,11 +599,45 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
       res.flags = KH_BAIL;                            // unequal logits share the bin
       return res;
     } else {
-      const uint32_t hb = __float_as_uint(kh_value(cbin)) >> 16;
       res.zt = kh_value(cbin);
-      res.idcut = kh_tie(src, nv, hb, q, S);
-      if (res.idcut < 0) res.flags = KH_BAIL;
+      res.pad[0] = (uint32_t)q;
+      const uint32_t hb = __float_as_uint(res.zt) >> 16;
+      if (defer_tie) {
+        res.idcut = KH_DEFER;
+      } else if (listed) {
+        // the q-th lowest id among the listed tokens on the cut value
+        if (tid == 0) S.idcut = -1;
+        __syncthreads();
+        for (uint32_t e = tid; e < ncand; e += KT) {
+          const unsigned long long x = clist[e];
+          if ((uint32_t)(x >> 32) != hb) continue;
+          const uint32_t id = (uint32_t)x;
+          int rank = 0;
+          for (uint32_t f = 0; f < ncand; ++f) {
+            const unsigned long long y = clist[f];
+            rank += ((uint32_t)(y >> 32) == hb && (uint32_t)y < id) ? 1 : 0;
+          }
+          if (rank == q - 1) S.idcut = (int)id;
+        }
+        __syncthreads();
+        res.idcut = S.idcut;
+        if (res.idcut < 0) res.flags = KH_BAIL;
+      } else {
+        res.idcut = kh_tie(src, nv, hb, q, S);
+        if (res.idcut < 0) res.flags = KH_BAIL;
+      }
     }
+  }
+  if (listed && res.flags == 0u) {
+    // the kept tokens, in no particular order
+    for (uint32_t e = tid; e < ncand; e += KT) {
+      const unsigned long long x = clist[e];
+      const int id = (int)(uint32_t)x;
+      if (kh_kept(__uint_as_float((uint32_t)(x >> 32) << 16), id, res.zt, res.idcut))
+        glist[atomicAdd(&S.gcount, 1u)] = (uint32_t)id;
+    }
+    __syncthreads();
+    res.pad[1] = S.gcount;
   }
   res.invZ = __fdiv_rn(17592186044416.0f, (float)Zk);   // 2^44 / Z
   return res;
@@ -420,8 +645,8 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
 
 // Sampling weights of one token: r = (p - q)+ and p, both 0 outside the
 // target's kept set (probabilities in fp32, as 2^44-frame weights times 1/Z).
-__device__ __forceinline__ void kh_elem(float zp, float zq, int id, bool paired, const KhRow& tp,
-                                        const KhRow& tq, float* r, float* p) {
+__device__ __forceinline__ void kh_elem(float zp, float zq, int id, bool paired, KhW tp, KhW tq,
+                                        float* r, float* p) {
   *r = 0.0f;
   *p = 0.0f;
   if (kh_kept(zp, id, tp.zt, tp.idcut)) {
@@ -435,112 +660,164 @@ __device__ __forceinline__ void kh_elem(float zp, float zq, int id, bool paired,
 __device__ __forceinline__ float kh_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float kh_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
-// Fixed-point (2^-40) residual and target masses of the 8 tokens of vector v.
-__device__ __forceinline__ void kh_vec_sums(const uint4* sp, const uint4* sq, int v, bool paired,
-                                            const KhRow& tp, const KhRow& tq,
-                                            unsigned long long* R, unsigned long long* Pm) {
-  const uint4 a = kh_ld_l2(sp + v);
+// Fixed-point (2^-40) residual and target masses of the 8 tokens of vector v
+// (target logits a already loaded), for a vector holding a token of the
+// target's kept set. *dhit is set when such a token sits on the draft row's
+// cut value while that cut's id split is still deferred (its q is then not
+// known yet).
+#ifdef SV_TRACE
+__device__ unsigned long long g_khheavy;
+#endif
+__device__ __noinline__ void kh_vec_heavy(uint4 a, const uint4* sq, int v, bool paired, KhW tp,
+                                          KhW tq, unsigned long long* R, unsigned long long* Pm,
+                                          bool* dhit) {
+#ifdef SV_TRACE
+  atomicAdd(&g_khheavy, 1ull);
+#endif
+  uint4 bq = make_uint4(0u, 0u, 0u, 0u);
+  if (paired) bq = kh_ld_l2(sq + v);
   const uint32_t as[4] = {a.x, a.y, a.z, a.w};
-  // cheap test first: most tokens of a peaked target row are outside its kept set
-  bool any = false;
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    any |= kh_kept(kh_lo(as[k]), v * 8 + 2 * k, tp.zt, tp.idcut) |
-           kh_kept(kh_hi(as[k]), v * 8 + 2 * k + 1, tp.zt, tp.idcut);
-  *R = 0ull;
-  *Pm = 0ull;
-  if (!any) return;
-  uint4 b = make_uint4(0u, 0u, 0u, 0u);
-  if (paired) b = kh_ld_l2(sq + v);
-  const uint32_t bs[4] = {b.x, b.y, b.z, b.w};
+  const uint32_t bs[4] = {bq.x, bq.y, bq.z, bq.w};
   unsigned long long ra = 0, pa = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  bool hit = false;
+#pragma unroll 1
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t xa = as[e >> 1], xb = bs[e >> 1];
+    const float zp = (e & 1) ? kh_hi(xa) : kh_lo(xa);
+    const float zq = (e & 1) ? kh_hi(xb) : kh_lo(xb);
+    const int id = v * 8 + e;
     float r, p;
-    kh_elem(kh_lo(as[k]), kh_lo(bs[k]), v * 8 + 2 * k, paired, tp, tq, &r, &p);
+    kh_elem(zp, zq, id, paired, tp, tq, &r, &p);
     ra += fixr(r);
     pa += fixr(p);
-    kh_elem(kh_hi(as[k]), kh_hi(bs[k]), v * 8 + 2 * k + 1, paired, tp, tq, &r, &p);
-    ra += fixr(r);
-    pa += fixr(p);
+    hit |= paired && tq.idcut == KH_DEFER && zq == tq.zt && kh_kept(zp, id, tp.zt, tp.idcut);
   }
   *R = ra;
   *Pm = pa;
+  if (hit) *dhit = true;
+}
+// Whether vector a holds a logit >= zt (packed bf16 compares): a necessary
+// condition for a kept token; zt2 holds the cut value (a bf16 value) twice.
+__device__ __forceinline__ bool kh_vec_cand(const uint4& a, __nv_bfloat162 zt2) {
+  __nv_bfloat162 x0, x1, x2, x3;
+  memcpy(&x0, &a.x, 4);
+  memcpy(&x1, &a.y, 4);
+  memcpy(&x2, &a.z, 4);
+  memcpy(&x3, &a.w, 4);
+  return (__hge2_mask(x0, zt2) | __hge2_mask(x1, zt2) | __hge2_mask(x2, zt2) | __hge2_mask(x3, zt2)) != 0u;
 }
 
 // Inverse CDF in token-id order over (p - q)+ (paired) or p: the smallest id j
 // whose running sum S_j satisfies S_j * 2^24 > kv * S (S the total); when the
-// residual mass is 0 the target p is used. -1 if no token qualifies.
+// residual mass is 0 the target p is used. Every warp sums its contiguous id
+// range per 32-vector block; warp 0 locates the crossing block with two
+// lane-parallel scans and walks it. -1 if no token qualifies.
 __device__ __noinline__ int kh_sample(const uint4* sp, const uint4* sq, int nv, bool paired,
-                                      const KhRow& tp, const KhRow& tq, uint32_t kv,
-                                      KhShared& S) {
+                                      const KhW tp, const KhW tq, uint32_t kv, KhShared& S, int bt) {
   const int w = warp_id(), l = lane_id();
   const int cw = (nv + KWARP - 1) / KWARP;
+  const int nb = (cw + 31) / 32;
   const int a0 = min(w * cw, nv), a1 = min(a0 + cw, nv);
-  unsigned long long R = 0, Pm = 0;
-  for (int v = a0 + l; v < a1; v += 32) {
-    unsigned long long r, p;
-    kh_vec_sums(sp, sq, v, paired, tp, tq, &r, &p);
-    R += r;
-    Pm += p;
-  }
-  R = warp_sum(R);
-  Pm = warp_sum(Pm);
-  if (l == 0) {
-    S.s64[w] = R;
-    S.s64b[w] = Pm;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned long long SR = 0, SP = 0;
-    for (int i = 0; i < KWARP; ++i) {
-      SR += S.s64[i];
-      SP += S.s64b[i];
+  unsigned long long* bR = kh_blk0();
+  unsigned long long* bP = kh_blk1();
+  unsigned long long tR = 0, tP = 0;
+  bool dhit = false;
+  const __nv_bfloat162 zt2 = __float2bfloat162_rn(tp.zt);   // zt is a bf16 value
+  constexpr int U = 8;                          // target vectors in flight per lane
+  for (int j = 0; j < nb; j += U) {
+    uint4 av[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = a0 + (j + u) * 32 + l;
+      av[u] = (j + u < nb && v < a1) ? kh_ld_l2(sp + v) : make_uint4(0u, 0u, 0u, 0u);
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (j + u < nb) {
+        const int v = a0 + (j + u) * 32 + l;
+        const bool cand = v < a1 && kh_vec_cand(av[u], zt2);
+        unsigned long long r = 0, p = 0;
+        // blocks without a kept target token contribute nothing
+        if (__any_sync(0xffffffffu, cand)) {
+          if (cand) kh_vec_heavy(av[u], sq, v, paired, tp, tq, &r, &p, &dhit);
+          r = warp_sum(r);
+          p = warp_sum(p);
+        }
+        if (l == 0) {
+          bR[w * KH_MAXBLK + j + u] = r;
+          bP[w * KH_MAXBLK + j + u] = p;
+        }
+        tR += r;
+        tP += p;
+      }
+    }
+  }
+  if (l == 0) {
+    S.s64[w] = tR;
+    S.s64b[w] = tP;
+  }
+  if (__syncthreads_or(dhit ? 1 : 0)) return -2;   // the caller splits the draft cut first
+  KF_MARK(bt, 6);
+  if (w == 0) {
+    const unsigned long long oR = l < KWARP ? S.s64[l] : 0ull, oP = l < KWARP ? S.s64b[l] : 0ull;
+    const unsigned long long SR = warp_sum(oR), SP = warp_sum(oP);
     const bool useR = SR > 0ull;
     const unsigned long long St = useR ? SR : SP;
-    unsigned long long acc = 0;
-    S.wq = -1;
-    for (int i = 0; i < KWARP; ++i) {
-      const unsigned long long own = useR ? S.s64[i] : S.s64b[i];
-      if (mul_gt(acc + own, 1ull << 24, kv, St)) {
-        S.wq = i;
-        break;
-      }
-      acc += own;
+    const unsigned long long* bv = useR ? bR : bP;
+    const unsigned long long own = useR ? oR : oP;
+    unsigned long long incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (l >= o) incl += t;
     }
-    S.acc = acc;
-    S.useR = useR;
-    S.Mcut = St;
-    S.tok = -1;
-  }
-  __syncthreads();
-  if (w == S.wq) {
-    const bool useR = S.useR != 0;
-    const unsigned long long St = S.Mcut;
-    unsigned long long acc = S.acc;
-    for (int v0 = a0; v0 < a1; v0 += 32) {
-      const int v = v0 + l;
-      unsigned long long r = 0, p = 0;
-      if (v < a1) kh_vec_sums(sp, sq, v, paired, tp, tq, &r, &p);
-      const unsigned long long own = useR ? r : p;
-      unsigned long long incl = own;
+    const uint32_t bw = __ballot_sync(0xffffffffu, l < KWARP && mul_gt(incl, 1ull << 24, kv, St));
+    int tok = -1;
+    if (bw) {
+      const int ww = __ffs(bw) - 1;
+      unsigned long long acc = __shfl_sync(0xffffffffu, incl - own, ww);
+      const int wa0 = min(ww * cw, nv), wa1 = min(wa0 + cw, nv);
+      const unsigned long long b0 = 2 * l < nb ? bv[ww * KH_MAXBLK + 2 * l] : 0ull;
+      const unsigned long long b1 = 2 * l + 1 < nb ? bv[ww * KH_MAXBLK + 2 * l + 1] : 0ull;
+      unsigned long long bi = b0 + b1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (l >= o) incl += t;
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, bi, o);
+        if (l >= o) bi += t;
       }
-      const bool hit = v < a1 && mul_gt(acc + incl, 1ull << 24, kv, St);
-      const uint32_t bal = __ballot_sync(0xffffffffu, hit);
-      if (bal) {
-        if (l == __ffs(bal) - 1) {
+      const uint32_t bl = __ballot_sync(0xffffffffu, mul_gt(acc + bi, 1ull << 24, kv, St));
+      if (bl) {
+        const int lb = __ffs(bl) - 1;
+        acc += __shfl_sync(0xffffffffu, bi - b0 - b1, lb);
+        const unsigned long long lb0 = __shfl_sync(0xffffffffu, b0, lb);
+        int jb = 2 * lb;
+        if (!mul_gt(acc + lb0, 1ull << 24, kv, St)) {
+          acc += lb0;
+          ++jb;
+        }
+        // the block: one vector per lane, in id order
+        const int v = wa0 + jb * 32 + l;
+        unsigned long long r = 0, p = 0;
+        bool dh = false;
+        if (v < wa1) {
+          const uint4 a = kh_ld_l2(sp + v);
+          if (kh_vec_cand(a, zt2)) kh_vec_heavy(a, sq, v, paired, tp, tq, &r, &p, &dh);
+        }
+        const unsigned long long mine = useR ? r : p;
+        unsigned long long ci = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long t = __shfl_up_sync(0xffffffffu, ci, o);
+          if (l >= o) ci += t;
+        }
+        const uint32_t hit = __ballot_sync(0xffffffffu, v < wa1 && mul_gt(acc + ci, 1ull << 24, kv, St));
+        if (hit && l == __ffs(hit) - 1) {
           // walk this vector's tokens in id order
           const uint4 a = kh_ld_l2(sp + v);
           uint4 b = make_uint4(0u, 0u, 0u, 0u);
           if (paired) b = kh_ld_l2(sq + v);
           const uint32_t as[4] = {a.x, a.y, a.z, a.w}, bs[4] = {b.x, b.y, b.z, b.w};
-          unsigned long long run = acc + incl - own;
-          int tok = -1;
+          unsigned long long run = acc + ci - mine;
           for (int e = 0; e < 8 && tok < 0; ++e) {
             const uint32_t xa = as[e >> 1], xb = bs[e >> 1];
             const float zp = (e & 1) ? kh_hi(xa) : kh_lo(xa);
@@ -550,15 +827,105 @@ __device__ __noinline__ int kh_sample(const uint4* sp, const uint4* sq, int nv, 
             run += fixr(useR ? rr : pp);
             if (mul_gt(run, 1ull << 24, kv, St)) tok = v * 8 + e;
           }
-          S.tok = tok;
         }
-        break;
+        tok = __reduce_max_sync(0xffffffffu, tok);
       }
-      acc += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (l == 0) S.tok = tok;
   }
   __syncthreads();
   return S.tok;
+}
+
+// Exclusive sums in ascending thread order and the total.
+template <typename T>
+__device__ __forceinline__ T kh_below(T v, T* scratch, T* total) {
+  const int l = lane_id(), w = warp_id();
+  T incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (l >= o) incl += t;
+  }
+  __syncthreads();
+  if (l == 31) scratch[w] = incl;
+  __syncthreads();
+  T off = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < KWARP; ++i) {
+    const T s = scratch[i];
+    if (i < w) off += s;
+    tot += s;
+  }
+  *total = tot;
+  return off + incl - v;
+}
+
+// The inverse CDF of kh_sample over a target row whose kept tokens are listed
+// (L <= KH_LCAP ids, any order): only listed tokens carry p > 0, so the sums run
+// over the list sorted by id. Uses the histogram's shared memory as scratch and
+// zeroes it again. -2 when a listed token sits on the draft row's deferred cut
+// value (the caller splits that cut first), -1 if no token qualifies.
+__device__ __noinline__ int kh_sample_list(const unsigned short* zp_row, const unsigned short* zq_row,
+                                           const uint32_t* glist, int L, bool paired, KhW tp, KhW tq,
+                                           uint32_t kv, KhShared& S) {
+  const int tid = threadIdx.x;
+  uint32_t* ids = kh_dyn;                                          // [KH_LCAP]
+  unsigned long long* wr = reinterpret_cast<unsigned long long*>(kh_dyn + KH_LCAP);   // [KH_LCAP] r, sorted
+  unsigned long long* wp = wr + KH_LCAP;                           // [KH_LCAP] p, sorted
+  uint32_t* sid = reinterpret_cast<uint32_t*>(wp + KH_LCAP);       // [KH_LCAP] ids, sorted
+  bool dhit = false;
+  for (int e = tid; e < L; e += KT) ids[e] = __ldcg(glist + e);
+  __syncthreads();
+  for (int e = tid; e < L; e += KT) {
+    const int id = (int)ids[e];
+    const float zp = __uint_as_float((uint32_t)__ldcg(zp_row + id) << 16);
+    const float zq = paired ? __uint_as_float((uint32_t)__ldcg(zq_row + id) << 16) : 0.0f;
+    float r, p;
+    kh_elem(zp, zq, id, paired, tp, tq, &r, &p);
+    dhit |= paired && tq.idcut == KH_DEFER && zq == tq.zt;
+    int rank = 0;
+    for (int f = 0; f < L; ++f) rank += (int)(ids[f] < (uint32_t)id);
+    wr[rank] = fixr(r);
+    wp[rank] = fixr(p);
+    sid[rank] = (uint32_t)id;
+  }
+  const bool redo = __syncthreads_or(dhit ? 1 : 0) != 0;
+  int tok = -2;
+  if (!redo) {
+    // two consecutive sorted entries per thread
+    const int e0 = 2 * tid;
+    unsigned long long r2 = 0, p2 = 0;
+    if (e0 < L) {
+      r2 += wr[e0];
+      p2 += wp[e0];
+    }
+    if (e0 + 1 < L) {
+      r2 += wr[e0 + 1];
+      p2 += wp[e0 + 1];
+    }
+    unsigned long long SR, SP;
+    const unsigned long long xr = kh_below<unsigned long long>(r2, S.s64, &SR);
+    const unsigned long long xp = kh_below<unsigned long long>(p2, S.s64b, &SP);
+    const bool useR = SR > 0ull;
+    const unsigned long long St = useR ? SR : SP;
+    if (tid == 0) S.tok = -1;
+    __syncthreads();
+    unsigned long long run = useR ? xr : xp;
+    for (int e = e0; e < min(e0 + 2, L); ++e) {
+      const unsigned long long own = useR ? wr[e] : wp[e];
+      if (!mul_gt(run, 1ull << 24, kv, St) && mul_gt(run + own, 1ull << 24, kv, St)) S.tok = (int)sid[e];
+      run += own;
+    }
+    __syncthreads();
+    tok = S.tok;
+  }
+  // restore the histogram's zeros
+  uint4* z4 = reinterpret_cast<uint4*>(kh_dyn);
+  const int n16 = (KH_LCAP * 4 + 2 * KH_LCAP * 8 + KH_LCAP * 4) / 16;
+  for (int t = tid; t < n16; t += KT) z4[t] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  return tok;
 }
 
 __device__ __forceinline__ float kh_ldz(const void* rows, size_t row, int V, int id) {
@@ -581,18 +948,50 @@ __device__ __forceinline__ KhRow kh_load_row(const KhRow* p) {
   return r;
 }
 
+// Number of tokens with id < id_end whose logit pattern is hb (CTA-wide).
+__device__ __noinline__ uint32_t kh_rank_before(const uint4* src, int id_end, uint32_t hb, KhShared& S) {
+  const int nfull = id_end / 8, rem = id_end % 8;
+  uint32_t n = 0;
+  for (int v = threadIdx.x; v < nfull; v += KT) n += __popc(kh_match8(kh_ld_l2(src + v), hb));
+  if (threadIdx.x == 0 && rem) n += __popc(kh_match8(kh_ld_l2(src + nfull), hb) & ((1u << rem) - 1u));
+  n = warp_sum(n);
+  __syncthreads();
+  if (lane_id() == 0) S.s32[warp_id()] = n;
+  __syncthreads();
+  uint32_t t = 0;
+#pragma unroll
+  for (int i = 0; i < KWARP; ++i) t += S.s32[i];
+  __syncthreads();
+  return t;
+}
+
+// Clears the kept-token lists of sequence b's target rows (the call leaves the
+// workspace zeroed); reads their lengths from the row results.
+__device__ __noinline__ void kh_clear_lists(const Params& P, int b, const KhRow* rr) {
+  for (int r = 0; r <= P.K; ++r) {
+    const uint32_t L = __ldcg(&rr[r].pad[1]);
+    if (L == KH_NOLIST || L == 0u) continue;
+    uint32_t* gl = P.ws_lists + ((size_t)b * (P.K + 1) + r) * KH_LCAP;
+    for (uint32_t e = threadIdx.x; e < L && e < (uint32_t)KH_LCAP; e += KT) gl[e] = 0u;
+  }
+}
+
 // The sequence's rows are all done: acceptance in order, then the replacement
 // or bonus token; writes the outputs (or hands the sequence to the cluster
 // kernel) and re-arms the ticket.
 __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
   const int K = P.K, R2 = 2 * K + 1, tid = threadIdx.x;
   const KhRow* rr = P.ws_rowres + (size_t)b * R2;
+  const __nv_bfloat16* tgt = static_cast<const __nv_bfloat16*>(P.rows0) + (size_t)b * (K + 1) * P.V;
+  const __nv_bfloat16* drf = static_cast<const __nv_bfloat16*>(P.rows1) + (size_t)b * K * P.V;
+  KF_MARK(b, 0);
   if (tid < 32) {
     uint32_t f = 0;
     for (int r = tid; r < R2; r += 32) f |= __ldcg(&rr[r].flags);
 #pragma unroll
     for (int o = 16; o; o >>= 1) f |= __shfl_xor_sync(0xffffffffu, f, o);
     uint32_t ok = 1u;
+    bool need = false;
     if (tid < K && !(f & (KH_ERR | KH_BAIL))) {
       const int i = tid;
       const int d = P.dtok[(size_t)b * K + i];
@@ -600,19 +999,51 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
       const float zp = kh_ldz(P.rows0, (size_t)b * (K + 1) + i, P.V, d);
       const float zq = kh_ldz(P.rows1, (size_t)b * K + i, P.V, d);
       const float p = kh_kept(zp, d, tp.zt, tp.idcut) ? __fmul_rn(kh_w(zp, tp.m, tp.c), tp.invZ) : 0.0f;
-      const float q = kh_kept(zq, d, tq.zt, tq.idcut) ? __fmul_rn(kh_w(zq, tq.m, tq.c), tq.invZ) : 0.0f;
+      const float qw = __fmul_rn(kh_w(zq, tq.m, tq.c), tq.invZ);
+      // d on the draft's cut value with the id split deferred: kept iff fewer
+      // than quota tokens on that value precede it (counted below)
+      need = tq.idcut == KH_DEFER && zq == tq.zt;
+      const float q = kh_kept(zq, d, tq.zt, tq.idcut) ? qw : 0.0f;
       uint32_t ku, kv;
       philox_uniform_bits(P.seed, P.offset, (uint32_t)b, (uint32_t)i, &ku, &kv);
       ok = __fmul_rn((float)ku * 5.9604644775390625e-08f, q) < p ? 1u : 0u;
+      S.pz[i] = p;
+      S.qz[i] = qw;
+      S.ku[i] = ku;
+      S.flag[i] = ok;
     }
-    const uint32_t rej = __ballot_sync(0xffffffffu, tid < K && !ok);
+    const uint32_t nm = __ballot_sync(0xffffffffu, need);
     if (tid == 0) {
       S.flags = (int)f;
-      S.nacc = rej ? __ffs(rej) - 1 : K;
+      S.need = nm;
     }
   }
   __syncthreads();
-  const int flags = S.flags, n = S.nacc;
+  const int flags = S.flags;
+  for (uint32_t nm = S.need; nm; nm &= nm - 1u) {
+    const int i = __ffs(nm) - 1;
+    const KhRow tq = kh_load_row(rr + K + 1 + i);
+    const int d = P.dtok[(size_t)b * K + i];
+    const uint32_t hb = __float_as_uint(tq.zt) >> 16;
+    const uint32_t rank = kh_rank_before(reinterpret_cast<const uint4*>(drf + (size_t)i * P.V), d, hb, S);
+    if (tid == 0) {
+      const float q = rank < tq.pad[0] ? S.qz[i] : 0.0f;
+      S.flag[i] = __fmul_rn((float)S.ku[i] * 5.9604644775390625e-08f, q) < S.pz[i] ? 1u : 0u;
+    }
+  }
+  if (tid == 0) {
+    int n = K;
+    for (int i = 0; i < K; ++i)
+      if (!S.flag[i]) {
+        n = i;
+        break;
+      }
+    S.nacc = n;
+  }
+  __syncthreads();
+  const int n = S.nacc;
+  KF_MARK(b, 1);
+  KF_SET(b, 5, n);
   if (flags & KH_BAIL) {
     // the cluster kernel serves the sequence and clears the flag
     if (tid == 0) {
@@ -620,6 +1051,8 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
       atomicOr(P.ws_work, 1u);
       P.ws_tickets[b] = 0u;
     }
+    kh_clear_lists(P, b, rr);
+    __syncthreads();
     uint4* rz = reinterpret_cast<uint4*>(P.ws_rowres + (size_t)b * R2);
     for (int t = tid; t < 2 * R2; t += KT) rz[t] = make_uint4(0u, 0u, 0u, 0u);
     return;
@@ -628,16 +1061,28 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
   if (!(flags & KH_ERR)) {
     const bool paired = n < K;
     const KhRow tp = kh_load_row(rr + n);
-    const KhRow tq = paired ? kh_load_row(rr + K + 1 + n) : tp;
+    KhRow tq = paired ? kh_load_row(rr + K + 1 + n) : tp;
     uint32_t ku, kv;
     philox_uniform_bits(P.seed, P.offset, (uint32_t)b, (uint32_t)n, &ku, &kv);
     const int nv = P.V / 8;
-    const uint4* sp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.rows0) +
-                                                     ((size_t)b * (K + 1) + n) * P.V);
-    const uint4* sq = paired ? reinterpret_cast<const uint4*>(
-                                   static_cast<const __nv_bfloat16*>(P.rows1) + ((size_t)b * K + n) * P.V)
-                             : sp;
-    tok = kh_sample(sp, sq, nv, paired, tp, tq, kv, S);
+    const uint4* sp = reinterpret_cast<const uint4*>(tgt + (size_t)n * P.V);
+    const uint4* sq = paired ? reinterpret_cast<const uint4*>(drf + (size_t)n * P.V) : sp;
+    KhW wq = kh_wof(tq);
+    const uint32_t L = tp.pad[1];
+    const uint32_t* glist = P.ws_lists + ((size_t)b * (K + 1) + n) * KH_LCAP;
+    const unsigned short* zpr = reinterpret_cast<const unsigned short*>(sp);
+    const unsigned short* zqr = reinterpret_cast<const unsigned short*>(sq);
+    if (L != KH_NOLIST) tok = kh_sample_list(zpr, zqr, glist, (int)L, paired, kh_wof(tp), wq, kv, S);
+    else tok = kh_sample(sp, sq, nv, paired, kh_wof(tp), wq, kv, S, b);
+    KF_MARK(b, 2);
+    KF_SET(b, 4, tok == -2 ? 1 : 0);
+    if (tok == -2) {
+      // a token of the target's kept set sits on the draft's deferred cut value
+      wq.idcut = kh_tie(sq, nv, __float_as_uint(tq.zt) >> 16, (int)tq.pad[0], S);
+      if (wq.idcut < 0) tok = -1;
+      else if (L != KH_NOLIST) tok = kh_sample_list(zpr, zqr, glist, (int)L, paired, kh_wof(tp), wq, kv, S);
+      else tok = kh_sample(sp, sq, nv, paired, kh_wof(tp), wq, kv, S, b);
+    }
   }
   if (tid == 0) {
     const bool bad = (flags & KH_ERR) || tok < 0;
@@ -648,15 +1093,18 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
     P.ws_tickets[b] = 0u;
   }
   // the call leaves the workspace zeroed
+  kh_clear_lists(P, b, rr);
+  __syncthreads();
   uint4* rz = reinterpret_cast<uint4*>(P.ws_rowres + (size_t)b * R2);
   for (int t = tid; t < 2 * R2; t += KT) rz[t] = make_uint4(0u, 0u, 0u, 0u);
+  KF_MARK(b, 3);
 }
 
 // Persistent CTAs take rows of the batch's sampled sequences from a work counter
 // (sequence-major, so a sequence's rows finish close together and its sampling
 // pass finds them in L2). Rows of other sequences are skipped.
 __global__ void __launch_bounds__(KT, 2) keyhist_kernel(const Params P, int nitems) {
-  extern __shared__ __align__(16) uint32_t kh_hist[];
+  uint32_t* kh_hist = kh_dyn;
   __shared__ KhShared S;
   const int tid = threadIdx.x;
   const int K = P.K, R2 = 2 * K + 1;
@@ -669,21 +1117,35 @@ __global__ void __launch_bounds__(KT, 2) keyhist_kernel(const Params P, int nite
     if (item >= nitems) break;
     const int b = item / R2, r = item - b * R2;
     if (!fast_seq(P, b)) continue;
+    KH_MARK(item, 0);
+#ifdef SV_TRACE
+    if (tid == 0 && item < 4096) {
+      uint32_t smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      g_khtrace[item * 8 + 7] = smid;
+    }
+#endif
     const __nv_bfloat16* row =
         r <= K ? static_cast<const __nv_bfloat16*>(P.rows0) + ((size_t)b * (K + 1) + r) * P.V
                : static_cast<const __nv_bfloat16*>(P.rows1) + ((size_t)b * K + (r - K - 1)) * P.V;
-    const KhRow res = kh_row(row, P.V, P.temp[b], P.topk[b], P.topp[b], kh_hist, S);
+    uint32_t* glist = r <= K ? P.ws_lists + ((size_t)b * (K + 1) + r) * KH_LCAP : nullptr;
+    const KhRow res = kh_row(row, P.V, P.temp[b], P.topk[b], P.topp[b], r <= K, kh_hist, S, glist, item);
+    KH_MARK(item, 4);
     if (tid == 0) {
       uint4* dst = reinterpret_cast<uint4*>(P.ws_rowres + item);
       dst[0] = make_uint4(__float_as_uint(res.zt), __float_as_uint(res.invZ), __float_as_uint(res.m),
                           __float_as_uint(res.c));
-      dst[1] = make_uint4((uint32_t)res.idcut, res.flags, 0u, 0u);
+      dst[1] = make_uint4((uint32_t)res.idcut, res.flags, res.pad[0], res.pad[1]);
       __threadfence();
       S.last = atomicAdd(&P.ws_tickets[b], 1u) == (unsigned int)(R2 - 1);
       if (S.last) __threadfence();
     }
     __syncthreads();
-    if (S.last) kh_finalize(P, b, S);
+    if (S.last) {
+      KH_MARK(item, 5);
+      kh_finalize(P, b, S);
+      KH_MARK(item, 6);
+    }
     __syncthreads();
   }
   // the last CTA to leave re-arms the work counter for the next call

@@ -96,6 +96,7 @@ struct Params {
   unsigned int* ws_fb;          // keyhist_kernel: 1 = sequence handed to the cluster kernel
   unsigned int* ws_fnext;       // keyhist_kernel: work counter
   unsigned int* ws_fdone;       // keyhist_kernel: CTAs finished
+  uint32_t* ws_lists;           // keyhist_kernel: kept-token ids of target rows [B][K+1][1024]
 };
 
 struct Meta {
@@ -2063,8 +2064,9 @@ size_t spec_verify_workspace_bytes(int B, int K) {
   const size_t rows = (size_t)B * (K + 1);
   const size_t tickets = ((size_t)B * sizeof(unsigned int) + 15) & ~(size_t)15;
   const size_t head = rows * 8 + tickets + 16 + rows * 8 + rows * 4 + rows * 4;
-  // keyhist_kernel: hand-back flags, row results, work counter
-  return ((head + 15) & ~(size_t)15) + tickets + (size_t)B * (2 * K + 1) * sizeof(KhRow) + 16;
+  // keyhist_kernel: hand-back flags, row results, work counter, kept-token lists
+  return ((head + 15) & ~(size_t)15) + tickets + (size_t)B * (2 * K + 1) * sizeof(KhRow) + 16 +
+         rows * KH_LCAP * sizeof(uint32_t);
 }
 
 sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
@@ -2123,6 +2125,7 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
     char* w4 = w3 + tickets + (size_t)B * (2 * K + 1) * sizeof(KhRow);
     p.ws_fnext = reinterpret_cast<unsigned int*>(w4);
     p.ws_fdone = reinterpret_cast<unsigned int*>(w4 + 4);
+    p.ws_lists = reinterpret_cast<uint32_t*>(w4 + 16);
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // temperature-0 units: streaming reduction; the cluster kernel takes the rest
@@ -2258,6 +2261,25 @@ int sv_version(void) { return 300; }
 int sv_trace_reset(void) {
   static unsigned long long zero[64 * 32 + 16];
   return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
+}
+int kh_trace_reset(void) {
+  static unsigned long long zero[4096 * 8];
+  if (cudaMemcpyToSymbol(g_khtrace, zero, sizeof(zero)) != cudaSuccess) return 1;
+  if (cudaMemcpyToSymbol(g_khheavy, zero, sizeof(unsigned long long)) != cudaSuccess) return 1;
+  return cudaMemcpyToSymbol(g_kftrace, zero, 1024 * 8 * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
+}
+unsigned long long kh_heavy_count(void) {
+  unsigned long long v = 0;
+  cudaMemcpyFromSymbol(&v, g_khheavy, sizeof(v));
+  return v;
+}
+int kf_trace_copy(unsigned long long* host, size_t n) {
+  if (n > 1024 * 8) n = 1024 * 8;
+  return cudaMemcpyFromSymbol(host, g_kftrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
+}
+int kh_trace_copy(unsigned long long* host, size_t n) {
+  if (n > 4096 * 8) n = 4096 * 8;
+  return cudaMemcpyFromSymbol(host, g_khtrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
 }
 int sv_trace_copy(unsigned long long* host, size_t n) {
   if (n > 64 * 32 + 16) n = 64 * 32 + 16;
