@@ -30,7 +30,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_NAME = "sv_kernel"          # dominant kernel of sampling workloads
+KERNEL_NAME = "keyhist_kernel"     # dominant kernel of sampled bf16 workloads
+CLUSTER_KERNEL = "sv_kernel"       # dominant kernel of sampled fp32 workloads
 GREEDY_KERNEL = "greedy_kernel"    # dominant kernel of temperature-0 workloads
 
 
@@ -61,7 +62,24 @@ def source_hash() -> str:
 
 
 def dominant_kernel(workload: str) -> str:
-    return GREEDY_KERNEL if workload == "greedy" else KERNEL_NAME
+    from speculative_decoding_verification_30_gb300.workloads import WORKLOADS
+    w = WORKLOADS[workload]
+    if workload == "greedy":
+        return GREEDY_KERNEL
+    keyhist = str(w.dtype).endswith("bfloat16") and w.B * (w.K + 1) >= 16
+    return KERNEL_NAME if keyhist else CLUSTER_KERNEL
+
+
+def launches_per_call(workload: str) -> int:
+    """Kernels one spec_verify call launches on this workload's 16-byte aligned rows:
+    greedy_kernel, then (with draft logits) keyhist_kernel for bf16 rows and the
+    cluster kernel sv_kernel."""
+    from speculative_decoding_verification_30_gb300.workloads import WORKLOADS
+    w = WORKLOADS[workload]
+    if workload == "greedy":
+        return 1                                   # no draft logits: greedy_kernel alone
+    keyhist = str(w.dtype).endswith("bfloat16") and w.B * (w.K + 1) >= 16
+    return 3 if keyhist else 2
 
 
 def profiled_traffic(workload: str):
@@ -276,9 +294,7 @@ def bench_gpu(args):
                      "timing": "CUDA events around each spec_verify call (all kernels of "
                                "the call), so the dominant kernel's own fraction is at "
                                "least this"},
-        # per call: greedy_kernel (temperature-0 rows), greedy_finalize, sv_kernel
-        # (clusters); rows are 16-byte aligned here, so all three launch
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches_per_call(w.name) * args.steps,
         "e2e": e2e,
         "clocks": clk.summary(),
     }

@@ -1218,9 +1218,10 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
   const int vlen = max(0, min(P.slice, P.V - base));
   const int nvec = (int)(slot_bytes / 16);
   int nmine = cid < P.nunits ? (P.nunits - 1 - cid) / ncl + 1 : 0;
-  // verify batches whose units are all temperature 0: nothing to do here
+  // verify batches whose units are all served by greedy_kernel or keyhist_kernel:
+  // nothing to do here (every CTA reads the same flag, so none waits on another)
   if (MODE == MODE_VERIFY && P.greedy_split && *reinterpret_cast<volatile unsigned int*>(P.ws_work) == 0u)
-    nmine = 0;
+    return;
   const uint32_t copy_bytes = (uint32_t)((size_t)vlen * sizeof(DT));
   const uint64_t pol = policy_evict_first();
 
@@ -1826,6 +1827,19 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
   int item = blockIdx.x, row = 0, nrow = 0;
   bool ok = false, nok = false;
   if (item < nitems) greedy_load<DT>(P, item, G, chunk, cur, &row, &ok);
+  // a batch without temperature-0 sequences: only the cluster kernel's work
+  // flag is left to set (for sequences keyhist_kernel does not serve)
+  // (checked only by CTAs whose first row is not on the greedy path)
+  bool zt = ok;
+  if (!__syncthreads_or(ok ? 1 : 0))
+    for (int b = tid; b < P.B; b += NT) zt |= P.temp[b] == 0.0f;
+  if (!__syncthreads_or(zt ? 1 : 0) && !P.greedy_only) {
+    bool other = false;
+    if (blockIdx.x == 0)
+      for (int b = tid; b < P.B; b += NT) other |= !(P.fast_split && fast_seq(P, b));
+    if (__syncthreads_or(other ? 1 : 0) && tid == 0) atomicOr(P.ws_work, 1u);
+    return;
+  }
   while (item < nitems) {
     const int next = item + (int)gridDim.x;
     if (next < nitems) greedy_load<DT>(P, next, G, chunk, nxt, &nrow, &nok);
@@ -2134,8 +2148,10 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
     // without draft logits every sequence must be greedy (others are data
     // errors), so the greedy kernel alone serves the batch
     p.greedy_only = draft_logits == nullptr ? 1 : 0;
-    // sampled bf16 sequences: one-pass key-histogram kernel
-    p.fast_split = (dtype == SV_BF16 && draft_logits != nullptr) ? 1 : 0;
+    // sampled bf16 sequences: one-pass key-histogram kernel, one CTA per row;
+    // batches of fewer units than the cluster kernel runs clusters keep each
+    // row spread over a cluster of SMs instead
+    p.fast_split = (dtype == SV_BF16 && draft_logits != nullptr && (long long)B * (K + 1) >= 16) ? 1 : 0;
     const int PV = 16 / (int)es;
     const int cmax = GV * NT * PV;
     const int G = (V + cmax - 1) / cmax;
