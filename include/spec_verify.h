@@ -118,8 +118,9 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
  * budget and allow no allocation while a decode step runs.
  *   - Nothing is allocated: no cudaMalloc/cudaFree and no allocating library call.
  *   - Limit: spec_verify_workspace_bytes(B, K) must not exceed
- *     SV_NOALLOC_SCRATCH_BYTES; larger batches return SV_ERR_SCRATCH and launch
- *     nothing (use spec_verify with a workspace).
+ *     SV_NOALLOC_SCRATCH_BYTES (B <= 189 at K = 4, B <= 55 at K = 16); larger
+ *     batches return SV_ERR_SCRATCH and launch nothing (use spec_verify with a
+ *     workspace).
  *   - The scratch is zero when the library loads, and each call leaves it zero
  *     again; a call must run to completion before the next one starts.
  *   - The first call on a device looks up the scratch's device address with that

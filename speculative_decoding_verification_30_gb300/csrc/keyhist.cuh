@@ -40,7 +40,8 @@ constexpr size_t KH_SMEM = KH_HIST_BYTES + 2 * (size_t)KWARP * KH_MAXBLK * 8;
 constexpr float KH_LOG2E = 1.44269504088896341f;
 
 constexpr uint32_t KH_ERR = 1u, KH_BAIL = 2u;
-constexpr int KH_LCAP = 1024;                             // listed kept tokens per target row
+constexpr int KH_LCAP = 1024;                             // window candidates per target row
+constexpr int KH_KCAP = 256;                              // kept-token list per target row (workspace)
 constexpr uint32_t KH_NOLIST = 0xFFFFFFFFu;
 constexpr float KH_LIST_BITS = 12.0f;                     // listed: weight >= 2^-12 of the maximum
 
@@ -585,7 +586,10 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   if (topk || topp) {
     const int cbin = S.cbin, q = S.cq, ccnt = S.ccnt;
     Zk = S.Mcut + (unsigned long long)q * S.Wcut;
-    listed = target && ncand <= (uint32_t)KH_LCAP && cbin != KH_OFF && kh_value(cbin) >= m - D;
+    // kept tokens: those before the cut bin plus the bin's quota
+    const int nkept = S.kq + min(q, ccnt);
+    listed = target && ncand <= (uint32_t)KH_LCAP && cbin != KH_OFF && kh_value(cbin) >= m - D &&
+             nkept <= KH_KCAP;
     if (q >= ccnt || S.Wcut == 0ull) {
       // the whole bin is kept (zero-weight tokens have p = 0 either way)
       if (cbin == KH_OFF) {
@@ -971,8 +975,8 @@ __device__ __noinline__ void kh_clear_lists(const Params& P, int b, const KhRow*
   for (int r = 0; r <= P.K; ++r) {
     const uint32_t L = __ldcg(&rr[r].pad[1]);
     if (L == KH_NOLIST || L == 0u) continue;
-    uint32_t* gl = P.ws_lists + ((size_t)b * (P.K + 1) + r) * KH_LCAP;
-    for (uint32_t e = threadIdx.x; e < L && e < (uint32_t)KH_LCAP; e += KT) gl[e] = 0u;
+    uint32_t* gl = P.ws_lists + ((size_t)b * (P.K + 1) + r) * KH_KCAP;
+    for (uint32_t e = threadIdx.x; e < L && e < (uint32_t)KH_KCAP; e += KT) gl[e] = 0u;
   }
 }
 
@@ -1069,7 +1073,7 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
     const uint4* sq = paired ? reinterpret_cast<const uint4*>(drf + (size_t)n * P.V) : sp;
     KhW wq = kh_wof(tq);
     const uint32_t L = tp.pad[1];
-    const uint32_t* glist = P.ws_lists + ((size_t)b * (K + 1) + n) * KH_LCAP;
+    const uint32_t* glist = P.ws_lists + ((size_t)b * (K + 1) + n) * KH_KCAP;
     const unsigned short* zpr = reinterpret_cast<const unsigned short*>(sp);
     const unsigned short* zqr = reinterpret_cast<const unsigned short*>(sq);
     if (L != KH_NOLIST) tok = kh_sample_list(zpr, zqr, glist, (int)L, paired, kh_wof(tp), wq, kv, S);
@@ -1128,7 +1132,7 @@ __global__ void __launch_bounds__(KT, 2) keyhist_kernel(const Params P, int nite
     const __nv_bfloat16* row =
         r <= K ? static_cast<const __nv_bfloat16*>(P.rows0) + ((size_t)b * (K + 1) + r) * P.V
                : static_cast<const __nv_bfloat16*>(P.rows1) + ((size_t)b * K + (r - K - 1)) * P.V;
-    uint32_t* glist = r <= K ? P.ws_lists + ((size_t)b * (K + 1) + r) * KH_LCAP : nullptr;
+    uint32_t* glist = r <= K ? P.ws_lists + ((size_t)b * (K + 1) + r) * KH_KCAP : nullptr;
     const KhRow res = kh_row(row, P.V, P.temp[b], P.topk[b], P.topp[b], r <= K, kh_hist, S, glist, item);
     KH_MARK(item, 4);
     if (tid == 0) {

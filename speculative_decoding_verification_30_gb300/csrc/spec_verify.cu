@@ -96,7 +96,7 @@ struct Params {
   unsigned int* ws_fb;          // keyhist_kernel: 1 = sequence handed to the cluster kernel
   unsigned int* ws_fnext;       // keyhist_kernel: work counter
   unsigned int* ws_fdone;       // keyhist_kernel: CTAs finished
-  uint32_t* ws_lists;           // keyhist_kernel: kept-token ids of target rows [B][K+1][1024]
+  uint32_t* ws_lists;           // keyhist_kernel: kept-token ids of target rows [B][K+1][256]
 };
 
 struct Meta {
@@ -2080,7 +2080,7 @@ size_t spec_verify_workspace_bytes(int B, int K) {
   const size_t head = rows * 8 + tickets + 16 + rows * 8 + rows * 4 + rows * 4;
   // keyhist_kernel: hand-back flags, row results, work counter, kept-token lists
   return ((head + 15) & ~(size_t)15) + tickets + (size_t)B * (2 * K + 1) * sizeof(KhRow) + 16 +
-         rows * KH_LCAP * sizeof(uint32_t);
+         rows * KH_KCAP * sizeof(uint32_t);
 }
 
 sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
