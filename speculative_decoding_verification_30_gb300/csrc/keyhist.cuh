@@ -159,6 +159,7 @@ struct KhShared {
   int item, last, flags, idcut, wq, rq;
   int nacc, tok, useR;
   uint32_t need;                       // positions whose acceptance waits for a draft id split
+  uint32_t llen[17];                   // kept-list lengths of the sequence's target rows
   uint32_t cmax;                       // collection: running block maximum (order-preserving key)
   uint32_t ccount;                     // collection: candidates pushed
   uint32_t gcount;                     // collection: kept tokens written out
@@ -166,6 +167,48 @@ struct KhShared {
   float pz[16], qz[16];                // p(d), and q(d) if d is kept
   uint32_t ku[16];
 };
+
+// Exclusive sums of a count and a mass in descending thread order (thread KT-1
+// first), and their totals, in one pass.
+__device__ __forceinline__ void kh_above2(uint32_t c, unsigned long long m, KhShared& S,
+                                          uint32_t* cab, uint32_t* ctot,
+                                          unsigned long long* mab, unsigned long long* mtot) {
+  const int l = lane_id(), w = warp_id();
+  uint32_t ic = c;
+  unsigned long long im = m;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t tc = __shfl_down_sync(0xffffffffu, ic, o);
+    const unsigned long long tm = __shfl_down_sync(0xffffffffu, im, o);
+    if (l + o < 32) {
+      ic += tc;
+      im += tm;
+    }
+  }
+  __syncthreads();
+  if (l == 0) {
+    S.s32[w] = ic;
+    S.s64[w] = im;
+  }
+  __syncthreads();
+  uint32_t oc = 0, tc = 0;
+  unsigned long long om = 0, tm = 0;
+#pragma unroll
+  for (int i = 0; i < KWARP; ++i) {
+    const uint32_t sc = S.s32[i];
+    const unsigned long long sm = S.s64[i];
+    if (i > w) {
+      oc += sc;
+      om += sm;
+    }
+    tc += sc;
+    tm += sm;
+  }
+  *cab = oc + ic - c;
+  *ctot = tc;
+  *mab = om + im - m;
+  *mtot = tm;
+}
 
 // Exclusive sums in descending thread order (thread KT-1 first) and the total.
 template <typename T>
@@ -506,9 +549,7 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   // sweep, words interleaved over the threads (occupied bins cluster in a few
   // value ranges): counts and fixed-point masses, added to the word's thread range
   uint32_t bad = 0;
-  for (int wd = tid; wd < KH_NW; wd += KT) {
-    const uint32_t x = hist[wd];
-    if (x == 0u) continue;
+  auto sweep_word = [&](int wd, uint32_t x) {
     const uint32_t chi = x >> 16, clo = x & 0xFFFFu;
     const int i0 = 2 * wd;
     if ((clo && (i0 < KH_NINF || i0 >= KH_PINF)) || (chi && (i0 + 1 < KH_NINF || i0 + 1 >= KH_PINF)))
@@ -518,14 +559,25 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
     const int r = wd / KH_WPT;
     atomicAdd(&rcnt[r], chi + clo);
     if (mw) atomicAdd(&rmass[r], mw);
+  };
+  // four words per 16-byte load; the last word (an odd count) separately
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist);
+  for (int v4 = tid; v4 < KH_NW / 4; v4 += KT) {
+    const uint4 x = h4[v4];
+    if ((x.x | x.y | x.z | x.w) == 0u) continue;
+    if (x.x) sweep_word(4 * v4, x.x);
+    if (x.y) sweep_word(4 * v4 + 1, x.y);
+    if (x.z) sweep_word(4 * v4 + 2, x.z);
+    if (x.w) sweep_word(4 * v4 + 3, x.w);
   }
+  for (int wd = (KH_NW / 4) * 4 + tid; wd < KH_NW; wd += KT)
+    if (hist[wd]) sweep_word(wd, hist[wd]);
   const int anyb = __syncthreads_or((int)bad);
   const uint32_t cnt = rcnt[tid];
-  const unsigned long long mass = bad ? 0ull : rmass[tid];
-  uint32_t ctot;
-  const uint32_t cab = kh_above<uint32_t>(cnt, S.s32, &ctot);
-  unsigned long long Ztot;
-  const unsigned long long mab = kh_above<unsigned long long>(mass, S.s64, &Ztot);
+  const unsigned long long mass = anyb ? 0ull : rmass[tid];
+  uint32_t ctot, cab;
+  unsigned long long Ztot, mab;
+  kh_above2(cnt, mass, S, &cab, &ctot, &mab, &Ztot);
   KH_MARK(item, 2);
 
   KhRow res;
@@ -970,10 +1022,10 @@ __device__ __noinline__ uint32_t kh_rank_before(const uint4* src, int id_end, ui
 }
 
 // Clears the kept-token lists of sequence b's target rows (the call leaves the
-// workspace zeroed); reads their lengths from the row results.
-__device__ __noinline__ void kh_clear_lists(const Params& P, int b, const KhRow* rr) {
+// workspace zeroed); their lengths were read from the row results into S.llen.
+__device__ __noinline__ void kh_clear_lists(const Params& P, int b, const KhShared& S) {
   for (int r = 0; r <= P.K; ++r) {
-    const uint32_t L = __ldcg(&rr[r].pad[1]);
+    const uint32_t L = S.llen[r];
     if (L == KH_NOLIST || L == 0u) continue;
     uint32_t* gl = P.ws_lists + ((size_t)b * (P.K + 1) + r) * KH_KCAP;
     for (uint32_t e = threadIdx.x; e < L && e < (uint32_t)KH_KCAP; e += KT) gl[e] = 0u;
@@ -992,6 +1044,7 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
   if (tid < 32) {
     uint32_t f = 0;
     for (int r = tid; r < R2; r += 32) f |= __ldcg(&rr[r].flags);
+    if (tid <= K) S.llen[tid] = __ldcg(&rr[tid].pad[1]);
 #pragma unroll
     for (int o = 16; o; o >>= 1) f |= __shfl_xor_sync(0xffffffffu, f, o);
     uint32_t ok = 1u;
@@ -1055,7 +1108,7 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
       atomicOr(P.ws_work, 1u);
       P.ws_tickets[b] = 0u;
     }
-    kh_clear_lists(P, b, rr);
+    kh_clear_lists(P, b, S);
     __syncthreads();
     uint4* rz = reinterpret_cast<uint4*>(P.ws_rowres + (size_t)b * R2);
     for (int t = tid; t < 2 * R2; t += KT) rz[t] = make_uint4(0u, 0u, 0u, 0u);
@@ -1097,7 +1150,7 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
     P.ws_tickets[b] = 0u;
   }
   // the call leaves the workspace zeroed
-  kh_clear_lists(P, b, rr);
+  kh_clear_lists(P, b, S);
   __syncthreads();
   uint4* rz = reinterpret_cast<uint4*>(P.ws_rowres + (size_t)b * R2);
   for (int t = tid; t < 2 * R2; t += KT) rz[t] = make_uint4(0u, 0u, 0u, 0u);
