@@ -1822,7 +1822,6 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
                                                      unsigned int* rflag, unsigned int* done) {
   const int tid = threadIdx.x;
   constexpr int PV = 16 / (int)sizeof(DT);
-  __shared__ unsigned long long red[NWARP];
   uint4 cur[GV], nxt[GV];
   int item = blockIdx.x, row = 0, nrow = 0;
   bool ok = false, nok = false;
@@ -1901,16 +1900,13 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
         const unsigned long long o2 = __shfl_xor_sync(0xffffffffu, key, o);
         key = o2 > key ? o2 : key;
       }
-      if (lane_id() == 0) red[warp_id()] = key;
-      const int anyb = __syncthreads_or(bad ? 1 : 0);
-      if (tid == 0) {
-        unsigned long long kb = red[0];
-        for (int q = 1; q < NWARP; ++q) kb = red[q] > kb ? red[q] : kb;
-        // one merge per item, without a reply (the row's slot takes the largest key)
-        if (anyb) atomicOr(&rflag[row], 1u);
-        else if (kb) atomicMax(&best[row], kb);
+      // one merge per warp and item, without a reply (the row's slot takes the
+      // largest key); no block barrier, so every warp keeps its loads flowing
+      const bool wbad = __any_sync(0xffffffffu, bad);
+      if (lane_id() == 0) {
+        if (wbad) atomicOr(&rflag[row], 1u);
+        else if (key) atomicMax(&best[row], key);
       }
-      __syncthreads();                           // red[] is reused by the next item
     }
 #pragma unroll
     for (int q = 0; q < GV; ++q) cur[q] = nxt[q];
