@@ -171,6 +171,20 @@ sv_status spec_sample(const void* logits, sv_dtype dtype, int B, int K, int V,
 sv_status spec_philox_uniforms(uint64_t philox_seed, uint64_t philox_offset, int B, int K1,
                                uint32_t* out, void* stream);
 
+/* Acceptance telemetry (page "Speculative decoding: draft models, VRAM economics,
+ * 3x", acceptance rate and draft length; page "MTPLX", the tune command). Adds
+ * the accepted-prefix lengths of one verify call to a caller-owned histogram:
+ *   n_accepted [B] int32 (device): out_n_accepted of a spec_verify call
+ *   hist       [K+2] uint64 (device, 8-byte aligned): hist[n] += #{b : n_b == n}
+ *              for n in 0..K; hist[K+1] += data errors (n = -1) and any value
+ *              outside [0, K]. The caller zeroes it to start a window; calls
+ *              on one stream accumulate.
+ * Limits: B >= 1, 1 <= K <= 16. Asynchronous on `stream`; allocates nothing.
+ * Returns SV_ERR_SHAPE / SV_ERR_NULL / SV_ERR_ALIGN before launching, SV_ERR_CUDA
+ * if the launch fails. */
+sv_status spec_accept_histogram(const int32_t* n_accepted, int B, int K,
+                                unsigned long long* hist, void* stream /* cudaStream_t */);
+
 /* Human-readable name of a status code (static storage). */
 const char* sv_status_string(sv_status status);
 

@@ -54,6 +54,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_sample.restype = i32
     lib.spec_philox_uniforms.argtypes = [u64, u64, i32, i32, vp, vp]
     lib.spec_philox_uniforms.restype = i32
+    lib.spec_accept_histogram.argtypes = [vp, i32, i32, vp, vp]
+    lib.spec_accept_histogram.restype = i32
     lib.sv_status_string.argtypes = [i32]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_version.argtypes = []
@@ -206,3 +208,18 @@ def spec_philox_uniforms(seed: int, offset: int, B: int, K1: int, device="cuda",
                                      out.data_ptr(), _stream(stream))
     _check(st, "spec_philox_uniforms")
     return (out.to(torch.int64) & 0xFFFFFFFF).view(B, K1, 2)
+
+
+def spec_accept_histogram(n_accepted: torch.Tensor, K: int, hist: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """Adds out_n_accepted of one verify call to an acceptance histogram [K+2] (int64 on
+    the device; bins 0..K count accepted-prefix lengths, bin K+1 data errors)."""
+    B = n_accepted.numel()
+    if hist is None:
+        hist = torch.zeros(K + 2, dtype=torch.int64, device=n_accepted.device)
+    if hist.numel() != K + 2 or hist.dtype != torch.int64 or not hist.is_contiguous():
+        raise ValueError("hist must be a contiguous int64 tensor of K+2 counters")
+    st = load().spec_accept_histogram(_dev(n_accepted, "n_accepted", torch.int32), B, K,
+                                      _dev(hist, "hist"), _stream(stream))
+    _check(st, "spec_accept_histogram")
+    return hist
