@@ -109,6 +109,29 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
                       int32_t* out_n_accepted, void* workspace, size_t workspace_bytes,
                       void* stream /* cudaStream_t */);
 
+/* One decode-loop step that keeps its state on the device, so that the step can
+ * be captured once in a CUDA graph and replayed (the GPU-resident token handoff
+ * of page "Optimizing on-device inference for Apple Silicon", decode section,
+ * done the CUDA way). Same arguments and results as spec_verify, except:
+ *   philox_offset [1] uint64 (device, 8-byte aligned): read as the Philox offset
+ *                 of this step, then incremented by 1 once the step is done;
+ *   next_token    [B] int32 (device, written; may be NULL): the last token the
+ *                 step emitted for each sequence (out_tokens[b][n_b]), -1 on a
+ *                 data error: the next step's input token;
+ *   seq_len       [B] int32 (device, read-modify-write; may be NULL): increased
+ *                 by n_b + 1, the tokens emitted (unchanged on a data error).
+ * Nothing is read back to the host and nothing is allocated. The first call in
+ * a process sets kernel attributes: make it before any stream capture. A
+ * replayed graph reads the inputs from the same addresses each time: write the
+ * next step's logits and drafts into them before replaying. Returns what
+ * spec_verify returns, or SV_ERR_NULL / SV_ERR_ALIGN for the new pointers. */
+sv_status spec_verify_step(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                           const int32_t* draft_tokens, const float* temperature,
+                           const int32_t* top_k, const float* top_p, uint64_t philox_seed,
+                           uint64_t* philox_offset, int B, int K, int V, int32_t* out_tokens,
+                           int32_t* out_n_accepted, int32_t* next_token, int32_t* seq_len,
+                           void* workspace, size_t workspace_bytes, void* stream /* cudaStream_t */);
+
 /* spec_verify without a caller workspace. Same arguments, semantics and results as
  * spec_verify, minus the workspace: the workspace is a fixed array of
  * SV_NOALLOC_SCRATCH_BYTES bytes in the library's own device memory (a file-scope

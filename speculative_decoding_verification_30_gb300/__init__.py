@@ -54,6 +54,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_sample.restype = i32
     lib.spec_philox_uniforms.argtypes = [u64, u64, i32, i32, vp, vp]
     lib.spec_philox_uniforms.restype = i32
+    lib.spec_verify_step.argtypes = [vp, vp, i32, vp, vp, vp, vp, u64, vp, i32, i32, i32, vp, vp,
+                                     vp, vp, vp, sz, vp]
+    lib.spec_verify_step.restype = i32
     lib.spec_accept_histogram.argtypes = [vp, i32, i32, vp, vp]
     lib.spec_accept_histogram.restype = i32
     lib.sv_status_string.argtypes = [i32]
@@ -223,3 +226,32 @@ def spec_accept_histogram(n_accepted: torch.Tensor, K: int, hist: torch.Tensor |
                                       _dev(hist, "hist"), _stream(stream))
     _check(st, "spec_accept_histogram")
     return hist
+
+
+def spec_verify_step(target: torch.Tensor, draft: torch.Tensor | None, draft_tokens: torch.Tensor,
+                     temperature: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor,
+                     seed: int, offset: torch.Tensor, out_tokens: torch.Tensor,
+                     out_n: torch.Tensor, workspace: Workspace,
+                     next_token: torch.Tensor | None = None, seq_len: torch.Tensor | None = None,
+                     stream=None):
+    """A graph-capturable verify step: the Philox offset lives in `offset` (a one-element
+    int64 device tensor, advanced by one per step); `next_token` [B] receives each
+    sequence's last emitted token and `seq_len` [B] grows by the tokens emitted."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    if offset.numel() != 1 or offset.dtype != torch.int64:
+        raise SpecVerifyError("offset must be a one-element int64 device tensor")
+    if not workspace.fits(B, K):
+        raise SpecVerifyError("workspace too small for this batch")
+    if draft is not None and (draft.shape != (B, K, V) or draft.dtype != target.dtype):
+        raise SpecVerifyError("draft must be [B, K, V] with the target's dtype")
+    st = load().spec_verify_step(
+        _dev(target, "target"), None if draft is None else _dev(draft, "draft"),
+        _dtype_code(target), _dev(draft_tokens, "draft_tokens", torch.int32),
+        _dev(temperature, "temperature", torch.float32), _dev(top_k, "top_k", torch.int32),
+        _dev(top_p, "top_p", torch.float32), seed & (2**64 - 1), _dev(offset, "offset"), B, K, V,
+        _dev(out_tokens, "out_tokens", torch.int32), _dev(out_n, "out_n", torch.int32),
+        None if next_token is None else _dev(next_token, "next_token", torch.int32),
+        None if seq_len is None else _dev(seq_len, "seq_len", torch.int32),
+        workspace.buf.data_ptr(), workspace.nbytes, _stream(stream))
+    _check(st, "spec_verify_step")

@@ -1062,7 +1062,7 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
       need = tq.idcut == KH_DEFER && zq == tq.zt;
       const float q = kh_kept(zq, d, tq.zt, tq.idcut) ? qw : 0.0f;
       uint32_t ku, kv;
-      philox_uniform_bits(P.seed, P.offset, (uint32_t)b, (uint32_t)i, &ku, &kv);
+      philox_uniform_bits(P.seed, philox_offset_of(P), (uint32_t)b, (uint32_t)i, &ku, &kv);
       ok = __fmul_rn((float)ku * 5.9604644775390625e-08f, q) < p ? 1u : 0u;
       S.pz[i] = p;
       S.qz[i] = qw;
@@ -1120,7 +1120,7 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
     const KhRow tp = kh_load_row(rr + n);
     KhRow tq = paired ? kh_load_row(rr + K + 1 + n) : tp;
     uint32_t ku, kv;
-    philox_uniform_bits(P.seed, P.offset, (uint32_t)b, (uint32_t)n, &ku, &kv);
+    philox_uniform_bits(P.seed, philox_offset_of(P), (uint32_t)b, (uint32_t)n, &ku, &kv);
     const int nv = P.V / 8;
     const uint4* sp = reinterpret_cast<const uint4*>(tgt + (size_t)n * P.V);
     const uint4* sq = paired ? reinterpret_cast<const uint4*>(drf + (size_t)n * P.V) : sp;

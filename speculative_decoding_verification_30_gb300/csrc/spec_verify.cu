@@ -97,7 +97,13 @@ struct Params {
   unsigned int* ws_fnext;       // keyhist_kernel: work counter
   unsigned int* ws_fdone;       // keyhist_kernel: CTAs finished
   uint32_t* ws_lists;           // keyhist_kernel: kept-token ids of target rows [B][K+1][256]
+  const uint64_t* offset_ptr;   // Philox offset in device memory (spec_verify_step), else NULL
 };
+
+// The Philox offset of this call: from device memory when the step keeps it there.
+__device__ __forceinline__ uint64_t philox_offset_of(const Params& P) {
+  return P.offset_ptr ? __ldcg(reinterpret_cast<const unsigned long long*>(P.offset_ptr)) : P.offset;
+}
 
 struct Meta {
   float T, P;
@@ -1616,7 +1622,7 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
           cluster_sync();                                          // end of unit
         } else {
           uint32_t ku, kv;
-          philox_uniform_bits(P.seed, P.offset, (uint32_t)b, (uint32_t)i, &ku, &kv);
+          philox_uniform_bits(P.seed, philox_offset_of(P), (uint32_t)b, (uint32_t)i, &ku, &kv);
           if (tid == 0) {
             uint32_t flag = 0;
             if (paired && m.d / P.slice == (int)rank) {
@@ -1938,6 +1944,21 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
 }
 
 
+// Decode-loop handoff after a verify step: each sequence's last emitted token
+// becomes its next input token, its length grows by the tokens emitted (n + 1;
+// nothing on a data error), and the Philox offset in device memory advances by
+// one for the next step. Runs after every kernel of the step (stream order).
+__global__ void handoff_kernel(const int32_t* out_tokens, const int32_t* out_n, int B, int K,
+                               int32_t* next_token, int32_t* seq_len, uint64_t* offset) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) {
+    const int n = out_n[b];
+    if (next_token) next_token[b] = n >= 0 ? out_tokens[(size_t)b * (K + 1) + n] : -1;
+    if (seq_len && n >= 0) seq_len[b] += n + 1;
+  }
+  if (b == 0) *offset += 1ull;
+}
+
 __global__ void philox_kernel(uint64_t seed, uint64_t offset, int B, int K1, uint32_t* out) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= B * K1) return;
@@ -2079,11 +2100,12 @@ size_t spec_verify_workspace_bytes(int B, int K) {
          rows * KH_KCAP * sizeof(uint32_t);
 }
 
-sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
-                      const int32_t* draft_tokens, const float* temperature, const int32_t* top_k,
-                      const float* top_p, uint64_t philox_seed, uint64_t philox_offset, int B,
-                      int K, int V, int32_t* out_tokens, int32_t* out_n_accepted, void* workspace,
-                      size_t workspace_bytes, void* stream) {
+static sv_status verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                             const int32_t* draft_tokens, const float* temperature,
+                             const int32_t* top_k, const float* top_p, uint64_t philox_seed,
+                             uint64_t philox_offset, const uint64_t* offset_ptr, int B, int K,
+                             int V, int32_t* out_tokens, int32_t* out_n_accepted, void* workspace,
+                             size_t workspace_bytes, void* stream) {
   sv_status s = check_common(V, dtype);
   if (s != SV_OK) return s;
   if (B < 1 || B > 65535 || K < 1 || K > 16) return SV_ERR_SHAPE;
@@ -2108,6 +2130,7 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
   p.topp = top_p;
   p.seed = philox_seed;
   p.offset = philox_offset;
+  p.offset_ptr = offset_ptr;
   p.B = B;
   p.K = K;
   p.nunits = B * (K + 1);
@@ -2189,6 +2212,35 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
     }
   }
   return do_launch(MODE_VERIFY, dtype, p, g, st);
+}
+
+sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      const int32_t* draft_tokens, const float* temperature, const int32_t* top_k,
+                      const float* top_p, uint64_t philox_seed, uint64_t philox_offset, int B,
+                      int K, int V, int32_t* out_tokens, int32_t* out_n_accepted, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  return verify_impl(target_logits, draft_logits, dtype, draft_tokens, temperature, top_k, top_p,
+                     philox_seed, philox_offset, nullptr, B, K, V, out_tokens, out_n_accepted,
+                     workspace, workspace_bytes, stream);
+}
+
+sv_status spec_verify_step(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                           const int32_t* draft_tokens, const float* temperature,
+                           const int32_t* top_k, const float* top_p, uint64_t philox_seed,
+                           uint64_t* philox_offset, int B, int K, int V, int32_t* out_tokens,
+                           int32_t* out_n_accepted, int32_t* next_token, int32_t* seq_len,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (!philox_offset) return SV_ERR_NULL;
+  if (!aligned(philox_offset, 8) || (next_token && !aligned(next_token, 4)) ||
+      (seq_len && !aligned(seq_len, 4)))
+    return SV_ERR_ALIGN;
+  const sv_status s = verify_impl(target_logits, draft_logits, dtype, draft_tokens, temperature,
+                                  top_k, top_p, philox_seed, 0, philox_offset, B, K, V, out_tokens,
+                                  out_n_accepted, workspace, workspace_bytes, stream);
+  if (s != SV_OK) return s;
+  handoff_kernel<<<(B + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      out_tokens, out_n_accepted, B, K, next_token, seq_len, philox_offset);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 sv_status spec_truncated_probs(const void* logits, sv_dtype dtype, int R, int V,
