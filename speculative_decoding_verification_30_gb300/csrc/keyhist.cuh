@@ -1163,6 +1163,8 @@ __device__ __noinline__ void kh_finalize(const Params& P, int b, KhShared& S) {
 __global__ void __launch_bounds__(KT, 2) keyhist_kernel(const Params P, int nitems) {
   uint32_t* kh_hist = kh_dyn;
   __shared__ KhShared S;
+  // the cluster kernel may launch now; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x;
   const int K = P.K, R2 = 2 * K + 1;
   for (int wd = tid; wd < KH_NW; wd += KT) kh_hist[wd] = 0u;
@@ -1205,6 +1207,9 @@ __global__ void __launch_bounds__(KT, 2) keyhist_kernel(const Params P, int nite
     }
     __syncthreads();
   }
+  // finish only after greedy_kernel (launched before, possibly still running):
+  // whatever waits for this grid then sees both
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the last CTA to leave re-arms the work counter for the next call
   if (tid == 0) {
     __threadfence();

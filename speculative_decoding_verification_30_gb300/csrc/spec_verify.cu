@@ -1223,6 +1223,9 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
   const int base = (int)rank * P.slice;
   const int vlen = max(0, min(P.slice, P.V - base));
   const int nvec = (int)(slot_bytes / 16);
+  // launched early (programmatic dependent launch) behind greedy_kernel and
+  // keyhist_kernel: wait until they are done before reading what they wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int nmine = cid < P.nunits ? (P.nunits - 1 - cid) / ncl + 1 : 0;
   // verify batches whose units are all served by greedy_kernel or keyhist_kernel:
   // nothing to do here (every CTA reads the same flag, so none waits on another)
@@ -1829,6 +1832,8 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
   const int tid = threadIdx.x;
   constexpr int PV = 16 / (int)sizeof(DT);
   uint4 cur[GV], nxt[GV];
+  // the step's later kernels may launch now; they wait for this grid where needed
+  asm volatile("griddepcontrol.launch_dependents;");
   int item = blockIdx.x, row = 0, nrow = 0;
   bool ok = false, nok = false;
   if (item < nitems) greedy_load<DT>(P, item, G, chunk, cur, &row, &ok);
@@ -2025,13 +2030,17 @@ static cudaError_t launch(const Params& p, const Geometry& g, cudaStream_t st) {
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = g.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)g.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // verify calls: may start while the step's earlier kernels finish (it waits for
+  // them with griddepcontrol.wait before reading their results)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (MODE == MODE_VERIFY && p.greedy_split) ? 2 : 1;
   if (cached_C != g.C || cached_smem != g.smem || cached_dev != dev) {
     cfg.gridDim = dim3((unsigned)g.C, 1, 1);
     int n = 0;
@@ -2207,8 +2216,19 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
       }
       const int kitems = B * (2 * K + 1);
       const int kgrid = kitems < kblocks ? kitems : kblocks;
-      keyhist_kernel<<<kgrid, KT, KH_SMEM, st>>>(p, kitems);
-      if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+      // starts while greedy_kernel runs (it reads nothing greedy_kernel writes, and
+      // waits for it before finishing, so the cluster kernel sees both)
+      cudaLaunchConfig_t kc = {};
+      kc.gridDim = dim3((unsigned)kgrid, 1, 1);
+      kc.blockDim = dim3(KT, 1, 1);
+      kc.dynamicSmemBytes = KH_SMEM;
+      kc.stream = st;
+      cudaLaunchAttribute ka[1];
+      ka[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      ka[0].val.programmaticStreamSerializationAllowed = 1;
+      kc.attrs = ka;
+      kc.numAttrs = 1;
+      if (cudaLaunchKernelEx(&kc, keyhist_kernel, p, kitems) != cudaSuccess) return SV_ERR_CUDA;
     }
   }
   return do_launch(MODE_VERIFY, dtype, p, g, st);
