@@ -549,6 +549,18 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   // sweep, words interleaved over the threads (occupied bins cluster in a few
   // value ranges): counts and fixed-point masses, added to the word's thread range
   uint32_t bad = 0;
+  // a lane's words are summed locally and added to their thread range once
+  int rcur = -1;
+  uint32_t cacc = 0;
+  unsigned long long macc = 0;
+  auto flush = [&]() {
+    if (rcur >= 0 && cacc) {
+      atomicAdd(&rcnt[rcur], cacc);
+      if (macc) atomicAdd(&rmass[rcur], macc);
+    }
+    cacc = 0;
+    macc = 0;
+  };
   auto sweep_word = [&](int wd, uint32_t x) {
     const uint32_t chi = x >> 16, clo = x & 0xFFFFu;
     const int i0 = 2 * wd;
@@ -557,8 +569,12 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
     const unsigned long long mw = (clo ? clo * kh_binw(i0, m, c) : 0ull) +
                                   (chi ? chi * kh_binw(i0 + 1, m, c) : 0ull);
     const int r = wd / KH_WPT;
-    atomicAdd(&rcnt[r], chi + clo);
-    if (mw) atomicAdd(&rmass[r], mw);
+    if (r != rcur) {
+      flush();
+      rcur = r;
+    }
+    cacc += chi + clo;
+    macc += mw;
   };
   // four words per 16-byte load; the last word (an odd count) separately
   const uint4* h4 = reinterpret_cast<const uint4*>(hist);
@@ -569,9 +585,11 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
     if (x.y) sweep_word(4 * v4 + 1, x.y);
     if (x.z) sweep_word(4 * v4 + 2, x.z);
     if (x.w) sweep_word(4 * v4 + 3, x.w);
+    flush();
   }
   for (int wd = (KH_NW / 4) * 4 + tid; wd < KH_NW; wd += KT)
     if (hist[wd]) sweep_word(wd, hist[wd]);
+  flush();
   const int anyb = __syncthreads_or((int)bad);
   const uint32_t cnt = rcnt[tid];
   const unsigned long long mass = anyb ? 0ull : rmass[tid];
