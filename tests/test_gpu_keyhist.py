@@ -199,3 +199,22 @@ def test_keyhist_workspace_stays_zeroed_and_calls_repeat():
     for o, n in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(n, outs[0][1])
     assert int(ws.buf.count_nonzero()) == 0
+
+
+def test_huge_logits():
+    # magnitudes far outside real logits (|z| >= 2^24): point masses and zero
+    # weights at the ends of the bin range; every sequence must match the oracle
+    g = torch.Generator().manual_seed(23)
+    B, K, V = 16, 4, 4096
+    tgt, drf = _batch(B, K, V, g)
+    tgt[0, 1, 7] = 3.0e7                     # one huge positive logit (a point mass)
+    drf[1, 0, 9] = -5.0e7                    # one huge negative logit (weight 0)
+    tgt[2, :, 100] = 2.0e9
+    drf[2, :, 100] = 2.0e9
+    dtok = _drafts(drf, g)
+    dtok[2, :] = 100
+    T = torch.full((B,), 1.0)
+    k = torch.tensor([0, 20] * 8, dtype=torch.int32)
+    P = torch.tensor([0.95, 1.0] * 8)
+    for step in range(3):
+        _check(tgt, drf, dtok, T, k, P, 12, step, f"huge logits step {step}")
