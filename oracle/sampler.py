@@ -22,7 +22,7 @@ What it computes, and where the pages say so (page titles as cited):
   one pass, accept in order with min(1, p/q), on rejection sample from
   (p(x) - q(x))+ and drop the remaining drafts).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 * truncation order: top-k first, renormalise, then top-p on that mass;
 * nucleus = shortest prefix of (logit desc, id asc) whose mass reaches top_p,
   i.e. keep x iff the mass strictly before x is < top_p (at least one token);
