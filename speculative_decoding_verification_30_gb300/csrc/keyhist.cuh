@@ -51,18 +51,18 @@ constexpr float KH_LIST_BITS = 12.0f;                     // listed: weight >= 2
 __device__ unsigned long long g_khtrace[4096 * 8];
 #define KH_MARK(item, k)                                                   \
   do {                                                                     \
-    if (threadIdx.x == 0 && (item) < 4096) g_khtrace[(item) * 8 + (k)] = global_timer_ns(); \
+    if (threadIdx.x == 0 && (item) >= 0 && (item) < 4096) g_khtrace[(item) * 8 + (k)] = global_timer_ns(); \
   } while (0)
 // Per-sequence finalize timestamps: 0 start, 1 acceptance done, 2 first sampling
 // pass done, 3 end; 4 = redo, 5 = n.
 __device__ unsigned long long g_kftrace[1024 * 8];
 #define KF_MARK(b, k)                                                      \
   do {                                                                     \
-    if (threadIdx.x == 0 && (b) < 1024) g_kftrace[(b) * 8 + (k)] = global_timer_ns(); \
+    if (threadIdx.x == 0 && (b) >= 0 && (b) < 1024) g_kftrace[(b) * 8 + (k)] = global_timer_ns(); \
   } while (0)
 #define KF_SET(b, k, v)                                                    \
   do {                                                                     \
-    if (threadIdx.x == 0 && (b) < 1024) g_kftrace[(b) * 8 + (k)] = (v);   \
+    if (threadIdx.x == 0 && (b) >= 0 && (b) < 1024) g_kftrace[(b) * 8 + (k)] = (v);   \
   } while (0)
 #else
 #define KF_MARK(b, k) \
@@ -781,6 +781,91 @@ __device__ __forceinline__ bool kh_vec_cand(const uint4& a, __nv_bfloat162 zt2) 
   return (__hge2_mask(x0, zt2) | __hge2_mask(x1, zt2) | __hge2_mask(x2, zt2) | __hge2_mask(x3, zt2)) != 0u;
 }
 
+// Warp sum of per-lane fixed-point masses below 2^51 (a vector's 8 weights of at
+// most 16 * 2^40 each), as two 32-bit lane reductions of the low 24 bits and the
+// rest: neither partial sum can overflow 32 bits.
+__device__ __forceinline__ unsigned long long kh_wsum(unsigned long long x) {
+  const uint32_t lo = __reduce_add_sync(0xffffffffu, (uint32_t)x & 0xFFFFFFu);
+  const uint32_t hi = __reduce_add_sync(0xffffffffu, (uint32_t)(x >> 24));
+  return ((unsigned long long)hi << 24) + lo;
+}
+// Weight tables of the sampling pass. A table holds one entry per bin from the
+// cut bin to the bin of the row maximum, except the bins of 2^-40 <= |z| < 2^-8
+// and the merged bin (a band around zero), whose rare tokens are evaluated
+// directly: without the band a table across zero would need ~10k entries.
+constexpr int KH_BAND = 32 * 128;
+// Table slot of a bin outside the band, -1 inside it; increasing in the bin.
+__device__ __forceinline__ int kh_slot(int bin) {
+  return bin > KH_OFF + KH_BAND ? bin - (2 * KH_BAND + 1) : (bin < KH_OFF - KH_BAND ? bin : -1);
+}
+__device__ __forceinline__ int kh_slot_bin(int s) {
+  return s >= KH_OFF - KH_BAND ? s + (2 * KH_BAND + 1) : s;
+}
+// Slots [*lo, *lo + *n) of the bins a cut at zt can keep on a row with maximum m.
+__device__ __forceinline__ void kh_slots(float zt, float m, int* lo, int* n) {
+  const int bz = zt > -INFINITY ? (int)kh_bin(__float_as_uint(zt) >> 16) : KH_NINF + 1;
+  const int bm = (int)kh_bin(__float_as_uint(m) >> 16);
+  const int l = bz < KH_OFF - KH_BAND ? bz : (bz > KH_OFF + KH_BAND ? bz - (2 * KH_BAND + 1) : KH_OFF - KH_BAND);
+  const int h = bm < KH_OFF - KH_BAND ? bm : (bm > KH_OFF + KH_BAND ? bm - (2 * KH_BAND + 1) : KH_OFF - KH_BAND - 1);
+  *lo = l;
+  *n = h - l + 1;
+}
+// p of one token from a float table (or directly, in the band).
+__device__ __forceinline__ float kh_ptab(uint32_t h, float z, const KhW& w, const float* tab, int lo,
+                                         int n) {
+  const int sl = kh_slot((int)kh_bin(h)) - lo;
+  if ((unsigned)sl < (unsigned)n) return tab[sl];
+  return __fmul_rn(kh_w(z, w.m, w.c), w.invZ);
+}
+// kh_vec_heavy with table lookups. Unpaired: tab64 holds fixr(p) per slot (w0 is
+// the weight of z = 0). Paired: tab holds p per slot, then q per slot at tab + np.
+// The weights are the ones kh_elem computes, so the sums match bit for bit.
+__device__ __forceinline__ void kh_vec_tab(uint4 a, const uint4* sq, int v, bool paired,
+                                           const KhW& tp, const KhW& tq, const float* tab,
+                                           const unsigned long long* tab64, unsigned long long w0,
+                                           int lop, int np, int loq, int nq, int cp, int cn,
+                                           int idcut0, unsigned long long* R,
+                                           unsigned long long* Pm, bool* dhit) {
+  uint4 bq = make_uint4(0u, 0u, 0u, 0u);
+  if (paired) bq = kh_ld_l2(sq + v);
+  const uint32_t as[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bs[4] = {bq.x, bq.y, bq.z, bq.w};
+  unsigned long long ra = 0, pa = 0;
+  bool hit = false;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t hp = (e & 1) ? as[e >> 1] >> 16 : as[e >> 1] & 0xFFFFu;
+    const float zp = __uint_as_float(hp << 16);
+    const int id = v * 8 + e;
+    if (!paired) {
+      // table index straight from the bits (slot - lo: a + cp above zero, cn - a
+      // below); below the cut it is negative, and the cut bin itself is index 0
+      // when the cut lies outside the band (idcut0 = its id cut, else INT_MAX)
+      const int a16 = (int)(hp & 0x7FFFu);
+      if (a16 < (int)KH_TSPLIT + KH_BAND) {
+        if (kh_kept(zp, id, tp.zt, tp.idcut))
+          pa += a16 == 0 ? w0 : fixr(__fmul_rn(kh_w(zp, tp.m, tp.c), tp.invZ));
+        continue;
+      }
+      const int ix = (hp & 0x8000u) ? cn - a16 : a16 + cp;
+      const bool in = (unsigned)ix < (unsigned)np && (ix != 0 || id <= idcut0);
+      pa += in ? tab64[ix] : 0ull;
+      continue;
+    }
+    if (!kh_kept(zp, id, tp.zt, tp.idcut)) continue;
+    const float pp = kh_ptab(hp, zp, tp, tab, lop, np);
+    const uint32_t hq = (e & 1) ? bs[e >> 1] >> 16 : bs[e >> 1] & 0xFFFFu;
+    const float zq = __uint_as_float(hq << 16);
+    const float q = kh_kept(zq, id, tq.zt, tq.idcut) ? kh_ptab(hq, zq, tq, tab + np, loq, nq) : 0.0f;
+    hit |= tq.idcut == KH_DEFER && zq == tq.zt;
+    ra += fixr(fmaxf(__fsub_rn(pp, q), 0.0f));
+    pa += fixr(pp);
+  }
+  *R = paired ? ra : pa;
+  *Pm = pa;
+  if (hit) *dhit = true;
+}
+
 // Inverse CDF in token-id order over (p - q)+ (paired) or p: the smallest id j
 // whose running sum S_j satisfies S_j * 2^24 > kv * S (S the total); when the
 // residual mass is 0 the target p is used. Every warp sums its contiguous id
@@ -797,7 +882,38 @@ __device__ __noinline__ int kh_sample(const uint4* sp, const uint4* sq, int nv, 
   unsigned long long tR = 0, tP = 0;
   bool dhit = false;
   const __nv_bfloat162 zt2 = __float2bfloat162_rn(tp.zt);   // zt is a bf16 value
-  constexpr int U = 8;                          // target vectors in flight per lane
+  // When the bins a cut keeps fit the histogram's shared memory (zero here), the
+  // weights are tabulated per bin once and the pass reads them instead of
+  // evaluating exp2 per token; the table is zeroed again afterwards.
+  float* tab = reinterpret_cast<float*>(kh_dyn);
+  unsigned long long* tab64 = reinterpret_cast<unsigned long long*>(kh_dyn);
+  int lop, np, loq = 0, nq = 0;
+  kh_slots(tp.zt, tp.m, &lop, &np);
+  if (paired) kh_slots(tq.zt, tq.m, &loq, &nq);
+  np = max(np, 0);
+  nq = max(nq, 0);
+  const int twords = paired ? np + nq : 2 * np;  // 32-bit words the table takes
+  const bool use_tab = twords <= KH_NW;
+  const unsigned long long w0 = fixr(__fmul_rn(kh_w(0.0f, tp.m, tp.c), tp.invZ));
+  // unpaired index constants: a bf16 magnitude a outside the band has slot
+  // a + (KH_OFF - KH_TSPLIT - 2 KH_BAND) when positive, KH_OFF + KH_TSPLIT - 1 - a when negative
+  const int cp = KH_OFF - (int)KH_TSPLIT - 2 * KH_BAND - lop;
+  const int cn = KH_OFF + (int)KH_TSPLIT - 1 - lop;
+  const int idcut0 =
+      (int)(__float_as_uint(tp.zt) >> 16 & 0x7FFFu) >= (int)KH_TSPLIT + KH_BAND && tp.zt > -INFINITY
+          ? tp.idcut : INT_MAX;
+  if (use_tab) {
+    for (int j = threadIdx.x; j < np + nq; j += KT) {
+      const bool isq = j >= np;
+      const KhW& w = isq ? tq : tp;
+      const float z = kh_value(kh_slot_bin(isq ? loq + (j - np) : lop + j));
+      const float pz = __fmul_rn(kh_w(z, w.m, w.c), w.invZ);
+      if (paired) tab[j] = pz;
+      else tab64[j] = fixr(pz);
+    }
+    __syncthreads();
+  }
+  constexpr int U = 4;                          // target vectors in flight per lane
   for (int j = 0; j < nb; j += U) {
     uint4 av[U];
 #pragma unroll
@@ -813,9 +929,14 @@ __device__ __noinline__ int kh_sample(const uint4* sp, const uint4* sq, int nv, 
         unsigned long long r = 0, p = 0;
         // blocks without a kept target token contribute nothing
         if (__any_sync(0xffffffffu, cand)) {
-          if (cand) kh_vec_heavy(av[u], sq, v, paired, tp, tq, &r, &p, &dhit);
-          r = warp_sum(r);
-          p = warp_sum(p);
+          if (cand) {
+            if (use_tab)
+              kh_vec_tab(av[u], sq, v, paired, tp, tq, tab, tab64, w0, lop, np, loq, nq, cp, cn, idcut0,
+                         &r, &p, &dhit);
+            else kh_vec_heavy(av[u], sq, v, paired, tp, tq, &r, &p, &dhit);
+          }
+          p = kh_wsum(p);
+          r = paired ? kh_wsum(r) : p;
         }
         if (l == 0) {
           bR[w * KH_MAXBLK + j + u] = r;
@@ -830,7 +951,12 @@ __device__ __noinline__ int kh_sample(const uint4* sp, const uint4* sq, int nv, 
     S.s64[w] = tR;
     S.s64b[w] = tP;
   }
-  if (__syncthreads_or(dhit ? 1 : 0)) return -2;   // the caller splits the draft cut first
+  const bool redo = __syncthreads_or(dhit ? 1 : 0) != 0;
+  if (use_tab) {
+    for (int j = threadIdx.x; j < twords; j += KT) tab[j] = 0.0f;
+    __syncthreads();
+  }
+  if (redo) return -2;                          // the caller splits the draft cut first
   KF_MARK(bt, 6);
   if (w == 0) {
     const unsigned long long oR = l < KWARP ? S.s64[l] : 0ull, oP = l < KWARP ? S.s64b[l] : 0ull;
@@ -949,7 +1075,7 @@ __device__ __noinline__ int kh_sample_list(const unsigned short* zp_row, const u
   unsigned long long* wp = wr + KH_LCAP;                           // [KH_LCAP] p, sorted
   uint32_t* sid = reinterpret_cast<uint32_t*>(wp + KH_LCAP);       // [KH_LCAP] ids, sorted
   bool dhit = false;
-  for (int e = tid; e < L; e += KT) ids[e] = __ldcg(glist + e);
+  for (int e = tid; e < L; e += KT) ids[e] = __isShared(glist) ? glist[e] : __ldcg(glist + e);
   __syncthreads();
   for (int e = tid; e < L; e += KT) {
     const int id = (int)ids[e];
@@ -1235,6 +1361,61 @@ __global__ void __launch_bounds__(KT, 2) keyhist_kernel(const Params P, int nite
       *P.ws_fnext = 0u;
       *P.ws_fdone = 0u;
     }
+  }
+}
+
+// ---------------------------------------------------------- draft sampler
+// A row the draft sampler leaves to the cluster kernel (temperature 0, a parameter
+// error, or a hand-back) carries this value in out_tokens until that kernel runs.
+constexpr int KH_HANDBACK = -2;
+
+// Draft-side sampler for bf16 rows (spec_sample): d ~ q for every row [B][K][V].
+// CTAs take rows by a static stride (there is no workspace for a work counter).
+// Each row is cut like a target row (window candidates, id split) and sampled in
+// the same CTA with the sampling uniform of Philox (b, i): over the kept ids when
+// they fit the shared list, else by a full-row inverse CDF.
+__global__ void __launch_bounds__(KT, 2) keyhist_sample_kernel(const Params P, int nitems) {
+  uint32_t* hist = kh_dyn;
+  __shared__ KhShared S;
+  const int tid = threadIdx.x;
+  for (int wd = tid; wd < KH_NW; wd += KT) hist[wd] = 0u;
+  __syncthreads();
+  uint32_t* klist = reinterpret_cast<uint32_t*>(kh_blk0());   // kept ids (after the cut)
+  const int nv = P.V / 8;
+  for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+    const int b = item / P.K, i = item - b * P.K;
+    const float T = P.temp[b];
+    const bool served = T > 0.0f && T < INFINITY && P.topp[b] > 0.0f && P.topk[b] >= 0 &&
+                        __fdiv_rn(KH_LOG2E, T) < 65536.0f;
+    if (!served) {
+      if (tid == 0) P.out_tokens[item] = KH_HANDBACK;
+      continue;
+    }
+    KH_MARK(item, 0);
+    const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(P.rows0) + (size_t)item * P.V;
+    const KhRow res = kh_row(row, P.V, T, P.topk[b], P.topp[b], true, hist, S, klist, item);
+    KH_MARK(item, 4);
+    int tok;
+    if (res.flags & KH_ERR) {
+      tok = -1;
+    } else if (res.flags & KH_BAIL) {
+      tok = KH_HANDBACK;
+    } else {
+      uint32_t ku, kv;
+      philox_uniform_bits(P.seed, philox_offset_of(P), (uint32_t)b, (uint32_t)i, &ku, &kv);
+      const KhW w = kh_wof(res);
+      if (res.pad[1] != KH_NOLIST) {
+        const unsigned short* zr = reinterpret_cast<const unsigned short*>(row);
+        tok = kh_sample_list(zr, zr, klist, (int)res.pad[1], false, w, w, kv, S);   // scratch: the histogram
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(row);
+        tok = kh_sample(src, src, nv, false, w, w, kv, S, -1);
+      }
+      if (tok < 0) tok = -1;
+    }
+    KH_MARK(item, 5);
+    if (tid == 0) P.out_tokens[item] = tok;
+    __syncthreads();
   }
 }
 

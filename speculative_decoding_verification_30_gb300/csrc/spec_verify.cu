@@ -1144,6 +1144,7 @@ template <int MODE>
 __device__ __forceinline__ int unit_rows(const Params& P, const Meta& m, int i) {
   if (param_error<MODE>(P, m, i)) return 0;
   if (MODE == MODE_VERIFY && P.greedy_split && m.g) return 0;   // greedy path
+  if (MODE == MODE_SAMPLE && P.fast_split && m.g) return 0;      // served by keyhist_sample_kernel
   if (MODE == MODE_VERIFY && i < P.K && m.T > 0.0f) return 2;
   return 1;
 }
@@ -1187,6 +1188,8 @@ __device__ __noinline__ void load_meta(Shared& S, const Params& P, int cid, int 
     m.g = (MODE == MODE_VERIFY && P.greedy_split)
               ? (int)(greedy_seq(P, b) || (P.fast_split && fast_seq(P, b) && P.ws_fb[b] == 0u))
               : 0;
+    // draft sampler: rows keyhist_sample_kernel served (not marked for this kernel)
+    if (MODE == MODE_SAMPLE && P.fast_split) m.g = P.out_tokens[(size_t)b * P.K + i] != KH_HANDBACK;
     S.meta[j % MR] = m;
   }
 }
@@ -1231,6 +1234,13 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
   // nothing to do here (every CTA reads the same flag, so none waits on another)
   if (MODE == MODE_VERIFY && P.greedy_split && *reinterpret_cast<volatile unsigned int*>(P.ws_work) == 0u)
     return;
+  // draft sampler: nothing left when no row carries the hand-back mark (every CTA
+  // scans the same outputs, so all of a cluster decide alike)
+  if (MODE == MODE_SAMPLE && P.fast_split && P.nunits <= 65536) {
+    int marked = 0;
+    for (int t = threadIdx.x; t < P.nunits; t += NT) marked |= P.out_tokens[t] == KH_HANDBACK;
+    if (!__syncthreads_or(marked)) return;
+  }
   const uint32_t copy_bytes = (uint32_t)((size_t)vlen * sizeof(DT));
   const uint64_t pol = policy_evict_first();
 
@@ -1322,8 +1332,9 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
       } else {
         for (int l = tid; l < vlen; l += NT) P.out_probs[(size_t)b * P.V + base + l] = __int_as_float(0x7fc00000);
       }
-    } else if (MODE == MODE_VERIFY && P.greedy_split && m.g) {
-      // units of greedy sequences are served by greedy_kernel
+    } else if ((MODE == MODE_VERIFY && P.greedy_split && m.g) ||
+               (MODE == MODE_SAMPLE && P.fast_split && m.g)) {
+      // units served by greedy_kernel, keyhist_kernel or keyhist_sample_kernel
     } else if (m.T == 0.0f) {
       // ------------------------------------------------ greedy (T = 0)
       X1Row& x = S.x1[xr & 1][0];
@@ -2311,7 +2322,27 @@ sv_status spec_sample(const void* logits, sv_dtype dtype, int B, int K, int V,
   p.nunits = B * K;
   p.bulk_ok = ((V * es) % 16 == 0) && aligned(logits, 16);
   p.out_tokens = out_tokens;
-  return do_launch(MODE_SAMPLE, dtype, p, g, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // bf16 rows, 16-byte aligned, at least 16 rows: the key-histogram sampler serves
+  // every row it can; the cluster kernel takes the rows it marks
+  p.fast_split = (dtype == SV_BF16 && p.bulk_ok && (long long)B * K >= 16) ? 1 : 0;
+  if (p.fast_split) {
+    static int sblocks = 0;
+    if (!sblocks) {
+      int dev = 0, sms = 0, per = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (cudaFuncSetAttribute(keyhist_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)KH_SMEM) != cudaSuccess)
+        return SV_ERR_CUDA;
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, keyhist_sample_kernel, KT, KH_SMEM);
+      sblocks = max(1, sms * max(1, per));
+    }
+    const int items = B * K;
+    keyhist_sample_kernel<<<items < sblocks ? items : sblocks, KT, KH_SMEM, st>>>(p, items);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  }
+  return do_launch(MODE_SAMPLE, dtype, p, g, st);
 }
 
 sv_status spec_philox_uniforms(uint64_t philox_seed, uint64_t philox_offset, int B, int K1,

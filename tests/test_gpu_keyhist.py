@@ -5,6 +5,7 @@ Tokens and n_accepted must equal the oracle's except on sequences with a
 boundary draw (an acceptance or sampling uniform within 1e-6 of its decision
 boundary); data errors must be reported as n = -1 with all tokens -1.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -218,3 +219,60 @@ def test_huge_logits():
     P = torch.tensor([0.95, 1.0] * 8)
     for step in range(3):
         _check(tgt, drf, dtok, T, k, P, 12, step, f"huge logits step {step}")
+
+
+def _sample_check(drf, T, k, P, seed, offset, label):
+    """spec_sample against the oracle's sample_row at Philox (b, i). A mismatch is
+    allowed only for a sampling uniform within 1e-6 of a CDF boundary, or, where the
+    nucleus cut lies within 1e-6 of top_p, for the token on either side of the cut
+    (the only token that a cut decided the other way adds or drops)."""
+    from oracle import sampler
+    from oracle.philox import uniforms
+    got = sv.spec_sample(drf.to(DEV), T.to(DEV), k.to(DEV), P.to(DEV), seed=seed,
+                         offset=offset).cpu().numpy()
+    z = drf.float().double().numpy()
+    B, K, V = drf.shape
+    bad, near_draw, near_cut = [], 0, 0
+    for b in range(B):
+        Tb, kb, Pb = float(T[b]), int(k[b]), float(P[b])
+        for i in range(K):
+            row = z[b, i]
+            if np.isnan(row).any() or np.isposinf(row).any() or np.isneginf(row).all() or Pb <= 0:
+                if got[b, i] != -1:
+                    bad.append((b, i, int(got[b, i]), "error expected"))
+                continue
+            _, v = uniforms(seed, offset, b, i)
+            tok, margin = sampler.sample_row(row, Tb, kb, Pb, v)
+            edge = set()
+            if Tb > 0:
+                t = sampler.truncate(row, Tb, kb, Pb)
+                if t.topp_margin < 1e-6:
+                    near_cut += 1
+                    order = sampler.descending_order(row)
+                    n = len(t.kept)
+                    edge = {int(order[n - 1])} | ({int(order[n])} if n < V else set())
+            near_draw += int(margin < 1e-6)
+            if got[b, i] != tok and margin >= 1e-6 and int(got[b, i]) not in edge:
+                bad.append((b, i, int(got[b, i]), tok))
+    print(label, "rows", B * K, "draws near a CDF boundary", near_draw,
+          "cuts near top_p", near_cut, "bad", len(bad))
+    assert not bad, bad[:4]
+
+
+def test_draft_sampler_full_size_and_edge_rows():
+    from speculative_decoding_verification_30_gb300.workloads import WORKLOADS, make_batch
+    w = WORKLOADS["nucleus_batch"]
+    b = make_batch(w, 3)
+    _sample_check(b.draft, b.temperature, b.top_k, b.top_p, 4242, 10, "nucleus drafts B=64")
+    g = torch.Generator().manual_seed(31)
+    B, K, V = 16, 4, 8192
+    _, drf = _batch(B, K, V, g, quant=0.5)
+    drf[3, 1, :] = -float("inf")
+    drf[3, 1, 5] = 2.0                                  # a single finite token
+    drf[5, 2, 9] = float("nan")                         # data error
+    T = torch.tensor([1.0, 0.6, 0.0, 1.3] * 4)          # T = 0 rows go to the cluster kernel
+    k = torch.tensor([0, 20, 0, 3] * 4, dtype=torch.int32)
+    P = torch.tensor([0.9, 1.0, 1.0, 0.7] * 4)
+    P[7] = 0.0                                          # parameter error (top_p <= 0)
+    for step in range(3):
+        _sample_check(drf, T, k, P, 9, step, f"edge drafts step {step}")
