@@ -276,3 +276,16 @@ def test_draft_sampler_full_size_and_edge_rows():
     P[7] = 0.0                                          # parameter error (top_p <= 0)
     for step in range(3):
         _sample_check(drf, T, k, P, 9, step, f"edge drafts step {step}")
+
+
+def test_draft_sampler_many_rows_per_cta():
+    # 640 rows on at most 304 CTAs: each CTA samples two or three rows in turn, so
+    # the histogram and the shared scratch must be left clean between rows
+    g = torch.Generator().manual_seed(77)
+    B, K, V = 160, 4, 8192
+    _, drf = _batch(B, K, V, g, quant=None)
+    drf[::7] = torch.round(drf[::7].float() / 0.25).to(torch.bfloat16) * 0.25   # tie-heavy rows
+    T = torch.tensor([0.6, 1.0, 0.8, 1.5] * (B // 4))
+    k = torch.tensor([0, 40, 0, 7] * (B // 4), dtype=torch.int32)
+    P = torch.tensor([0.95, 1.0, 0.5, 0.9] * (B // 4))
+    _sample_check(drf, T, k, P, 2024, 3, "many rows per CTA")
