@@ -52,11 +52,19 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+# Sources of the translation unit that holds the profiled kernels (keyhist_kernel,
+# greedy_kernel, the cluster kernel): a profile's counters stay valid while these
+# bytes are unchanged; other translation units do not affect those kernels.
+PROFILED_SOURCES = ("speculative_decoding_verification_30_gb300/csrc/spec_verify.cu",
+                    "speculative_decoding_verification_30_gb300/csrc/keyhist.cuh",
+                    "speculative_decoding_verification_30_gb300/csrc/sv_device.cuh",
+                    "include/spec_verify.h")
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "speculative_decoding_verification_30_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+    for rel in PROFILED_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
