@@ -1,0 +1,71 @@
+/* spec_lm_head.h — LM-head logits on the tensor cores, and the verify step fed
+ * from hidden states (the fused LM-head + verify row of this library).
+ *
+ * What the pages define. "Apple Silikon İçin Cihaz Üstü Çıkarımı Optimize Etme"
+ * (perplexity.coolkeypoint.com), decode section: every decode step ends by
+ * choosing the next token from the position's logit row, the output projection
+ * z = h . W^T of its final hidden state h against the LM-head weight W. Its
+ * section on the limits of further optimisation reports that fusing the output
+ * projection with token selection was tried there. The verify step that consumes
+ * the rows is spec_verify (include/spec_verify.h).
+ *
+ * Status: these entry points compile for sm_103a. Their GEMM kernel (tcgen05.mma
+ * with TMA-staged operands and a TMEM accumulator) has not yet run on a GPU, and
+ * no test calls it; only the argument checks below are exercised.
+ */
+#ifndef SPEC_LM_HEAD_H
+#define SPEC_LM_HEAD_H
+
+#include "spec_verify.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* logits[M][N] = hidden[M][d] . weight[N][d]^T, accumulated in fp32.
+ *   hidden  [M][d] bf16, row-major, device memory, 16-byte aligned
+ *   weight  [N][d] bf16, row-major (row v = token v's LM-head vector), device,
+ *           16-byte aligned
+ *   logits  [M][N] fp32, row-major, device, caller-owned, 4-byte aligned
+ *   flag    [1] int32, device, caller-owned: set to 1 when a pipeline wait of the
+ *           kernel timed out (the logits are then undefined); never cleared here
+ * Limits: 1 <= M <= 8,388,480 (65,535 row tiles of 128), 1 <= N <= 2^31 - 1,
+ * d a positive multiple of 64 and at most 65,536.
+ * Every bf16 product is exact in fp32, so each logit lies within
+ * gamma_(d-1) * sum_j |hidden_j * weight_vj| of the exact dot product
+ * (gamma_n = n u / (1 - n u), u = 2^-23; the oracle's logit_error_bound).
+ * Returns SV_ERR_NULL, SV_ERR_SHAPE or SV_ERR_ALIGN before launching; SV_ERR_CUDA
+ * when the tensor-map encoder or the launch fails; SV_OK once the work is queued
+ * on `stream` (a cudaStream_t). */
+sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int N, int d,
+                              float* logits, int32_t* flag, void* stream);
+
+/* spec_verify on logit rows computed from hidden states.
+ *   hidden_target [B][K+1][d] bf16 and weight_target [V][d] bf16 give the K+1
+ *                 target rows;
+ *   hidden_draft  [B][K][d_draft] bf16 and weight_draft [V][d_draft] bf16 give the
+ *                 K draft rows (an MTP head that shares the target's head passes
+ *                 the same weight); both NULL when every temperature is 0;
+ *   logits_scratch [B][2K+1][V] fp32, device, caller-owned, 16-byte aligned: the
+ *                 target rows [B][K+1][V] first, then the draft rows [B][K][V];
+ *                 they hold the computed logits when the call's work is done.
+ *   flag          as in spec_lm_head_logits (set when either GEMM timed out).
+ * The two GEMMs run first (spec_lm_head_logits), then spec_verify with SV_F32 on
+ * the scratch rows. All other arguments and results are those of spec_verify.
+ * Every argument is checked before anything is launched: SV_ERR_NULL,
+ * SV_ERR_SHAPE (B, K, V outside spec_verify's limits, or d / d_draft not a
+ * positive multiple of 64 up to 65,536), SV_ERR_ALIGN, SV_ERR_WORKSPACE; then
+ * SV_ERR_CUDA from a failed launch, else SV_OK. */
+sv_status spec_verify_from_hidden(const void* hidden_target, const void* weight_target, int d,
+                                  const void* hidden_draft, const void* weight_draft, int d_draft,
+                                  const int32_t* draft_tokens, const float* temperature,
+                                  const int32_t* top_k, const float* top_p, uint64_t philox_seed,
+                                  uint64_t philox_offset, int B, int K, int V, float* logits_scratch,
+                                  int32_t* flag, int32_t* out_tokens, int32_t* out_n_accepted,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_LM_HEAD_H */

@@ -17,7 +17,7 @@ from ._build import LIB, build
 
 __all__ = ["load", "spec_verify", "spec_verify_noalloc", "spec_verify_workspace_bytes",
            "spec_truncated_probs", "NOALLOC_SCRATCH_BYTES",
-           "spec_sample", "spec_philox_uniforms", "sv_version", "Workspace", "SV_BF16", "SV_F32", "SpecVerifyError"]
+           "spec_sample", "spec_philox_uniforms", "spec_lm_head_logits", "sv_version", "Workspace", "SV_BF16", "SV_F32", "SpecVerifyError"]
 
 SV_BF16, SV_F32 = 0, 1
 _STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "workspace", 5: "cuda",
@@ -59,6 +59,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_step.restype = i32
     lib.spec_accept_histogram.argtypes = [vp, i32, i32, vp, vp]
     lib.spec_accept_histogram.restype = i32
+    lib.spec_lm_head_logits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    lib.spec_lm_head_logits.restype = i32
+    lib.spec_verify_from_hidden.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, u64, u64, i32,
+                                            i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.spec_verify_from_hidden.restype = i32
     lib.sv_status_string.argtypes = [i32]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_version.argtypes = []
@@ -255,3 +260,25 @@ def spec_verify_step(target: torch.Tensor, draft: torch.Tensor | None, draft_tok
         None if seq_len is None else _dev(seq_len, "seq_len", torch.int32),
         workspace.buf.data_ptr(), workspace.nbytes, _stream(stream))
     _check(st, "spec_verify_step")
+
+
+def spec_lm_head_logits(hidden: torch.Tensor, weight: torch.Tensor, out: torch.Tensor | None = None,
+                        flag: torch.Tensor | None = None, stream=None):
+    """logits [..., V] fp32 = hidden [..., d] . weight [V, d]^T on the tensor cores
+    (bf16 operands). Returns (logits, flag); flag [1] int32 becomes 1 if a wait of
+    the kernel timed out. The kernel has not yet been run on a GPU."""
+    d = hidden.shape[-1]
+    V = weight.shape[0]
+    if weight.dim() != 2 or weight.shape[1] != d:
+        raise SpecVerifyError("weight must be [V, d] with the hidden states' d")
+    M = hidden.numel() // d
+    dev = hidden.device
+    if out is None:
+        out = torch.empty(*hidden.shape[:-1], V, dtype=torch.float32, device=dev)
+    if flag is None:
+        flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = load().spec_lm_head_logits(_dev(hidden, "hidden", torch.bfloat16), _dev(weight, "weight", torch.bfloat16),
+                                    M, V, d, _dev(out, "out", torch.float32), _dev(flag, "flag", torch.int32),
+                                    _stream(stream))
+    _check(st, "spec_lm_head_logits")
+    return out, flag

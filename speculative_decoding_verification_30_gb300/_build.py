@@ -8,9 +8,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libspec_verify.so")
 SOURCES = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "spec_verify_noalloc.cu"),
-           os.path.join(CSRC, "telemetry.cu")]
+           os.path.join(CSRC, "telemetry.cu"), os.path.join(CSRC, "lm_head.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(CSRC, "keyhist.cuh"),
-                  os.path.join(os.path.dirname(HERE), "include", "spec_verify.h")]
+                  os.path.join(os.path.dirname(HERE), "include", "spec_verify.h"),
+                  os.path.join(os.path.dirname(HERE), "include", "spec_lm_head.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -1,0 +1,316 @@
+// LM-head logits on the 5th-generation tensor cores, and the verify step fed from
+// hidden states (C ABI in include/spec_lm_head.h).
+//
+// Z[M][N] = H[M][d] . W[N][d]^T with bf16 operands and an fp32 accumulator: the
+// output projection that ends a decode step ("Apple Silikon İçin Cihaz Üstü
+// Çıkarımı Optimize Etme", perplexity.coolkeypoint.com, decode section).
+//
+// One CTA per 128 x 128 output tile. Both operands are K-major and staged by TMA
+// (128-byte swizzle, one 64-element K slice per stage) into a 4-stage ring; one
+// thread issues tcgen05.mma (M = 128, N = 128, K = 16) into a 128-column TMEM
+// accumulator; the four warps read it back with tcgen05.ld (warp w owns TMEM lanes
+// 32w..32w+31, i.e. those output rows) and store fp32 rows. Every wait is bounded:
+// a timeout sets the caller's flag, the CTA lets its issued copies land and frees
+// its TMEM before it returns.
+//
+// Not yet run on a GPU: compiled for sm_103a, exercised only by the argument checks.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spec_lm_head.h"
+
+namespace svlm {
+
+constexpr int BM = 128, BN = 128, BK = 64;   // BK bf16 = 128 bytes: one swizzle row
+constexpr int NS = 4;                          // pipeline stages
+constexpr int STAGE_A = BM * BK * 2, STAGE_B = BN * BK * 2;   // 16 KB each
+constexpr int TMEM_COLS = BN;                  // fp32 accumulator, 128 lanes x 128 columns
+constexpr uint64_t WAIT_NS = 200ull * 1000 * 1000;
+
+struct __align__(8) Ctl {
+  unsigned long long full[NS], empty[NS], done;
+  uint32_t taddr;
+  int err;
+};
+constexpr int SMEM_BYTES = 1024 /* alignment slack */ + NS * (STAGE_A + STAGE_B) + (int)sizeof(Ctl);
+
+__device__ __forceinline__ uint32_t sa(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void bar_init(unsigned long long* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_expect(unsigned long long* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try(unsigned long long* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for phase `parity` of b for at most WAIT_NS; false on timeout.
+__device__ __forceinline__ bool bar_wait(unsigned long long* b, uint32_t parity) {
+  if (bar_try(b, parity)) return true;
+  const uint64_t t0 = now_ns();
+  while (!bar_try(b, parity))
+    if (now_ns() - t0 > WAIT_NS) return false;
+  return true;
+}
+// 2-D tiled TMA load of the box at (x = K coordinate, y = row); x is a multiple
+// of 64 elements, so x * 2 bytes is 16-byte aligned.
+__device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, int x, int y,
+                                         unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(sa(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(sa(bar))
+      : "memory");
+}
+// Shared-memory matrix descriptor of a K-major operand with 128-byte swizzle:
+// start address, leading byte offset (unused with this swizzle), stride byte
+// offset 1024 (eight 128-byte rows), descriptor version 1, swizzle code 2. Stage
+// bases are 1024-byte aligned, so the base offset field stays 0.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor (kind::f16): fp32 D (bits 4-5 = 1), bf16 A and B (bits
+// 7-9 and 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma(uint32_t taddr, uint64_t a, uint64_t b, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(taddr),
+      "l"(a), "l"(b), "r"(IDESC), "r"(accum)
+      : "memory");
+}
+// Arrives on bar once every tcgen05 operation this thread issued before is done.
+__device__ __forceinline__ void commit(unsigned long long* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sa(bar))
+               : "memory");
+}
+
+__global__ void __launch_bounds__(128, 1)
+    lm_head_kernel(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapW,
+                   float* __restrict__ Z, int M, int N, int d, int32_t* flag) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + NS * STAGE_A;
+  Ctl& C = *reinterpret_cast<Ctl*>(smem + NS * (STAGE_A + STAGE_B));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nk = d / BK;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      bar_init(&C.full[s], 1);
+      bar_init(&C.empty[s], 1);
+    }
+    bar_init(&C.done, 1);
+    C.err = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 2) {   // the whole warp allocates (and later frees) the accumulator
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sa(&C.taddr)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  }
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t taddr = C.taddr;
+
+  int issued = 0;   // K slices the producer has loaded
+  if (warp == 0 && lane == 0) {
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % NS;
+      // reuse of stage s waits for the MMAs of its previous slice
+      if (kb >= NS && !bar_wait(&C.empty[s], (uint32_t)((kb / NS - 1) & 1))) {
+        atomicExch(&C.err, 1);
+        break;
+      }
+      if (*reinterpret_cast<volatile int*>(&C.err)) break;
+      bar_expect(&C.full[s], STAGE_A + STAGE_B);
+      tma_load(sA + s * STAGE_A, &mapH, kb * BK, m0, &C.full[s]);
+      tma_load(sB + s * STAGE_B, &mapW, kb * BK, n0, &C.full[s]);
+      issued = kb + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % NS;
+      if (!bar_wait(&C.full[s], (uint32_t)((kb / NS) & 1))) {
+        atomicExch(&C.err, 1);
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t a0 = sa(sA + s * STAGE_A), b0 = sa(sB + s * STAGE_B);
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k)   // 16 bf16 = 32 bytes along K per instruction
+        mma(taddr, sdesc(a0 + k * 32), sdesc(b0 + k * 32), (kb | k) != 0);
+      commit(&C.empty[s]);
+    }
+    commit(&C.done);
+  }
+  __syncwarp();
+
+  // tcgen05.ld is warp-collective: every thread of the block takes the same branch
+  const bool ok = __syncthreads_and(bar_wait(&C.done, 0u) && !*reinterpret_cast<volatile int*>(&C.err)) != 0;
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (ok) {
+    const int row = m0 + warp * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      const uint32_t ta = taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32);
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+          "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+          "[%32];"
+          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+            "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+            "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+            "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          : "r"(ta));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const int col = n0 + c * 32;
+      if (row < M && col < N) {
+        float* zr = Z + (size_t)row * N + col;
+        const int lim = min(32, N - col);
+        if (lim == 32 && (reinterpret_cast<uintptr_t>(zr) & 15) == 0) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(zr + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                             __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        } else {
+          for (int j = 0; j < lim; ++j) zr[j] = __uint_as_float(r[j]);
+        }
+      }
+    }
+  }
+  // after a timeout, the copies issued but never consumed land before the CTA leaves
+  if (warp == 0 && lane == 0 && C.err) {
+    for (int kb = issued > NS ? issued - NS : 0; kb < issued; ++kb)
+      bar_wait(&C.full[kb % NS], (uint32_t)((kb / NS) & 1));
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 2) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TMEM_COLS)
+                 : "memory");
+  }
+  if (tid == 0 && !ok) atomicExch(flag, 1);
+}
+
+typedef CUresult (*EncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// rows x d bf16, row-major; boxes of 64 x box_rows with 128-byte swizzle; rows
+// past the end read as zero
+static bool make_map(CUtensorMap* map, const void* base, int rows, int d, int box_rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace svlm
+
+sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int N, int d, float* logits,
+                              int32_t* flag, void* stream) {
+  using namespace svlm;
+  if (!hidden || !weight || !logits || !flag) return SV_ERR_NULL;
+  if (M < 1 || M > 65535 * BM || N < 1 || d < BK || d > 65536 || d % BK) return SV_ERR_SHAPE;
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(logits, 4) || !aligned(flag, 4))
+    return SV_ERR_ALIGN;
+  CUtensorMap mh, mw;
+  if (!make_map(&mh, hidden, M, d, BM) || !make_map(&mw, weight, N, d, BN)) return SV_ERR_CUDA;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+        cudaSuccess)
+      return SV_ERR_CUDA;
+    attr = true;
+  }
+  const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  lm_head_kernel<<<grid, 128, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(mh, mw, logits, M, N, d, flag);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status spec_verify_from_hidden(const void* hidden_target, const void* weight_target, int d,
+                                  const void* hidden_draft, const void* weight_draft, int d_draft,
+                                  const int32_t* draft_tokens, const float* temperature, const int32_t* top_k,
+                                  const float* top_p, uint64_t philox_seed, uint64_t philox_offset, int B, int K,
+                                  int V, float* logits_scratch, int32_t* flag, int32_t* out_tokens,
+                                  int32_t* out_n_accepted, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  // every argument is checked here, so that an error launches nothing
+  if (!hidden_target || !weight_target || !logits_scratch || !flag || !draft_tokens || !temperature ||
+      !top_k || !top_p || !out_tokens || !out_n_accepted || !workspace)
+    return SV_ERR_NULL;
+  if ((hidden_draft == nullptr) != (weight_draft == nullptr)) return SV_ERR_NULL;
+  const auto bad_d = [](int dd) { return dd < svlm::BK || dd > 65536 || dd % svlm::BK != 0; };
+  if (B < 1 || B > 65535 || K < 1 || K > 16 || V < 2 || V > 262144 || bad_d(d) ||
+      (hidden_draft && bad_d(d_draft)))
+    return SV_ERR_SHAPE;
+  if (!svlm::aligned(logits_scratch, 16) || !svlm::aligned(hidden_target, 16) ||
+      !svlm::aligned(weight_target, 16) || !svlm::aligned(flag, 4) ||
+      (hidden_draft && (!svlm::aligned(hidden_draft, 16) || !svlm::aligned(weight_draft, 16))))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < spec_verify_workspace_bytes(B, K)) return SV_ERR_WORKSPACE;
+  float* zt = logits_scratch;
+  float* zd = logits_scratch + (size_t)B * (K + 1) * V;
+  sv_status s = spec_lm_head_logits(hidden_target, weight_target, B * (K + 1), V, d, zt, flag, stream);
+  if (s != SV_OK) return s;
+  if (hidden_draft) {
+    s = spec_lm_head_logits(hidden_draft, weight_draft, B * K, V, d_draft, zd, flag, stream);
+    if (s != SV_OK) return s;
+  }
+  return spec_verify(zt, hidden_draft ? zd : nullptr, SV_F32, draft_tokens, temperature, top_k, top_p,
+                     philox_seed, philox_offset, B, K, V, out_tokens, out_n_accepted, workspace,
+                     workspace_bytes, stream);
+}

@@ -1,6 +1,6 @@
 """Host-side checks of the C ABI (no GPU needed): the library builds, loads,
-exports every function include/spec_verify.h declares, and rejects bad
-arguments before launching anything."""
+exports every function include/*.h declares, and rejects bad arguments before
+launching anything."""
 import ctypes
 import os
 import re
@@ -10,14 +10,17 @@ import pytest
 import speculative_decoding_verification_30_gb300 as sv
 from speculative_decoding_verification_30_gb300 import _build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "spec_verify.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:sv_status|size_t|int|const char\*)\s+(\w+)\s*\(",
-                                 src, flags=re.M)))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if not h.endswith(".h"):
+            continue
+        src = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:sv_status|size_t|int|const char\*)\s+(\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
 
 
 def test_library_builds_and_exports_every_declared_symbol():
@@ -25,7 +28,7 @@ def test_library_builds_and_exports_every_declared_symbol():
     lib = ctypes.CDLL(path)
     names = declared_functions()
     assert {"spec_verify", "spec_verify_workspace_bytes", "spec_truncated_probs",
-            "spec_sample", "sv_status_string"} <= set(names)
+            "spec_sample", "sv_status_string", "spec_lm_head_logits", "spec_verify_from_hidden"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -78,3 +81,27 @@ def test_noalloc_entry_point_rejects_oversized_batches_before_any_cuda_call():
     assert lib.spec_verify_noalloc(*args(65535, 16)) == 7
     assert lib.spec_verify_noalloc(*args(0, 4)) == 2
     assert lib.spec_verify_noalloc(*args(4, 17)) == 2
+
+
+def test_lm_head_entry_points_validate_before_launching():
+    lib = sv.load()
+    A = 1 << 12
+
+    def lm(h=A, w=A, M=128, N=256, d=128, z=A, f=A):
+        return lib.spec_lm_head_logits(h, w, M, N, d, z, f, None)
+    assert lm(h=None) == 1 and lm(z=None) == 1 and lm(f=None) == 1
+    assert lm(M=0) == 2 and lm(N=0) == 2 and lm(d=0) == 2 and lm(d=96) == 2 and lm(d=65600) == 2
+    assert lm(M=65535 * 128 + 1) == 2
+    assert lm(h=A + 8) == 6 and lm(w=A + 4) == 6 and lm(z=A + 2) == 6
+
+    wsb = sv.spec_verify_workspace_bytes(2, 2)
+
+    def vh(ht=A, wt=A, d=128, hd=A, wd=A, dd=64, B=2, K=2, V=1024, z=A, ws=A, wsb=wsb):
+        return lib.spec_verify_from_hidden(ht, wt, d, hd, wd, dd, A, A, A, A, 0, 0, B, K, V, z, A, A, A,
+                                           ws, wsb, None)
+    assert vh(ht=None) == 1 and vh(z=None) == 1 and vh(ws=None) == 1
+    assert vh(hd=None) == 1                    # draft hidden states without their weight
+    assert vh(B=0) == 2 and vh(K=17) == 2 and vh(V=1) == 2 and vh(V=262145) == 2
+    assert vh(d=65) == 2 and vh(dd=100) == 2
+    assert vh(z=A + 4) == 6 and vh(ht=A + 8) == 6
+    assert vh(wsb=8) == 4
