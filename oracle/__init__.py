@@ -12,14 +12,14 @@ and feeds them to the same verify.
 """
 from . import lm_head
 from .philox import philox4, philox4x32_10, to_uniform, uniforms
-from .sampler import (BOUNDARY, SeqResult, Truncated, accepts, descending_order, draft_sample,
+from .sampler import (BOUNDARY, SeqResult, Truncated, accept_margin, accepts, descending_order, draft_sample,
                       inverse_cdf, residual_weights, sample_row, truncate, truncated_probs, verify_batch,
                       verify_sequence)
 
 __all__ = [
     "lm_head",
     "philox4", "philox4x32_10", "to_uniform", "uniforms",
-    "BOUNDARY", "SeqResult", "Truncated", "accepts", "descending_order", "draft_sample",
+    "BOUNDARY", "SeqResult", "Truncated", "accept_margin", "accepts", "descending_order", "draft_sample",
     "inverse_cdf", "residual_weights", "sample_row", "truncate", "truncated_probs", "verify_batch",
     "verify_sequence",
 ]

@@ -64,6 +64,22 @@ def descending_order(z: np.ndarray) -> np.ndarray:
     return np.lexsort((ids, -z))
 
 
+def topp_margin(excl: np.ndarray, n_keep: int, top_p: float) -> float:
+    """Distance of top_p from the nearest value at which the nucleus changes.
+
+    excl[j] is the renormalised mass strictly before the j-th token of L1 (in
+    (logit desc, id asc) order) and the first n_keep tokens are kept (those with
+    excl < top_p). Lowering top_p to excl[n_keep-1] drops the last kept token;
+    raising it above excl[n_keep] (the mass before the first dropped token) keeps
+    one more. The margin is the smaller of the two distances (only the first when
+    no token was dropped). The first token is kept for every top_p > 0 (its
+    exclusive mass is 0), so with a single kept token only the upper side counts."""
+    margin = top_p - excl[n_keep - 1] if n_keep > 1 else math.inf
+    if n_keep < len(excl):
+        margin = min(margin, excl[n_keep] - top_p)
+    return float(margin)
+
+
 def truncate(z, temperature: float, top_k: int, top_p: float) -> Truncated:
     """Temperature-scaled softmax restricted by top-k then top-p, renormalised.
 
@@ -83,9 +99,7 @@ def truncate(z, temperature: float, top_k: int, top_p: float) -> Truncated:
         excl = np.concatenate(([0.0], np.cumsum(w)[:-1]))   # mass strictly before each token
         n_keep = int(np.count_nonzero(excl < top_p))         # excl is increasing: a prefix
         n_keep = max(n_keep, 1)
-        margin = top_p - excl[n_keep - 1]
-        if n_keep < kk:
-            margin = min(margin, excl[n_keep] - top_p)
+        margin = topp_margin(excl, n_keep, top_p)
     kept = top[:n_keep]
     probs = np.zeros(V, dtype=np.float64)
     probs[kept] = e[kept] / np.sum(e[kept])
@@ -155,6 +169,15 @@ def accepts(u: float, p_d: float, q_d: float) -> bool:
     return u * q_d < p_d
 
 
+def accept_margin(u: float, p_d: float, q_d: float) -> float:
+    """Distance of the acceptance uniform u from the value at which accepts() flips.
+
+    For q > 0 the test u*q < p flips at u = p/q, so the margin is |u - p/q|; for
+    q == 0 the outcome does not depend on u (accept iff p > 0) and the margin is
+    infinite."""
+    return abs(u - p_d / q_d) if q_d > 0.0 else math.inf
+
+
 def residual_weights(p: np.ndarray, q: np.ndarray) -> np.ndarray:
     """(p - q)+, the distribution a rejected position is resampled from (unnormalised);
     falls back to p when its mass is zero."""
@@ -209,7 +232,7 @@ def verify_sequence(target, draft, draft_tokens, temperature: float, top_k: int,
         pd, qd = p.probs[d[i]], q.probs[d[i]]
         res.n_draws += 1
         if qd > 0.0:
-            res.accept_margins.append(abs(u - pd / qd))
+            res.accept_margins.append(accept_margin(u, pd, qd))
         if accepts(u, pd, qd):
             continue
         n = i
