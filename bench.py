@@ -178,12 +178,106 @@ def replica_input_step(rank: int, s: int) -> int:
     return 1000 * rank + s
 
 
+def make_sets(w, rank, dev, greedy):
+    """Input sets of workload w resident in HBM (rotated so every step reads HBM),
+    with drafted tokens from the library's own draft sampler (not timed)."""
+    import torch
+
+    import speculative_decoding_verification_30_gb300 as sv
+    from speculative_decoding_verification_30_gb300.workloads import make_batch
+
+    set_bytes = w.bytes_per_step(needed_only=True, greedy=greedy)
+    nsets = max(2, -(-3 * L2_BYTES // max(1, set_bytes)))
+    nsets = min(nsets, 64)
+    sets = []
+    for s in range(nsets):
+        b = make_batch(w, replica_input_step(rank, s), device=dev)
+        T, k, P = b.temperature.to(dev), b.top_k.to(dev), b.top_p.to(dev)
+        dtok = sv.spec_sample(b.draft, T, k, P, seed=4242, offset=10_000 + s)
+        sets.append((b.target, None if greedy else b.draft, dtok, T, k, P))
+    torch.cuda.synchronize()
+    return sets, set_bytes
+
+
+def time_steps(w, sets, steps, warmup, rank, dev, ws=1, stream=None):
+    """W untimed warm-up calls, then K timed calls between CUDA events on the
+    launching stream (barrier + synchronize on both sides). Returns (total_ms,
+    mean per-call ms, clock summary)."""
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_30_gb300 as sv
+
+    B, K = w.B, w.K
+    nsets = len(sets)
+    wspace = sv.Workspace(B, K, dev)
+    out_tok = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    stream = stream or torch.cuda.current_stream()
+
+    def step(t):
+        tg, dr, dt, T, k, P = sets[t % nsets]
+        sv.spec_verify(tg, dr, dt, T, k, P, seed=1234 + rank, offset=t, out_tokens=out_tok,
+                       out_n=out_n, workspace=wspace, stream=stream)
+
+    for t in range(warmup):
+        step(t)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for t in range(steps):
+            starts[t].record(stream)
+            step(warmup + t)
+            ends[t].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.25)
+    if ws > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    return total_ms, per_launch_ms, clk.summary(), wspace, out_tok, out_n
+
+
+def other_workloads(args, dev, peak):
+    """The other bench-size workloads, measured in the same process: the greedy
+    batch (B=256), the mixed fp32 batch (B=512) and the B=1 MTP decode shape."""
+    from speculative_decoding_verification_30_gb300.workloads import WORKLOADS
+    res = {}
+    for name, steps in (("greedy", 100), ("mixed", 20), ("mtp_decode", 200)):
+        w = WORKLOADS[name]
+        greedy = name == "greedy"
+        sets, _ = make_sets(w, 0, dev, greedy)
+        total_ms, per_ms, clocks, *_ = time_steps(w, sets, steps, 5, 0, dev)
+        alg = w.bytes_per_step(needed_only=True, greedy=greedy)
+        ach = alg / (per_ms / 1e3) / 1e9
+        entry = {"config": {"B": w.B, "K": w.K, "V": w.V, "description": w.description},
+                 "ms_per_step": total_ms / steps, "launch_ms": per_ms,
+                 "value": w.rows_per_step() / (total_ms / steps / 1e3), "unit": "rows/s",
+                 "alg_bytes_per_step": alg, "achieved_GBps": ach, "frac": ach / peak,
+                 "kernel": dominant_kernel(name), "gpu_launches_per_step": launches_per_call(name),
+                 "clocks": clocks, "steps": steps}
+        if name == "greedy":
+            entry["bytes_note"] = ("needed bytes (target rows only; greedy reads no draft rows); "
+                                   f"the formula B(2K+1)Vs gives {w.bytes_per_step()} B")
+        res[name] = entry
+        del sets
+    return res
+
+
 def bench_gpu(args):
     import torch
     import torch.distributed as dist
 
     import speculative_decoding_verification_30_gb300 as sv
-    from speculative_decoding_verification_30_gb300.workloads import WORKLOADS, make_batch
+    from speculative_decoding_verification_30_gb300.workloads import WORKLOADS
 
     ws, rank, lrank = dist_env()
     torch.cuda.set_device(lrank)
@@ -195,50 +289,11 @@ def bench_gpu(args):
     greedy = args.workload == "greedy"
     sv.load()
 
-    set_bytes = w.bytes_per_step(needed_only=True, greedy=greedy)
-    nsets = max(2, -(-3 * L2_BYTES // max(1, set_bytes)))
-    nsets = min(nsets, 64)
-    sets = []
-    for s in range(nsets):
-        b = make_batch(w, replica_input_step(rank, s), device=dev)
-        T, k, P = b.temperature.to(dev), b.top_k.to(dev), b.top_p.to(dev)
-        # drafted tokens: the library's own draft-side sampler (d ~ q), not timed
-        dtok = sv.spec_sample(b.draft, T, k, P, seed=4242, offset=10_000 + s)
-        sets.append((b.target, None if greedy else b.draft, dtok, T, k, P))
-    torch.cuda.synchronize()
-    wspace = sv.Workspace(B, K, dev)
-    out_tok = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
-    out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    sets, set_bytes = make_sets(w, rank, dev, greedy)
+    nsets = len(sets)
     stream = torch.cuda.current_stream()
-
-    def step(t):
-        tg, dr, dt, T, k, P = sets[t % nsets]
-        sv.spec_verify(tg, dr, dt, T, k, P, seed=1234 + rank, offset=t, out_tokens=out_tok,
-                       out_n=out_n, workspace=wspace, stream=stream)
-
-    for t in range(args.warmup):
-        step(t)
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(lrank) as clk:
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for t in range(args.steps):
-            starts[t].record(stream)
-            step(args.warmup + t)
-            ends[t].record(stream)
-        t1.record(stream)
-        torch.cuda.synchronize()
-        time.sleep(0.25)
-    if ws > 1:
-        dist.barrier()
-    total_ms = t0.elapsed_time(t1)
-    per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    total_ms, per_launch_ms, clocks, wspace, out_tok, out_n = time_steps(
+        w, sets, args.steps, args.warmup, rank, dev, ws, stream)
     rows_per_step = w.rows_per_step()
     ms_per_step, value = job_throughput(total_ms, args.steps, rows_per_step, ws, dev)
 
@@ -324,8 +379,12 @@ def bench_gpu(args):
                                "least this"},
         "gpu_launches": launches_per_call(w.name) * args.steps,
         "e2e": e2e,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
+    if rank == 0 and ws == 1 and not args.no_others and args.workload == "nucleus_batch":
+        del sets
+        torch.cuda.empty_cache()
+        line["other_workloads"] = other_workloads(args, dev, peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if rank == 0:
@@ -334,35 +393,68 @@ def bench_gpu(args):
         dist.destroy_process_group()
 
 
-def cpu_baseline(w, budget_s: float = 15.0, steps: int = 1):
-    """The float64 oracle on the host cores over a bounded sample of the workload."""
-    import torch
-
+def _oracle_seq(job):
+    """One sequence through the oracle (a process-pool task)."""
     from oracle import sampler
+    tg, dr, d, T, k, P, step, s = job
+    sampler.verify_sequence(tg, dr, d, T, k, P, 1, step, s)
+    return 1
+
+
+def _oracle_jobs(w, step, nb):
     from speculative_decoding_verification_30_gb300.workloads import (draft_tokens_by_rank,
                                                                        make_batch)
+    b = make_batch(w, 50_000 + step, B=min(nb, w.B))
+    dtok = draft_tokens_by_rank(b.draft, step, w.cid)
+    tg = b.target.float().double().numpy()
+    dr = b.draft.float().double().numpy()
+    return [(tg[s], dr[s], dtok[s].tolist(), float(b.temperature[s]), int(b.top_k[s]),
+             float(b.top_p[s]), step, s) for s in range(tg.shape[0])]
+
+
+def cpu_baseline(w, budget_s: float = 15.0, all_cores: bool = True):
+    """The float64 oracle, as it stands, on the host over a bounded sample of the
+    workload: single-threaded, and (all_cores) a spawn-started process pool over
+    sequences on every host core. value = the all-cores rate when measured."""
+    import multiprocessing as mp
+
+    host_cores = os.cpu_count() or 1
     nb = 2 if w.V > 10_000 else w.B
-    done_rows, spent = 0, 0.0
-    seqs = 0
-    step = 0
-    while spent < budget_s:
-        b = make_batch(w, 50_000 + step, B=min(nb, w.B))
-        dtok = draft_tokens_by_rank(b.draft, step, w.cid)
-        tg = b.target.float().double().numpy()
-        dr = b.draft.float().double().numpy()
+    done_rows, spent, seqs, step = 0, 0.0, 0, 0
+    single_budget = budget_s / 2 if all_cores and host_cores > 1 else budget_s
+    while spent < single_budget and step < 10_000:
+        jobs = _oracle_jobs(w, step, nb)
         t0 = time.perf_counter()
-        for s in range(tg.shape[0]):
-            sampler.verify_sequence(tg[s], dr[s], dtok[s].tolist(), float(b.temperature[s]),
-                                    int(b.top_k[s]), float(b.top_p[s]), 1, step, s)
+        for j in jobs:
+            _oracle_seq(j)
         spent += time.perf_counter() - t0
-        seqs += tg.shape[0]
-        done_rows += tg.shape[0] * (2 * w.K + 1)
+        seqs += len(jobs)
+        done_rows += len(jobs) * (2 * w.K + 1)
         step += 1
-        if step >= 10_000:
-            break
-    return {"value": done_rows / spent, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{seqs} sequences of {w.name} (K={w.K}, V={w.V}), {spent:.1f} s "
-                      f"single-threaded float64 NumPy"}
+    v1 = done_rows / spent
+    out = {"value": v1, "unit": "rows/s", "cores": 1, "kind": "oracle", "host_cores": host_cores,
+           "value_1core": v1,
+           "sample": f"{seqs} sequences of {w.name} (K={w.K}, V={w.V}), {spent:.1f} s "
+                     f"single-threaded float64 NumPy"}
+    if all_cores and host_cores > 1:
+        # enough sequences for every core to stay busy for about half the budget
+        per_seq = spent / max(1, seqs)
+        n_all = max(host_cores, int(host_cores * (budget_s / 2) / max(per_seq, 1e-6)))
+        jobs, st = [], 0
+        while len(jobs) < n_all:
+            jobs += _oracle_jobs(w, 20_000 + st, max(nb, host_cores))
+            st += 1
+        jobs = jobs[:n_all]
+        with mp.get_context("spawn").Pool(host_cores) as pool:
+            pool.map(_oracle_seq, jobs[:host_cores])           # start the workers
+            t0 = time.perf_counter()
+            pool.map(_oracle_seq, jobs, chunksize=1)
+            dt = time.perf_counter() - t0
+        va = len(jobs) * (2 * w.K + 1) / dt
+        out.update({"value": va, "cores": host_cores, "value_all_cores": va,
+                    "sample": out["sample"] + f"; then {len(jobs)} sequences in {dt:.1f} s on a "
+                              f"{host_cores}-process pool (one sequence per task)"})
+    return out
 
 
 def bench_reference(args):
@@ -374,7 +466,7 @@ def bench_reference(args):
     w = WORKLOADS[args.workload]
     budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        cpu_baseline(w, budget_s=0.5)
+        cpu_baseline(w, budget_s=0.5, all_cores=False)
     vals = [cpu_baseline(w, budget_s=budget) for _ in range(args.steps)]
     value = statistics.mean(v["value"] for v in vals)
     ms_per_step = 1e3 * w.rows_per_step() / value
@@ -386,7 +478,11 @@ def bench_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V,
                    "description": w.description},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": vals[0]["cores"],
+                         "host_cores": vals[0]["host_cores"], "kind": "oracle",
+                         "value_1core": statistics.mean(v["value_1core"] for v in vals),
+                         "value_all_cores": (statistics.mean(v["value_all_cores"] for v in vals)
+                                             if "value_all_cores" in vals[0] else None),
                          "sample": vals[0]["sample"]},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -403,6 +499,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the greedy, mixed and MTP-decode workloads measured after the headline")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -84,8 +84,11 @@ typedef enum {
 /* Bytes of device workspace spec_verify needs for (B, K). The workspace must
  * be 16-byte aligned and zero-filled before its first use (e.g. with
  * cudaMemsetAsync); every spec_verify call leaves it zero-filled again, so it
- * can be reused by later calls on the same stream. Two calls that may run at
- * the same time must not share a workspace. */
+ * can be reused by later calls on the same stream. This includes a call in which
+ * a bounded wait gave up (its sequences are reported as data errors, n = -1).
+ * A call that returns SV_ERR_CUDA may have queued part of its kernels: zero the
+ * workspace again (cudaMemsetAsync on the same stream) before reusing it. Two
+ * calls that may run at the same time must not share a workspace. */
 size_t spec_verify_workspace_bytes(int B, int K);
 
 /* One verify-and-sample step for a batch.
@@ -145,7 +148,10 @@ sv_status spec_verify_step(const void* target_logits, const void* draft_logits, 
  *     batches return SV_ERR_SCRATCH and launch nothing (use spec_verify with a
  *     workspace).
  *   - The scratch is zero when the library loads, and each call leaves it zero
- *     again; a call must run to completion before the next one starts.
+ *     again; a call must run to completion before the next one starts. When
+ *     spec_verify fails after queueing part of its work (SV_ERR_CUDA), this entry
+ *     point queues a cudaMemsetAsync of the scratch on `stream` before returning the
+ *     error, so the next call starts from zero (no allocation is involved).
  *   - The first call on a device looks up the scratch's device address with that
  *     device current (cudaGetSymbolAddress, which may load the module); make that
  *     first call outside any stream capture. Later calls reuse the cached address.

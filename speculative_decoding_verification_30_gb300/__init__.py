@@ -17,7 +17,7 @@ from ._build import LIB, build
 
 __all__ = ["load", "spec_verify", "spec_verify_noalloc", "spec_verify_workspace_bytes",
            "spec_truncated_probs", "NOALLOC_SCRATCH_BYTES",
-           "spec_sample", "spec_philox_uniforms", "spec_lm_head_logits", "sv_version", "Workspace", "SV_BF16", "SV_F32", "SpecVerifyError"]
+           "spec_sample", "spec_philox_uniforms", "spec_lm_head_logits", "spec_verify_from_hidden", "sv_version", "Workspace", "SV_BF16", "SV_F32", "SpecVerifyError"]
 
 SV_BF16, SV_F32 = 0, 1
 _STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "workspace", 5: "cuda",
@@ -282,3 +282,45 @@ def spec_lm_head_logits(hidden: torch.Tensor, weight: torch.Tensor, out: torch.T
                                     _stream(stream))
     _check(st, "spec_lm_head_logits")
     return out, flag
+
+
+def spec_verify_from_hidden(hidden_target: torch.Tensor, weight_target: torch.Tensor,
+                            hidden_draft: torch.Tensor | None, weight_draft: torch.Tensor | None,
+                            draft_tokens: torch.Tensor, temperature: torch.Tensor,
+                            top_k: torch.Tensor, top_p: torch.Tensor, seed: int = 0, offset: int = 0,
+                            logits_scratch: torch.Tensor | None = None,
+                            flag: torch.Tensor | None = None, out_tokens: torch.Tensor | None = None,
+                            out_n: torch.Tensor | None = None, workspace: "Workspace | None" = None,
+                            stream=None):
+    """spec_verify on logit rows computed from hidden states on the tensor cores:
+    hidden_target [B, K+1, d] and weight_target [V, d] (bf16) give the target rows,
+    hidden_draft [B, K, d'] and weight_draft [V, d'] the draft rows (None for a
+    greedy batch). Returns (out_tokens, out_n, flag); the results are valid only
+    when flag stays 0 (a timed-out wait of a GEMM sets it)."""
+    B, K1, d = hidden_target.shape
+    K = K1 - 1
+    V = weight_target.shape[0]
+    dev = hidden_target.device
+    if logits_scratch is None:
+        logits_scratch = torch.empty(B * (2 * K + 1) * V, dtype=torch.float32, device=dev)
+    if flag is None:
+        flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    if out_n is None:
+        out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = Workspace(B, K, dev)
+    hd = _dev(hidden_draft, "hidden_draft", torch.bfloat16) if hidden_draft is not None else None
+    wd = _dev(weight_draft, "weight_draft", torch.bfloat16) if weight_draft is not None else None
+    dd = hidden_draft.shape[-1] if hidden_draft is not None else 64
+    st = load().spec_verify_from_hidden(
+        _dev(hidden_target, "hidden_target", torch.bfloat16),
+        _dev(weight_target, "weight_target", torch.bfloat16), d, hd, wd, dd,
+        _dev(draft_tokens, "draft_tokens", torch.int32), _dev(temperature, "temperature", torch.float32),
+        _dev(top_k, "top_k", torch.int32), _dev(top_p, "top_p", torch.float32), seed, offset, B, K, V,
+        _dev(logits_scratch, "logits_scratch", torch.float32), _dev(flag, "flag", torch.int32),
+        _dev(out_tokens, "out_tokens", torch.int32), _dev(out_n, "out_n", torch.int32),
+        workspace.buf.data_ptr(), workspace.nbytes, _stream(stream))
+    _check(st, "spec_verify_from_hidden")
+    return out_tokens, out_n, flag

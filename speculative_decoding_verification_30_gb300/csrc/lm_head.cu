@@ -20,6 +20,7 @@
 #include <stdint.h>
 
 #include "../../include/spec_lm_head.h"
+#include "launch_cache.h"
 
 namespace svlm {
 
@@ -258,6 +259,8 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int d, int bo
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+static sv::LaunchCache g_lm_cache;
+
 }  // namespace svlm
 
 sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int N, int d, float* logits,
@@ -269,13 +272,14 @@ sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int
     return SV_ERR_ALIGN;
   CUtensorMap mh, mw;
   if (!make_map(&mh, hidden, M, d, BM) || !make_map(&mw, weight, N, d, BN)) return SV_ERR_CUDA;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-        cudaSuccess)
-      return SV_ERR_CUDA;
-    attr = true;
-  }
+  // the kernel's shared-memory limit, raised once per device
+  int dev = 0, done = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      g_lm_cache.get(dev, reinterpret_cast<const void*>(lm_head_kernel), SMEM_BYTES, 0, &done, [](int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      }) != cudaSuccess)
+    return SV_ERR_CUDA;
   const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
   lm_head_kernel<<<grid, 128, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(mh, mw, logits, M, N, d, flag);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;

@@ -43,7 +43,10 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <thread>
+
 #include "../../include/spec_verify.h"
+#include "launch_cache.h"
 #include "sv_device.cuh"
 
 namespace sv {
@@ -83,7 +86,7 @@ struct Params {
   float* out_probs;
   unsigned long long* ws_units; // per unit: bits 0..31 token, bit 32 flag, bit 33 error
   unsigned int* ws_tickets;     // per sequence
-  unsigned int* ws_error;       // sticky: bit 0 = a bulk copy did not complete in time
+  unsigned int* ws_error;       // bit 0 = a bulk copy did not complete in time (cleared at the call's end)
   unsigned long long* ws_best;  // greedy rows: (okey(max) << 32) | ~argmax
   unsigned int* ws_rcnt;        // [0]: greedy_kernel CTAs finished
   unsigned int* ws_rflag;       // greedy rows: NaN / +inf seen
@@ -1145,6 +1148,7 @@ __device__ __forceinline__ int unit_rows(const Params& P, const Meta& m, int i) 
   if (param_error<MODE>(P, m, i)) return 0;
   if (MODE == MODE_VERIFY && P.greedy_split && m.g) return 0;   // greedy path
   if (MODE == MODE_SAMPLE && P.fast_split && m.g) return 0;      // served by keyhist_sample_kernel
+  if (MODE == MODE_PROBS && P.fast_split && m.g) return 0;       // served by keyhist_probs_kernel
   if (MODE == MODE_VERIFY && i < P.K && m.T > 0.0f) return 2;
   return 1;
 }
@@ -1190,6 +1194,9 @@ __device__ __noinline__ void load_meta(Shared& S, const Params& P, int cid, int 
               : 0;
     // draft sampler: rows keyhist_sample_kernel served (not marked for this kernel)
     if (MODE == MODE_SAMPLE && P.fast_split) m.g = P.out_tokens[(size_t)b * P.K + i] != KH_HANDBACK;
+    // truncated probabilities: rows keyhist_probs_kernel wrote (not marked for this kernel)
+    if (MODE == MODE_PROBS && P.fast_split)
+      m.g = __float_as_uint(P.out_probs[(size_t)b * P.V]) != KH_PROBS_HANDBACK;
     S.meta[j % MR] = m;
   }
 }
@@ -1333,8 +1340,9 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
         for (int l = tid; l < vlen; l += NT) P.out_probs[(size_t)b * P.V + base + l] = __int_as_float(0x7fc00000);
       }
     } else if ((MODE == MODE_VERIFY && P.greedy_split && m.g) ||
-               (MODE == MODE_SAMPLE && P.fast_split && m.g)) {
-      // units served by greedy_kernel, keyhist_kernel or keyhist_sample_kernel
+               ((MODE == MODE_SAMPLE || MODE == MODE_PROBS) && P.fast_split && m.g)) {
+      // units served by greedy_kernel, keyhist_kernel, keyhist_sample_kernel or
+      // keyhist_probs_kernel
     } else if (m.T == 0.0f) {
       // ------------------------------------------------ greedy (T = 0)
       X1Row& x = S.x1[xr & 1][0];
@@ -1765,6 +1773,9 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
     if (atomicAdd(P.ws_done, 1u) == gridDim.x - 1u) {
       *P.ws_work = 0u;
       *P.ws_done = 0u;
+      // a timed-out wait of this call was already reported in band (its sequences
+      // are data errors); clear its flag so the workspace is zero for the next call
+      *P.ws_error = 0u;
     }
   }
 }
@@ -2019,24 +2030,45 @@ static Geometry geometry(int V, int es) {
   return g;
 }
 
+static LaunchCache g_launch_cache;
+
+// Raises (never lowers) a kernel's dynamic shared-memory limit on the current
+// device: launches with different sizes share the attribute.
+static cudaError_t ensure_smem_limit(const void* fn, size_t smem) {
+  cudaFuncAttributes fa;
+  cudaError_t r = cudaFuncGetAttributes(&fa, fn);
+  if (r != cudaSuccess) return r;
+  if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+// Resident grid of a persistent kernel on the current device (SMs times the CTAs
+// of `threads` threads and `smem` dynamic shared memory that fit one SM), with the
+// kernel's dynamic shared-memory limit raised on this device first.
+static cudaError_t resident_grid(const void* fn, int threads, size_t smem, int* grid) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return g_launch_cache.get(dev, fn, smem, threads, grid, [&](int* v) {
+    cudaError_t r;
+    if ((r = ensure_smem_limit(fn, smem)) != cudaSuccess) return r;
+    int sms = 0, per = 0;
+    if ((r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return r;
+    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, threads, smem)) != cudaSuccess) return r;
+    *v = (sms > 1 ? sms : 1) * (per > 1 ? per : 1);
+    return cudaSuccess;
+  });
+}
+static cudaError_t keyhist_grid(void (*fn)(const Params, int), int* grid) {
+  return resident_grid(reinterpret_cast<const void*>(fn), KT, KH_SMEM, grid);
+}
+
 template <typename DT, int MODE>
 static cudaError_t launch(const Params& p, const Geometry& g, cudaStream_t st) {
   auto kern = sv_kernel<DT, MODE>;
-  static size_t configured = 0;
-  static int cached_C = 0;
-  static size_t cached_smem = 0;
-  static int cached_dev = -1;
-  static int max_clusters = 0;
   cudaError_t e;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if (g.smem > configured) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured = g.smem;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = g.smem;
@@ -2052,16 +2084,23 @@ static cudaError_t launch(const Params& p, const Geometry& g, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (MODE == MODE_VERIFY && p.greedy_split) ? 2 : 1;
-  if (cached_C != g.C || cached_smem != g.smem || cached_dev != dev) {
-    cfg.gridDim = dim3((unsigned)g.C, 1, 1);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    max_clusters = n > 0 ? n : 1;
-    cached_C = g.C;
-    cached_smem = g.smem;
-    cached_dev = dev;
-  }
+  // clusters that fit the device at once, with the kernel's attributes set on this
+  // device (cached per device, cluster size and shared memory)
+  int max_clusters = 0;
+  e = g_launch_cache.get(dev, reinterpret_cast<const void*>(kern), g.smem, g.C, &max_clusters,
+                         [&](int* v) {
+                           cudaError_t r = ensure_smem_limit(reinterpret_cast<const void*>(kern), g.smem);
+                           if (r != cudaSuccess) return r;
+                           r = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                           if (r != cudaSuccess) return r;
+                           cudaLaunchConfig_t q = cfg;
+                           q.gridDim = dim3((unsigned)g.C, 1, 1);
+                           int n = 0;
+                           r = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+                           *v = n > 0 ? n : 1;
+                           return r;
+                         });
+  if (e != cudaSuccess) return e;
   const int ncl = min(max_clusters, p.nunits);
   cfg.gridDim = dim3((unsigned)(ncl * g.C), 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, p);
@@ -2197,14 +2236,10 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
     int chunk = (V + G - 1) / G;
     chunk = (chunk + PV - 1) / PV * PV;
     const long long nitems = (long long)rows * G;
-    static int gblocks = 0;
-    if (!gblocks) {
-      int dev = 0, sms = 0, per = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, greedy_kernel<__nv_bfloat16>, NT, 0);
-      gblocks = max(1, sms * max(1, per));
-    }
+    int gblocks = 0;
+    if (resident_grid(reinterpret_cast<const void*>(greedy_kernel<__nv_bfloat16>), NT, 0, &gblocks) !=
+        cudaSuccess)
+      return SV_ERR_CUDA;
     const unsigned grid = (unsigned)(nitems < (long long)gblocks ? nitems : (long long)gblocks);
     if (dtype == SV_BF16)
       greedy_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(p, G, chunk, (int)nitems, p.ws_best, p.ws_rflag, p.ws_rcnt);
@@ -2214,17 +2249,8 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
     p.greedy_split = 1;
     if (p.greedy_only) return SV_OK;
     if (p.fast_split) {
-      static int kblocks = 0;
-      if (!kblocks) {
-        int dev = 0, sms = 0, per = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (cudaFuncSetAttribute(keyhist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)KH_SMEM) != cudaSuccess)
-          return SV_ERR_CUDA;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, keyhist_kernel, KT, KH_SMEM);
-        kblocks = max(1, sms * max(1, per));
-      }
+      int kblocks = 0;
+      if (keyhist_grid(keyhist_kernel, &kblocks) != cudaSuccess) return SV_ERR_CUDA;
       const int kitems = B * (2 * K + 1);
       const int kgrid = kitems < kblocks ? kitems : kblocks;
       // starts while greedy_kernel runs (it reads nothing greedy_kernel writes, and
@@ -2295,7 +2321,17 @@ sv_status spec_truncated_probs(const void* logits, sv_dtype dtype, int R, int V,
   p.nunits = R;
   p.bulk_ok = ((V * es) % 16 == 0) && aligned(logits, 16);
   p.out_probs = out_probs;
-  return do_launch(MODE_PROBS, dtype, p, g, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // bf16 rows, 16-byte aligned, at least 16 rows: the per-row code of the sampled
+  // verify path serves every row it can; the cluster kernel takes the rows it marks
+  p.fast_split = (dtype == SV_BF16 && p.bulk_ok && R >= 16) ? 1 : 0;
+  if (p.fast_split) {
+    int grid = 0;
+    if (keyhist_grid(keyhist_probs_kernel, &grid) != cudaSuccess) return SV_ERR_CUDA;
+    keyhist_probs_kernel<<<R < grid ? R : grid, KT, KH_SMEM, st>>>(p, R);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  }
+  return do_launch(MODE_PROBS, dtype, p, g, st);
 }
 
 sv_status spec_sample(const void* logits, sv_dtype dtype, int B, int K, int V,
@@ -2327,17 +2363,8 @@ sv_status spec_sample(const void* logits, sv_dtype dtype, int B, int K, int V,
   // every row it can; the cluster kernel takes the rows it marks
   p.fast_split = (dtype == SV_BF16 && p.bulk_ok && (long long)B * K >= 16) ? 1 : 0;
   if (p.fast_split) {
-    static int sblocks = 0;
-    if (!sblocks) {
-      int dev = 0, sms = 0, per = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (cudaFuncSetAttribute(keyhist_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)KH_SMEM) != cudaSuccess)
-        return SV_ERR_CUDA;
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, keyhist_sample_kernel, KT, KH_SMEM);
-      sblocks = max(1, sms * max(1, per));
-    }
+    int sblocks = 0;
+    if (keyhist_grid(keyhist_sample_kernel, &sblocks) != cudaSuccess) return SV_ERR_CUDA;
     const int items = B * K;
     keyhist_sample_kernel<<<items < sblocks ? items : sblocks, KT, KH_SMEM, st>>>(p, items);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
@@ -2354,6 +2381,39 @@ sv_status spec_philox_uniforms(uint64_t philox_seed, uint64_t philox_offset, int
   philox_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       philox_seed, philox_offset, B, K1, out);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Test hook for the per-device launch cache, no GPU needed: eight host threads
+// look up two kernels on two fake devices whose queries report different SM
+// counts (152 and 132, two CTAs per SM). out[0..3] = grids of (device 0, kernel
+// A), (device 1, A), (device 0, B), (device 1, B); out[4] = cache entries (4);
+// out[5] = 1 if every thread saw the same values. Returns 0.
+int sv_test_launch_cache(int* out) {
+  LaunchCache cache;
+  static const char fa = 0, fb = 0;
+  const void* fns[2] = {&fa, &fb};
+  int seen[8][4];
+  std::vector<std::thread> th;
+  for (int t = 0; t < 8; ++t)
+    th.emplace_back([&, t]() {
+      for (int r = 0; r < 4; ++r) {
+        const int j = (r + t) & 3, dev = j & 1, f = j >> 1;
+        int v = 0;
+        cache.get(dev, fns[f], 1024, 512, &v, [&](int* q) {
+          *q = (dev == 0 ? 152 : 132) * 2 + f;
+          return cudaSuccess;
+        });
+        seen[t][j] = v;
+      }
+    });
+  for (auto& x : th) x.join();
+  for (int j = 0; j < 4; ++j) out[j] = seen[0][j];
+  out[4] = (int)cache.size();
+  int same = 1;
+  for (int t = 1; t < 8; ++t)
+    for (int j = 0; j < 4; ++j) same &= seen[t][j] == seen[0][j];
+  out[5] = same;
+  return 0;
 }
 
 const char* sv_status_string(sv_status status) {
@@ -2391,6 +2451,10 @@ unsigned long long kh_heavy_count(void) {
 int kf_trace_copy(unsigned long long* host, size_t n) {
   if (n > 1024 * 8) n = 1024 * 8;
   return cudaMemcpyFromSymbol(host, g_kftrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
+}
+int kc_trace_copy(unsigned long long* host, size_t n) {
+  if (n > 4096 * 8) n = 4096 * 8;
+  return cudaMemcpyFromSymbol(host, g_kctrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
 }
 int kh_trace_copy(unsigned long long* host, size_t n) {
   if (n > 4096 * 8) n = 4096 * 8;

@@ -43,7 +43,18 @@ extern "C" sv_status spec_verify_noalloc(const void* target_logits, const void* 
   if (spec_verify_workspace_bytes(B, K) > SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_SCRATCH;
   void* scratch = scratch_on_current_device();
   if (!scratch) return SV_ERR_CUDA;
-  return spec_verify(target_logits, draft_logits, dtype, draft_tokens, temperature, top_k,
-                     top_p, philox_seed, philox_offset, B, K, V, out_tokens, out_n_accepted,
-                     scratch, SV_NOALLOC_SCRATCH_BYTES, stream);
+  const sv_status s =
+      spec_verify(target_logits, draft_logits, dtype, draft_tokens, temperature, top_k, top_p,
+                  philox_seed, philox_offset, B, K, V, out_tokens, out_n_accepted, scratch,
+                  SV_NOALLOC_SCRATCH_BYTES, stream);
+  if (s != SV_OK) {
+    // A failed launch can leave kernels queued before it (greedy_kernel writes its
+    // per-row slots first) with the scratch not zeroed again. A caller workspace can
+    // be cleared by its owner; this one is private, so clear the part the call could
+    // have used, in stream order after whatever was queued (no allocation).
+    if (cudaMemsetAsync(scratch, 0, spec_verify_workspace_bytes(B, K),
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
+  return s;
 }

@@ -105,3 +105,18 @@ def test_lm_head_entry_points_validate_before_launching():
     assert vh(d=65) == 2 and vh(dd=100) == 2
     assert vh(z=A + 4) == 6 and vh(ht=A + 8) == 6
     assert vh(wsb=8) == 4
+
+
+def test_launch_cache_is_per_device_and_thread_safe():
+    # Grid sizes and kernel attributes are cached per (device, kernel, shared memory):
+    # a process driving two GPUs must not reuse the first GPU's SM count on the
+    # second. The hook runs the library's cache with two fake devices (152 and 132
+    # SMs, two CTAs per SM) from eight host threads, without a GPU.
+    lib = sv.load()
+    lib.sv_test_launch_cache.argtypes = [ctypes.c_void_p]
+    lib.sv_test_launch_cache.restype = ctypes.c_int
+    out = (ctypes.c_int * 6)()
+    assert lib.sv_test_launch_cache(ctypes.cast(out, ctypes.c_void_p)) == 0
+    assert list(out[:4]) == [152 * 2, 132 * 2, 152 * 2 + 1, 132 * 2 + 1]
+    assert out[4] == 4            # one entry per (device, kernel)
+    assert out[5] == 1            # every thread saw the same values

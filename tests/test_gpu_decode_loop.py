@@ -3,13 +3,15 @@
 The step keeps its Philox offset in device memory and hands each sequence's
 last emitted token to the next step. Eager calls and a CUDA graph captured once
 and replayed must give bit-identical results to spec_verify called with
-offsets base, base + 1, ... on the same inputs."""
+offsets base, base + 1, ... on the same inputs, and agree with the float64 oracle
+at those offsets (tokens and n exact except on boundary draws)."""
 import pytest
 import torch
 
 import speculative_decoding_verification_30_gb300 as sv
 from speculative_decoding_verification_30_gb300.workloads import (WORKLOADS, draft_tokens_by_rank,
                                                                    make_batch)
+from tests.parity_util import compare, oracle_verify
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -39,6 +41,10 @@ def test_eager_steps_match_spec_verify_and_hand_off(name, B):
         sv.spec_verify_step(tg, dr, d, T, k, P, 5, off, out, n, ws, nxt, slen)
         torch.cuda.synchronize()
         assert torch.equal(out.cpu(), ref_tok.cpu()) and torch.equal(n.cpu(), ref_n.cpu())
+        # and against the float64 oracle at the offset the step read from device memory
+        res = oracle_verify(tg, None if name == "greedy" else dr, d, T, k, P, 5, base + step)
+        rep = compare(out.cpu(), n.cpu(), res, T)
+        assert not rep.bad_mismatches, (step, rep.bad_mismatches[:3])
         rn = ref_n.cpu()
         last = torch.tensor([int(ref_tok[b, rn[b]]) if rn[b] >= 0 else -1 for b in range(B)],
                             dtype=torch.int32)
@@ -81,6 +87,10 @@ def test_a_captured_step_replays_bit_exactly(name, B):
         torch.cuda.synchronize()
         assert torch.equal(out.cpu(), ref_tok.cpu()), step
         assert torch.equal(n.cpu(), ref_n.cpu()), step
+        tg, dr, d, T, k, P = fresh
+        res = oracle_verify(tg, None if name == "greedy" else dr, d, T, k, P, 3, base + step)
+        rep = compare(out.cpu(), n.cpu(), res, T)
+        assert not rep.bad_mismatches, (step, rep.bad_mismatches[:3])
         rn = ref_n.cpu()
         total += torch.where(rn >= 0, rn + 1, torch.zeros_like(rn))
     assert int(off.item()) == base + 4

@@ -51,7 +51,29 @@ def test_philox_stream_is_bit_exact():
 
 
 # ------------------------------------------------------- truncated probs
+def _ambiguous(z, T, k, P):
+    """Tokens that may sit on either side of the nucleus cut: those whose exclusive
+    renormalised mass (oracle, float64) lies within 1e-6 of top_p. Elsewhere the
+    kernel's kept set must equal the oracle's."""
+    if P >= 1.0:
+        return set()
+    V = z.shape[0]
+    order = sampler.descending_order(z)
+    kk = k if 0 < k < V else V
+    top = order[:kk]
+    e = np.exp((z[top] - z[order[0]]) / T)
+    w = e / e.sum()
+    excl = np.concatenate(([0.0], np.cumsum(w)[:-1]))
+    return set(int(top[j]) for j in np.nonzero(np.abs(excl - P) < 1e-6)[0])
+
+
 def _probs_case(rows, T, k, P):
+    """Worst |p_gpu - p_ref| over the rows and the number of cut-near rows.
+
+    p_ref is the oracle's float64 distribution on the kernel's kept set. That set
+    must equal the oracle's kept set except for tokens whose exclusive mass lies
+    within 1e-6 of top_p (where float64 and the kernel's exact fixed-point sums may
+    place the cut on either side of one token); every other token is compared."""
     R = rows.shape[0]
     Tt = torch.full((R,), T) if np.isscalar(T) else T
     kt = torch.full((R,), k, dtype=torch.int32) if np.isscalar(k) else k
@@ -59,32 +81,45 @@ def _probs_case(rows, T, k, P):
     got = sv.spec_truncated_probs(rows.to(DEV).contiguous(), Tt.float().to(DEV),
                                   kt.to(DEV), Pt.float().to(DEV)).cpu().double().numpy()
     z = f64(rows)
-    worst, cut_boundary = 0.0, 0
+    worst, cut_near = 0.0, 0
     for r in range(R):
-        t = sampler.truncate(z[r], float(Tt[r]), int(kt[r]), float(Pt[r]))
-        if t.topp_margin < 1e-6:
-            cut_boundary += 1
-            continue
-        # weights below 2^-S of the maximum are zero in the kernel's fixed point
-        kept = set(t.kept.tolist())
-        assert set(np.nonzero(got[r])[0]) <= kept, r
-        assert set(np.nonzero(t.probs > 1e-12)[0]) <= set(np.nonzero(got[r])[0]), r
-        worst = max(worst, float(np.max(np.abs(got[r] - t.probs))))
-    return worst, cut_boundary
+        Tr, kr, Pr = float(Tt[r]), int(kt[r]), float(Pt[r])
+        t = sampler.truncate(z[r], Tr, kr, Pr)
+        amb = _ambiguous(z[r], Tr, kr, Pr) if Tr > 0 else set()
+        cut_near += int(bool(amb))
+        kept_o = set(t.kept.tolist())
+        kept_g = set(np.nonzero(got[r])[0].tolist())
+        # weights below 2^-44 of the maximum are zero in the kernel's fixed point
+        sig_o = set(np.nonzero(t.probs > 1e-12)[0].tolist())
+        assert kept_g <= kept_o | amb, (r, sorted(kept_g - kept_o)[:5])
+        assert sig_o <= kept_g | amb, (r, sorted(sig_o - kept_g)[:5])
+        if Tr > 0:
+            ref_set = np.array(sorted(kept_g | (kept_o - amb)))
+            e = np.exp((z[r][ref_set] - z[r].max()) / Tr)
+            ref = np.zeros_like(got[r])
+            ref[ref_set] = e / e.sum()
+        else:
+            ref = t.probs
+        worst = max(worst, float(np.max(np.abs(got[r] - ref))))
+    return worst, cut_near
 
 
-@pytest.mark.parametrize("name", ["tiny", "mtp_decode", "nucleus_batch", "mixed"])
-def test_truncated_probs_match_oracle(name):
+@pytest.mark.parametrize("name,B", [("tiny", 4), ("mtp_decode", 16), ("nucleus_batch", 4),
+                                    ("mixed", 4)])
+@pytest.mark.parametrize("side", ["target", "draft"])
+def test_truncated_probs_match_oracle(name, B, side):
+    # bf16 batches of at least 16 rows run the per-row code of the sampled verify path
+    # (the key-histogram kernel); fp32 and smaller batches the cluster kernel
     w = WORKLOADS[name]
-    b = make_batch(w, 0, B=4)
-    rows = b.target.reshape(-1, w.V)
-    per = w.K + 1
+    b = make_batch(w, 0, B=B)
+    rows = (b.target if side == "target" else b.draft).reshape(-1, w.V)
+    per = w.K + 1 if side == "target" else w.K
     T = b.temperature.repeat_interleave(per)
     k = b.top_k.repeat_interleave(per)
     P = b.top_p.repeat_interleave(per)
-    worst, cut_b = _probs_case(rows, T, k, P)
+    worst, cut_near = _probs_case(rows, T, k, P)
+    print(name, side, "rows", rows.shape[0], "worst", worst, "cut-near rows", cut_near)
     assert worst < PROB_TOL, worst
-    assert cut_b == 0
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -189,8 +224,6 @@ def test_repeated_calls_are_deterministic_and_reuse_the_workspace():
     for o, n in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(n, outs[0][1])
     assert int(ws.buf.count_nonzero()) == 0       # the call leaves the workspace zeroed
-    o2, _ = sv.spec_verify(tgt, drf, dtok, T, k, P, seed=9, offset=5, workspace=ws)
-    assert not torch.equal(o2, outs[0][0]) or True
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -265,23 +298,30 @@ def test_draft_sampler_matches_oracle(name):
             _, v = uniforms(77, 8, s, i)
             tok, margin = sampler.sample_row(z[s, i], float(b.temperature[s]), int(b.top_k[s]),
                                              float(b.top_p[s]), v)
-            t = sampler.truncate(z[s, i], float(b.temperature[s]), int(b.top_k[s]),
-                                 float(b.top_p[s]))
-            if got[s, i] != tok and min(margin, t.topp_margin) >= 1e-6:
+            # only a sampling uniform within 1e-6 of a CDF boundary excuses a difference
+            if got[s, i] != tok and margin >= 1e-6:
                 bad += 1
     assert bad == 0
 
 
 # --------------------------------------------------- distribution (GPU)
-def test_gpu_output_distribution_is_the_truncated_target():
-    # Monte Carlo over Philox offsets: the first emitted token ~ p_0 (3-sigma per token)
-    V, K, N = 8, 2, 20000
-    g = torch.Generator().manual_seed(5)
-    tgt = torch.randn(1, K + 1, V, generator=g) * 1.5
-    drf = 0.5 * tgt[:, :K] + torch.randn(1, K, V, generator=g)
+@pytest.mark.parametrize("dtype,V", [(torch.float32, 8), (torch.bfloat16, 64)])
+def test_gpu_output_distribution_is_the_truncated_target(dtype, V):
+    # Monte Carlo over the sequences of one call (each with its own Philox
+    # counter): the first emitted token is distributed as p_0, the truncated target
+    # ("MTPLX", section 3.3: the verifier is exact). fp32 rows run the cluster
+    # kernel; bf16 rows of a batch this size run the key-histogram kernel.
+    # Marginals within 3 sigma, read for many tokens at once: with ~30 kept tokens
+    # one of them lies beyond 3 sigma by chance in ~8% of runs, so at most one may,
+    # none beyond 4 sigma; and a chi-square test over all kept tokens.
+    from scipy.stats import chi2
+    K, N = 2, 20000
+    g = torch.Generator().manual_seed(5 + V)
+    tgt = (torch.randn(1, K + 1, V, generator=g) * 1.5).to(dtype)
+    drf = (0.5 * tgt[:, :K].float() + torch.randn(1, K, V, generator=g)).to(dtype)
     T, k, P = 1.0, 0, 0.9
-    q = [sampler.truncate(drf[0, i].double().numpy(), T, k, P).probs for i in range(K)]
-    p0 = sampler.truncate(tgt[0, 0].double().numpy(), T, k, P).probs
+    q = [sampler.truncate(f64(drf[0, i]), T, k, P).probs for i in range(K)]
+    p0 = sampler.truncate(f64(tgt[0, 0]), T, k, P).probs
     rng = np.random.default_rng(0)
     dt = torch.tensor(np.stack([rng.choice(V, size=N, p=q[i] / q[i].sum()) for i in range(K)], 1),
                       dtype=torch.int32)
@@ -291,9 +331,18 @@ def test_gpu_output_distribution_is_the_truncated_target():
                             torch.zeros(N, dtype=torch.int32, device=DEV),
                             torch.full((N,), P, device=DEV), seed=11, offset=0)
     first = out[:, 0].cpu().numpy()
-    freq = np.bincount(first, minlength=V) / N
-    sigma = np.sqrt(p0 * (1 - p0) / N) + 1e-12
-    assert np.all(np.abs(freq - p0) <= 3.5 * sigma + 1e-4), (freq, p0)
+    assert (first >= 0).all()
+    cnt = np.bincount(first, minlength=V)
+    assert cnt[p0 == 0].sum() == 0                     # never a token outside the nucleus
+    freq = cnt / N
+    sigma = np.sqrt(p0 * (1 - p0) / N)
+    z = np.abs(freq - p0) / np.maximum(sigma, 1e-300)
+    print(dtype, "kept tokens", int((p0 > 0).sum()), "beyond 3 sigma", int((z > 3).sum()),
+          "max sigma", float(z[p0 > 0].max()))
+    assert int((z > 3).sum()) <= 1 and np.all(z <= 4), (freq, p0)
+    kept = p0 > 0
+    stat = float(np.sum((cnt[kept] - N * p0[kept]) ** 2 / (N * p0[kept])))
+    assert chi2.sf(stat, int(kept.sum()) - 1) > 1e-3, stat
     acc = (n.cpu().numpy() >= 1).mean()
     expect = np.minimum(p0, q[0]).sum()
-    assert abs(acc - expect) < 3.5 * math.sqrt(expect * (1 - expect) / N)
+    assert abs(acc - expect) < 3 * math.sqrt(expect * (1 - expect) / N)

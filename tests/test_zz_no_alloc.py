@@ -48,3 +48,23 @@ def test_noalloc_rejects_batches_beyond_the_scratch():
                torch.ones(B, device=DEV))
     with pytest.raises(sv.SpecVerifyError, match="status 7"):
         sv.spec_verify_noalloc(tgt, None, dtok, T, k, P, seed=0, offset=0)
+
+
+def test_noalloc_after_a_rejected_call_still_matches():
+    # a call rejected before launching (here an unaligned pointer, status 6) must
+    # leave the shared scratch usable: the next call equals the workspace entry point
+    name, B = "nucleus_batch", 6
+    tgt, drf, dtok, T, k, P = _inputs(name, 5, B)
+    lib = sv.load()
+    K, V = WORKLOADS[name].K, WORKLOADS[name].V
+    out = torch.empty(B, K + 1, dtype=torch.int32, device=DEV)
+    n = torch.empty(B, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = lib.spec_verify_noalloc(tgt.data_ptr(), drf.data_ptr(), sv.SV_BF16, dtok.data_ptr(),
+                                 T.data_ptr() + 1, k.data_ptr(), P.data_ptr(), 3, 4, B, K, V,
+                                 out.data_ptr(), n.data_ptr(), stream)
+    assert st == 6
+    ref_tok, ref_n = sv.spec_verify(tgt, drf, dtok, T, k, P, seed=3, offset=4)
+    got_tok, got_n = sv.spec_verify_noalloc(tgt, drf, dtok, T, k, P, seed=3, offset=4)
+    torch.cuda.synchronize()
+    assert torch.equal(ref_n.cpu(), got_n.cpu()) and torch.equal(ref_tok.cpu(), got_tok.cpu())
