@@ -9,9 +9,10 @@
  * projection with token selection was tried there. The verify step that consumes
  * the rows is spec_verify (include/spec_verify.h).
  *
- * Status: these entry points compile for sm_103a. Their GEMM kernel (tcgen05.mma
- * with TMA-staged operands and a TMEM accumulator) has not yet run on a GPU, and
- * no test calls it; only the argument checks below are exercised.
+ * The GEMM kernel runs on the 5th-generation tensor cores: tcgen05.mma with
+ * TMA-staged operands (128-byte swizzle) and a TMEM accumulator. Its logits are
+ * checked against the float64 oracle within the fp32 accumulation bound, and the
+ * verify step fed from it against the oracle's verify on those logits.
  */
 #ifndef SPEC_LM_HEAD_H
 #define SPEC_LM_HEAD_H
@@ -28,8 +29,9 @@ extern "C" {
  *           16-byte aligned
  *   logits  [M][N] fp32, row-major, device, caller-owned, 4-byte aligned
  *   flag    [1] int32, device, caller-owned: set to 1 when a pipeline wait of the
- *           kernel timed out (the logits are then undefined); never cleared here
- * Limits: 1 <= M <= 8,388,480 (65,535 row tiles of 128), 1 <= N <= 2^31 - 1,
+ *           kernel timed out (the logits are then undefined); never cleared here.
+ *           The caller zeroes it before the call and checks it afterwards.
+ * Limits: 1 <= M <= 2^31 - 129, 1 <= N <= 16,776,960 (65,535 column tiles of 256),
  * d a positive multiple of 64 and at most 65,536.
  * Every bf16 product is exact in fp32, so each logit lies within
  * gamma_(d-1) * sum_j |hidden_j * weight_vj| of the exact dot product
@@ -49,7 +51,9 @@ sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int
  *   logits_scratch [B][2K+1][V] fp32, device, caller-owned, 16-byte aligned: the
  *                 target rows [B][K+1][V] first, then the draft rows [B][K][V];
  *                 they hold the computed logits when the call's work is done.
- *   flag          as in spec_lm_head_logits (set when either GEMM timed out).
+ *   flag          as in spec_lm_head_logits (set when either GEMM timed out). When
+ *                 it is set, the verify step has run on undefined logits: its
+ *                 out_tokens and out_n_accepted are not valid and must be dropped.
  * The two GEMMs run first (spec_lm_head_logits), then spec_verify with SV_F32 on
  * the scratch rows. All other arguments and results are those of spec_verify.
  * Every argument is checked before anything is launched: SV_ERR_NULL,

@@ -44,13 +44,6 @@ constexpr int KH_LCAP = 1024;                             // window candidates p
 constexpr int KH_KCAP = 256;                              // kept-token list per target row (workspace)
 constexpr uint32_t KH_NOLIST = 0xFFFFFFFFu;
 constexpr float KH_LIST_BITS = 12.0f;                     // listed: weight >= 2^-12 of the maximum
-// Sparse rows: logits with weight below 2^-KH_WS of the first wave's maximum are
-// summed (one exp2 each) instead of counted; a row is sparse when at most one in
-// KH_SPARSE_DIV of its first-wave vectors holds a logit above that band edge.
-constexpr float KH_WS = 16.0f;
-constexpr int KH_SPARSE_DIV = 8;
-constexpr int KH_QCAP = 64;                               // per-warp queue of head vectors (ring)
-constexpr uint32_t KH_REDO = 4u;                          // sparse row whose cut lies below the band
 
 #ifdef SV_TRACE
 // Phase timestamps per row item (trace builds): 0 fetched, 1 streamed, 2 swept,
@@ -71,17 +64,7 @@ __device__ unsigned long long g_kftrace[1024 * 8];
   do {                                                                     \
     if (threadIdx.x == 0 && (b) >= 0 && (b) < 1024) g_kftrace[(b) * 8 + (k)] = (v);   \
   } while (0)
-// kh_cut sub-phases per row item: 0 start, 1 scanned, 2 shares summed, 3 tail
-// added, 4 top-k walked, 5 top-p walked.
-__device__ unsigned long long g_kctrace[4096 * 8];
-#define KC_MARK(item, k)                                                   \
-  do {                                                                     \
-    if (threadIdx.x == 0 && (item) >= 0 && (item) < 4096) g_kctrace[(item) * 8 + (k)] = global_timer_ns(); \
-  } while (0)
 #else
-#define KC_MARK(item, k) \
-  do {                   \
-  } while (0)
 #define KF_MARK(b, k) \
   do {                \
   } while (0)
@@ -183,13 +166,6 @@ struct KhShared {
   uint32_t flag[16];
   float pz[16], qz[16];                // p(d), and q(d) if d is kept
   uint32_t ku[16];
-  // streaming mode of the current row (chosen from the first load wave)
-  uint32_t sparse;                     // 1: only logits >= theta are counted, the rest summed
-  uint32_t nhead;                      // first wave: vectors holding a logit >= theta
-  float R, theta;                      // first-wave maximum; band edge R - KH_WS / c
-  // occupied span of the histogram (finite bins), words [wlo, whi]; -inf count
-  uint32_t wlo, whi, ninf;
-  int span_n;                          // words per thread over the span
 };
 
 // Exclusive sums of a count and a mass in descending thread order (thread KT-1
@@ -319,193 +295,63 @@ __device__ __forceinline__ void kh_collect(const uint4& w, int v, __nv_bfloat162
   }
 }
 
-// Packed maximum of the 8 logits of one vector (NaN ignored).
-__device__ __forceinline__ __nv_bfloat162 kh_vmax(const uint4& w) {
-  __nv_bfloat162 a, b, c, d;
-  memcpy(&a, &w.x, 4);
-  memcpy(&b, &w.y, 4);
-  memcpy(&c, &w.z, 4);
-  memcpy(&d, &w.w, 4);
-  return __hmax2(__hmax2(a, b), __hmax2(c, d));
-}
-__device__ __forceinline__ float kh_f2max(__nv_bfloat162 v) {
-  return fmaxf(__low2float(v), __high2float(v));
-}
-
-// Logits a sparse row does not count: per thread, the sum of their weights
-// 2^((z - R) * c) relative to the first wave's maximum R (each below 2^-KH_WS, so
-// no overflow; NaN propagates into the sum), and how many there were.
-struct KhTail {
-  float sum;
-  uint32_t n;
-};
-
-// 2^((z - R) c) summed over the 8 logits of w, nRc = -(R c). Two partial sums for
-// instruction-level parallelism; the order is fixed, so the result is a pure
-// function of the vector.
-__device__ __forceinline__ float kh_esum8(const uint4& w, float c, float nRc) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    s0 += ex2_approx(fmaf(__uint_as_float(ws[k] << 16), c, nRc));
-    s1 += ex2_approx(fmaf(__uint_as_float(ws[k] & 0xFFFF0000u), c, nRc));
-  }
-  return s0 + s1;
-}
-
-// One head vector of a sparse row (a vector holding a logit >= theta): logits at or
-// above theta are counted in the histogram, the others go to the thread's tail;
-// target rows also list their candidates.
+// Streams one row (nv 16-byte vectors) into the histogram; returns this
+// thread's maximum (NaN is ignored here: NaN bins are checked afterwards).
+// COLLECT: also lists the candidates of kh_collect (threshold seeded by the
+// block maximum of the first load wave).
 template <bool COLLECT>
-__device__ __forceinline__ void kh_head8(uint32_t* hist, const uint4& w, int v, float theta, float c,
-                                         float nRc, float D, float* ctheta, KhShared& S,
-                                         unsigned long long* list, KhTail* t) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const uint32_t bits = (e & 1) ? ws[e >> 1] >> 16 : ws[e >> 1] & 0xFFFFu;
-    const float z = __uint_as_float(bits << 16);
-    if (z >= theta) {
-      const uint32_t i = kh_bin(bits);
-      atomicAdd(&hist[i >> 1], 1u << ((i & 1u) << 4));
-    } else {
-      t->sum += ex2_approx(fmaf(z, c, nRc));      // -inf adds 0, NaN poisons the sum
-      t->n += 1u;
-    }
-  }
-  if (COLLECT) kh_collect(w, v, kh_vmax(w), D, ctheta, S, list);
-}
-
-__device__ __forceinline__ unsigned long long* kh_blk0();
-
-// Streams one row (nv 16-byte vectors); returns this thread's maximum (NaN is
-// ignored here: NaN is caught by the histogram's NaN bins or the tail sum).
-//
-// The first load wave (KH_PF vectors per thread) decides the row's mode. R = its
-// block maximum, theta = R - KH_WS / c. If at most one in KH_SPARSE_DIV of those
-// vectors holds a logit >= theta, the row is sparse: a vector whose logits all lie
-// below theta is summed into the thread's tail (one exp2 per logit, no atomics);
-// the few head vectors are queued per warp (their indices, in a ring in the block
-// scratch) and counted 32 at a time, one vector per lane, logit by logit. The
-// histogram then holds exactly the logits >= theta. Otherwise (or when
-// allow_sparse is false) every logit is counted. COLLECT: target rows also list
-// the candidates of kh_collect (threshold seeded by R). FIRST: the row's first
-// pass (resets the candidate list). L2: loads from L2 (a repeated pass).
-template <bool COLLECT, bool L2>
-__device__ __noinline__ float kh_stream(const uint4* src, int nv, uint32_t* hist, float c, float D,
-                                        KhShared& S, unsigned long long* list, bool allow_sparse,
-                                        bool first, KhTail* tl) {
-  const int tid = threadIdx.x, l = lane_id(), w = warp_id();
-  // double-buffered waves of KH_PF vectors per thread: the next wave's loads are
-  // issued before the current wave is processed, so they stay in flight meanwhile
-  uint4 cur[KH_PF], nxt[KH_PF];
-  const uint4 NEG8 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-  const int b0 = tid - l;                              // warp-uniform base of this warp's vectors
+__device__ __forceinline__ float kh_stream(const uint4* src, int nv, uint32_t* hist, float D,
+                                           KhShared& S, unsigned long long* list) {
+  const int tid = threadIdx.x;
+  uint4 buf[KH_PF];
+  const uint32_t NEG2 = 0xFF80FF80u;
 #pragma unroll
   for (int p = 0; p < KH_PF; ++p) {
     const int q = tid + p * KT;
-    cur[p] = q < nv ? (L2 ? kh_ld_l2(src + q) : kh_ld(src + q)) : NEG8;
+    buf[p] = q < nv ? kh_ld(src + q) : make_uint4(NEG2, NEG2, NEG2, NEG2);
   }
   __nv_bfloat162 m2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0xFF80u),
                                          __ushort_as_bfloat16((unsigned short)0xFF80u));
-  // block maximum of the first wave
-  __nv_bfloat162 f2 = m2;
+  float theta = -INFINITY;
+  if (COLLECT) {
+    __nv_bfloat162 f2 = m2;
 #pragma unroll
-  for (int p = 0; p < KH_PF; ++p) f2 = __hmax2(f2, kh_vmax(cur[p]));
-  float fm = kh_f2max(f2);
+    for (int p = 0; p < KH_PF; ++p) {
+      __nv_bfloat162 a, b, c, d;
+      memcpy(&a, &buf[p].x, 4);
+      memcpy(&b, &buf[p].y, 4);
+      memcpy(&c, &buf[p].z, 4);
+      memcpy(&d, &buf[p].w, 4);
+      f2 = __hmax2(f2, __hmax2(__hmax2(a, b), __hmax2(c, d)));
+    }
+    float fm = fmaxf(__low2float(f2), __high2float(f2));
 #pragma unroll
-  for (int o = 16; o; o >>= 1) fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, o));
-  __syncthreads();                                     // S is free (previous row done)
-  if (tid == 0) {
-    S.cmax = okey(-INFINITY);
-    S.nhead = 0u;
-    if (first) {
+    for (int o = 16; o; o >>= 1) fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, o));
+    if (tid == 0) {
+      S.cmax = okey(-INFINITY);
       S.ccount = 0u;
       S.gcount = 0u;
     }
+    __syncthreads();
+    if (lane_id() == 0) atomicMax(&S.cmax, okey(fm));
+    __syncthreads();
+    theta = key_to_float(S.cmax) - D;
   }
-  __syncthreads();
-  if (l == 0) atomicMax(&S.cmax, okey(fm));
-  __syncthreads();
-  const float R = key_to_float(S.cmax);
-  const float theta = R - __fdiv_rn(KH_WS, c);
-  uint32_t nh = 0;
-#pragma unroll
-  for (int p = 0; p < KH_PF; ++p)
-    nh += (tid + p * KT < nv && kh_f2max(kh_vmax(cur[p])) >= theta) ? 1u : 0u;
-  nh = warp_sum(nh);
-  if (l == 0 && nh) atomicAdd(&S.nhead, nh);
-  __syncthreads();                                     // R read by all before S.cmax moves on
-  const int nfirst = min(nv, KH_PF * KT);
-  const bool sparse = allow_sparse && R > -INFINITY && R < INFINITY &&
-                      (int)S.nhead * KH_SPARSE_DIV <= nfirst;
-  if (tid == 0) {
-    S.sparse = sparse ? 1u : 0u;
-    S.R = R;
-    S.theta = theta;
-  }
-  float ctheta = R - D;                                // candidate threshold (COLLECT)
-  const float nRc = -(R * c);
-  KhTail t{0.0f, 0u};                                  // this thread's tail, in registers
-  uint32_t* ring = reinterpret_cast<uint32_t*>(kh_blk0()) + w * KH_QCAP;
-  uint32_t qh = 0, qt = 0;                             // ring head / tail (warp-uniform)
-  const uint32_t below = (1u << l) - 1u;
-  for (int w0 = b0; w0 < nv; w0 += KH_PF * KT) {       // warp-uniform trip count
+  for (int q0 = tid; q0 < nv; q0 += KH_PF * KT) {
 #pragma unroll
     for (int p = 0; p < KH_PF; ++p) {
-      const int q = w0 + KH_PF * KT + l + p * KT;
-      nxt[p] = q < nv ? (L2 ? kh_ld_l2(src + q) : kh_ld(src + q)) : NEG8;
-    }
-    if (!sparse) {
-#pragma unroll
-      for (int p = 0; p < KH_PF; ++p) {
-        const int q = w0 + l + p * KT;
-        if (q < nv) {
-          const __nv_bfloat162 vm2 = kh_count8(hist, cur[p]);
-          m2 = __hmax2(m2, vm2);
-          if (COLLECT) kh_collect(cur[p], q, vm2, D, &ctheta, S, list);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int p = 0; p < KH_PF; ++p) {
-        const int q = w0 + l + p * KT;
-        const bool valid = q < nv;                     // else cur[p] holds -inf
-        const __nv_bfloat162 vm2 = kh_vmax(cur[p]);
+      const int q = q0 + p * KT;
+      if (q < nv) {
+        const uint4 w = buf[p];
+        const int qn = q + KH_PF * KT;
+        if (qn < nv) buf[p] = kh_ld(src + qn);
+        const __nv_bfloat162 vm2 = kh_count8(hist, w);
         m2 = __hmax2(m2, vm2);
-        const bool head = valid && kh_f2max(vm2) >= theta;
-        const float s8 = kh_esum8(cur[p], c, nRc);
-        if (valid && !head) {
-          t.sum += s8;
-          t.n += 8u;
-        }
-        const uint32_t bal = __ballot_sync(0xffffffffu, head);
-        if (bal) {
-          if (head) ring[(qt + __popc(bal & below)) % KH_QCAP] = (uint32_t)q;
-          qt += __popc(bal);
-          if (qt - qh >= 32u) {
-            __syncwarp();
-            const int v = (int)ring[(qh + l) % KH_QCAP];
-            __syncwarp();
-            qh += 32u;
-            kh_head8<COLLECT>(hist, kh_ld_l2(src + v), v, theta, c, nRc, D, &ctheta, S, list, &t);
-          }
-        }
+        if (COLLECT) kh_collect(w, q, vm2, D, &theta, S, list);
       }
     }
-#pragma unroll
-    for (int p = 0; p < KH_PF; ++p) cur[p] = nxt[p];
   }
-  if (sparse) {
-    __syncwarp();
-    if ((uint32_t)l < qt - qh) {
-      const int v = (int)ring[(qh + l) % KH_QCAP];
-      kh_head8<COLLECT>(hist, kh_ld_l2(src + v), v, theta, c, nRc, D, &ctheta, S, list, &t);
-    }
-  }
-  *tl = t;
-  return kh_f2max(m2);
+  return fmaxf(__low2float(m2), __high2float(m2));
 }
 
 // 8-bit mask (token-id order) of the logits in w whose bf16 pattern is hb.
@@ -627,24 +473,21 @@ __device__ __forceinline__ unsigned long long kh_binw(int idx, float m, float c)
 
 constexpr int KH_DEFER = -2;       // idcut of a partial cut bin not yet split by id
 
-// Warp 0: walks the bins of thread t's words of the occupied span (words
-// [wlo + t*n, ...), n = S.span_n) in descending order from the running count acc /
-// mass M before them, and stops at the first bin where the count reaches k
-// (by_mass false) or the mass exceeds Y. Publishes the bin, its count and weight,
-// and the count and mass before it. The -inf bin is not counted (weight 0; its
-// tokens are counted apart).
+// Warp 0: walks the bins of thread range t (words [t*WPT, ...)) in descending
+// order from the running count acc / mass M before the range, and stops at the
+// first bin where the count reaches k (by_mass false) or the mass exceeds Y.
+// Publishes the bin, its count and weight, and the count and mass before it.
 __device__ __forceinline__ void kh_walk(const uint32_t* hist, int t, uint32_t acc,
                                         unsigned long long M, bool by_mass, uint32_t k,
                                         unsigned long long Y, float m, float c, KhShared& S) {
   const int l = lane_id();
-  const int w0 = (int)S.wlo + t * S.span_n, w1 = min(w0 + S.span_n, (int)S.whi + 1);
+  const int w0 = min(t * KH_WPT, KH_NW), w1 = min(w0 + KH_WPT, KH_NW);
   const int n = w1 - w0;
   for (int base = 0; base < n; base += 32) {
     const int pos = base + l;
     const int wd = w1 - 1 - pos;
     const uint32_t x = pos < n ? hist[wd] : 0u;
-    const uint32_t chi = 2 * wd + 1 == KH_NINF ? 0u : x >> 16;
-    const uint32_t clo = 2 * wd == KH_NINF ? 0u : x & 0xFFFFu;
+    const uint32_t chi = x >> 16, clo = x & 0xFFFFu;
     const unsigned long long Whi = chi ? kh_binw(2 * wd + 1, m, c) : 0ull;
     const unsigned long long Wlo = clo ? kh_binw(2 * wd, m, c) : 0ull;
     const uint32_t cw = chi + clo;
@@ -684,150 +527,103 @@ __device__ __forceinline__ void kh_walk(const uint32_t* hist, int t, uint32_t ac
   }
 }
 
-// Zeroes the histogram words the last kh_cut found occupied (all words when it
-// found a NaN or +inf bin, which lie outside the span).
-__device__ __forceinline__ void kh_clear(uint32_t* hist, const KhShared& S, bool all) {
-  if (all) {
-    for (int wd = threadIdx.x; wd < KH_NW; wd += KT) hist[wd] = 0u;
-  } else {
-    if (S.wlo != 0xFFFFFFFFu)
-      for (int wd = (int)S.wlo + threadIdx.x; wd <= (int)S.whi; wd += KT) hist[wd] = 0u;
-    if (threadIdx.x == 0) hist[KH_NINF >> 1] = 0u;
-  }
-}
-
-// Totals and cut of one streamed row, from the histogram (and, for a sparse row,
-// the threads' tails):
-//   1. the occupied span of finite bins is found by one scan of the histogram;
-//      NaN and +inf bins make the row a data error; the -inf bin is counted apart;
-//   2. each thread sums the counts and exact fixed-point masses of a contiguous
-//      share of the span (no atomics), block scans give counts and masses above
-//      every share;
-//   3. the tail of a sparse row is moved to the frame of the row maximum m and
-//      added to the normaliser and the count;
-//   4. warp 0 walks the share holding the k-th token (top-k), then the share
-//      holding the bin where the exclusive mass first exceeds Y = the largest
-//      integer below P * Z(L1) (top-p), as kh_walk describes.
-// Returns the row flags (KH_ERR, KH_BAIL, or KH_REDO when a sparse row's cut lies
-// below its band) and, in *ZL1 / *Ztot, the masses of L1 and of the whole row.
-__device__ __noinline__ uint32_t kh_cut(const uint32_t* hist, int V, float m, float c, int k,
-                                        float topP, KhTail tl, KhShared& S, unsigned long long* ZL1o,
-                                        unsigned long long* Ztoto, bool* anybad, bool* cut, int item) {
+// One row: histogram, maximum, normaliser, top-k / top-p cut and (target rows)
+// the id split of a partial cut bin; a draft row's split is left to the
+// sequence's finalizer, which needs it only for tokens on the cut value.
+// Leaves the histogram zeroed. The result is returned in every thread.
+__device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, int k, float topP,
+                                     bool target, uint32_t* hist, KhShared& S, uint32_t* glist,
+                                     int item) {
   const int tid = threadIdx.x, l = lane_id(), w = warp_id();
-  KC_MARK(item, 0);
-  if (tid == 0) {
-    S.wlo = 0xFFFFFFFFu;
-    S.whi = 0u;
-    S.ninf = 0u;
-  }
-  __syncthreads();
-  uint32_t lo = 0xFFFFFFFFu, hi = 0u, bad = 0u, ninf = 0u;
-  auto scan_word = [&](int wd, uint32_t x) {
-    const uint32_t clo = x & 0xFFFFu, chi = x >> 16;
-    const int i0 = 2 * wd;
-    bool fin = false;
-    if (clo) {
-      if (i0 < KH_NINF || i0 >= KH_PINF) bad = 1u;
-      else if (i0 == KH_NINF) ninf += clo;
-      else fin = true;
+  const int nv = V / 8;
+  const bool defer_tie = !target;
+  const uint4* src = reinterpret_cast<const uint4*>(row);
+  uint32_t* rcnt = reinterpret_cast<uint32_t*>(kh_blk0());      // per thread range
+  unsigned long long* rmass =
+      reinterpret_cast<unsigned long long*>(reinterpret_cast<unsigned char*>(kh_blk0()) + KT * 4);
+  unsigned long long* clist = kh_blk1();                         // candidates (id | bits << 32)
+  rcnt[tid] = 0u;
+  rmass[tid] = 0ull;
+  const float c = __fdiv_rn(KH_LOG2E, T);
+  const float D = __fdiv_rn(KH_LIST_BITS, c);                    // z >= m - D: weight >= 2^-12
+  float mt = target ? kh_stream<true>(src, nv, hist, D, S, clist)
+                    : kh_stream<false>(src, nv, hist, D, S, clist);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+  if (l == 0) S.fmax[w] = mt;
+  __syncthreads();                              // the histogram is complete
+  KH_MARK(item, 1);
+  float m = S.fmax[0];
+#pragma unroll
+  for (int i = 1; i < KWARP; ++i) m = fmaxf(m, S.fmax[i]);
+
+  // sweep, words interleaved over the threads (occupied bins cluster in a few
+  // value ranges): counts and fixed-point masses, added to the word's thread range
+  uint32_t bad = 0;
+  // a lane's words are summed locally and added to their thread range once
+  int rcur = -1;
+  uint32_t cacc = 0;
+  unsigned long long macc = 0;
+  auto flush = [&]() {
+    if (rcur >= 0 && cacc) {
+      atomicAdd(&rcnt[rcur], cacc);
+      if (macc) atomicAdd(&rmass[rcur], macc);
     }
-    if (chi) {
-      if (i0 + 1 < KH_NINF || i0 + 1 >= KH_PINF) bad = 1u;
-      else if (i0 + 1 == KH_NINF) ninf += chi;
-      else fin = true;
-    }
-    if (fin) {
-      lo = min(lo, (uint32_t)wd);
-      hi = max(hi, (uint32_t)wd);
-    }
+    cacc = 0;
+    macc = 0;
   };
+  auto sweep_word = [&](int wd, uint32_t x) {
+    const uint32_t chi = x >> 16, clo = x & 0xFFFFu;
+    const int i0 = 2 * wd;
+    if ((clo && (i0 < KH_NINF || i0 >= KH_PINF)) || (chi && (i0 + 1 < KH_NINF || i0 + 1 >= KH_PINF)))
+      bad = 1u;
+    const unsigned long long mw = (clo ? clo * kh_binw(i0, m, c) : 0ull) +
+                                  (chi ? chi * kh_binw(i0 + 1, m, c) : 0ull);
+    const int r = wd / KH_WPT;
+    if (r != rcur) {
+      flush();
+      rcur = r;
+    }
+    cacc += chi + clo;
+    macc += mw;
+  };
+  // four words per 16-byte load; the last word (an odd count) separately
   const uint4* h4 = reinterpret_cast<const uint4*>(hist);
   for (int v4 = tid; v4 < KH_NW / 4; v4 += KT) {
     const uint4 x = h4[v4];
     if ((x.x | x.y | x.z | x.w) == 0u) continue;
-    if (x.x) scan_word(4 * v4, x.x);
-    if (x.y) scan_word(4 * v4 + 1, x.y);
-    if (x.z) scan_word(4 * v4 + 2, x.z);
-    if (x.w) scan_word(4 * v4 + 3, x.w);
+    if (x.x) sweep_word(4 * v4, x.x);
+    if (x.y) sweep_word(4 * v4 + 1, x.y);
+    if (x.z) sweep_word(4 * v4 + 2, x.z);
+    if (x.w) sweep_word(4 * v4 + 3, x.w);
+    flush();
   }
   for (int wd = (KH_NW / 4) * 4 + tid; wd < KH_NW; wd += KT)
-    if (hist[wd]) scan_word(wd, hist[wd]);
-  lo = __reduce_min_sync(0xffffffffu, lo);
-  hi = __reduce_max_sync(0xffffffffu, hi);
-  ninf = __reduce_add_sync(0xffffffffu, ninf);
-  if (l == 0) {
-    if (lo != 0xFFFFFFFFu) {
-      atomicMin(&S.wlo, lo);
-      atomicMax(&S.whi, hi);
-    }
-    if (ninf) atomicAdd(&S.ninf, ninf);
-  }
-  // a sparse row's tail: NaN is a data error
-  const bool sparse = S.sparse != 0u;
-  if (sparse && !(tl.sum == tl.sum)) bad = 1u;
-  bad = (uint32_t)__syncthreads_or((int)bad);
-  KC_MARK(item, 1);
-  *anybad = bad != 0u;
-  const uint32_t wlo = S.wlo, whi = S.whi;
-  const int n = wlo != 0xFFFFFFFFu ? (int)((whi - wlo + KT) / KT) : 0;
-  uint32_t cnt = 0u;
-  unsigned long long mass = 0ull;
-  if (n && !bad) {
-    const int w0 = (int)wlo + tid * n, w1 = min(w0 + n, (int)whi + 1);
-    for (int wd = w0; wd < w1; ++wd) {
-      const uint32_t x = hist[wd];
-      if (!x) continue;
-      const uint32_t clo = 2 * wd == KH_NINF ? 0u : x & 0xFFFFu;
-      const uint32_t chi = 2 * wd + 1 == KH_NINF ? 0u : x >> 16;
-      cnt += clo + chi;
-      mass += (clo ? clo * kh_binw(2 * wd, m, c) : 0ull) + (chi ? chi * kh_binw(2 * wd + 1, m, c) : 0ull);
-    }
-  }
-  if (tid == 0) S.span_n = n;
-  uint32_t cab, ctot;
-  unsigned long long mab, Zhead;
-  kh_above2(cnt, mass, S, &cab, &ctot, &mab, &Zhead);      // barriers: S.span_n visible after
-  KC_MARK(item, 2);
-  // the tail of a sparse row in the frame of m (weights relative to R times 2^((R - m) c))
-  unsigned long long tfix = 0ull;
-  uint32_t tn = 0u;
-  if (sparse && !bad) {
-    tfix = fix_pow2(tl.sum * ex2_approx((S.R - m) * c), FIX);
-    tn = tl.n;
-  }
-  tfix = warp_sum(tfix);
-  tn = warp_sum(tn);
-  __syncthreads();
-  if (l == 0) {
-    S.s64b[w] = tfix;
-    S.s32[w] = tn;
-  }
-  __syncthreads();
-  unsigned long long Ttail = 0ull;
-  uint32_t Ntail = 0u;
-#pragma unroll
-  for (int i = 0; i < KWARP; ++i) {
-    Ttail += S.s64b[i];
-    Ntail += S.s32[i];
-  }
-  const unsigned long long Ztot = Zhead + Ttail;
-  KC_MARK(item, 3);
-  *Ztoto = Ztot;
-  *ZL1o = Ztot;
-  *cut = false;
-  uint32_t flags = 0u;
-  if (bad || !(m > -INFINITY)) return KH_ERR;
-  if (ctot + S.ninf + Ntail != (uint32_t)V) return KH_BAIL;
-  bool topk = k > 0 && k < V;
+    if (hist[wd]) sweep_word(wd, hist[wd]);
+  flush();
+  const int anyb = __syncthreads_or((int)bad);
+  const uint32_t cnt = rcnt[tid];
+  const unsigned long long mass = anyb ? 0ull : rmass[tid];
+  uint32_t ctot, cab;
+  unsigned long long Ztot, mab;
+  kh_above2(cnt, mass, S, &cab, &ctot, &mab, &Ztot);
+  KH_MARK(item, 2);
+
+  KhRow res;
+  res.m = m;
+  res.c = c;
+  res.zt = -INFINITY;
+  res.idcut = V;
+  res.invZ = 0.0f;
+  res.flags = 0u;
+  res.pad[0] = 0u;
+  res.pad[1] = KH_NOLIST;
+  if (anyb || !(m > -INFINITY)) res.flags = KH_ERR;
+  else if (ctot != (uint32_t)V) res.flags = KH_BAIL;
+  const bool topk = k > 0 && k < V;
   const bool topp = topP < 1.0f;
-  if (topk && (uint32_t)k > ctot) {
-    // fewer counted finite tokens than k: a sparse row's k-th token lies below its
-    // band; in a full histogram the rest are -inf (weight 0): top-k keeps all mass
-    if (sparse) return KH_REDO;
-    topk = false;
-  }
   unsigned long long ZL1 = Ztot;
-  if (topk) {
+  if (res.flags == 0u && topk) {
     // the bin holding the k-th token in (logit desc, id asc) order
     if (cab < (uint32_t)k && (uint32_t)k <= cab + cnt) {
       S.wq = tid;
@@ -840,12 +636,10 @@ __device__ __noinline__ uint32_t kh_cut(const uint32_t* hist, int V, float m, fl
     ZL1 = S.Mcut + (unsigned long long)(k - S.kq) * S.Wcut;
     if (!topp && tid == 0) S.cq = k - S.kq;   // tokens of the bin inside the top k
   }
-  KC_MARK(item, 4);
-  if (topp) {
+  if (res.flags == 0u && topp) {
     // the bin where the exclusive mass first exceeds Y = the largest integer
     // below P * Z(L1); tokens with exclusive mass <= Y are kept
     const unsigned long long Y = mass_threshold(topP, ZL1);
-    if (Y >= Zhead) return KH_REDO;            // only a sparse row's tail can hold the cut
     __syncthreads();
     if (mab <= Y && Y < mab + mass) {
       S.wq = tid;
@@ -860,71 +654,8 @@ __device__ __noinline__ uint32_t kh_cut(const uint32_t* hist, int V, float m, fl
     }
     __syncthreads();
   }
-  KC_MARK(item, 5);
-  *ZL1o = ZL1;
-  *cut = topk || topp;
-  return flags;
-}
-
-// One row: histogram (sparse rows: band plus summed tail), maximum, normaliser,
-// top-k / top-p cut and (target rows) the id split of a partial cut bin; a draft
-// row's split is left to the sequence's finalizer, which needs it only for tokens
-// on the cut value. A sparse row whose cut falls below its band is streamed again
-// (from L2) into the full histogram. Leaves the histogram zeroed. The result is
-// returned in every thread.
-__device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, int k, float topP,
-                                     bool target, uint32_t* hist, KhShared& S, uint32_t* glist,
-                                     int item) {
-  const int tid = threadIdx.x, l = lane_id(), w = warp_id();
-  const int nv = V / 8;
-  const bool defer_tie = !target;
-  const uint4* src = reinterpret_cast<const uint4*>(row);
-  unsigned long long* clist = kh_blk1();                         // candidates (id | bits << 32)
-  const float c = __fdiv_rn(KH_LOG2E, T);
-  const float D = __fdiv_rn(KH_LIST_BITS, c);                    // z >= m - D: weight >= 2^-12
-  KhTail tl{0.0f, 0u};
-  float mt = target ? kh_stream<true, false>(src, nv, hist, c, D, S, clist, true, true, &tl)
-                    : kh_stream<false, false>(src, nv, hist, c, D, S, clist, true, true, &tl);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-  if (l == 0) S.fmax[w] = mt;
-  __syncthreads();                              // the histogram is complete
-  KH_MARK(item, 1);
-  float m = S.fmax[0];
-#pragma unroll
-  for (int i = 1; i < KWARP; ++i) m = fmaxf(m, S.fmax[i]);
-
-  unsigned long long ZL1, Ztot;
-  bool anyb, cut;
-  uint32_t fl = kh_cut(hist, V, m, c, k, topP, tl, S, &ZL1, &Ztot, &anyb, &cut, item);
-  KH_MARK(item, 2);
-#ifdef SV_TRACE
-  if (tid == 0 && item >= 0 && item < 4096)
-    g_khtrace[item * 8 + 7] |= ((unsigned long long)S.sparse << 32) | ((unsigned long long)(fl == KH_REDO) << 33);
-#endif
-  if (fl == KH_REDO) {
-    // the cut lies in the summed tail: count the whole row (L2-resident by now)
-    kh_clear(hist, S, false);
-    __syncthreads();
-    tl.sum = 0.0f;
-    tl.n = 0u;
-    (void)kh_stream<false, true>(src, nv, hist, c, D, S, clist, false, false, &tl);
-    __syncthreads();
-    fl = kh_cut(hist, V, m, c, k, topP, tl, S, &ZL1, &Ztot, &anyb, &cut, item);
-  }
-
-  KhRow res;
-  res.m = m;
-  res.c = c;
-  res.zt = -INFINITY;
-  res.idcut = V;
-  res.invZ = 0.0f;
-  res.flags = fl;
-  res.pad[0] = 0u;
-  res.pad[1] = KH_NOLIST;
   // the histogram is not read again for this row
-  __syncthreads();
-  kh_clear(hist, S, anyb);
+  for (int wd = tid; wd < KH_NW; wd += KT) hist[wd] = 0u;
   KH_MARK(item, 3);
   if (res.flags != 0u) return res;
 
@@ -933,7 +664,7 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   // within D of the maximum and the list did not overflow
   const uint32_t ncand = target ? S.ccount : 0u;
   bool listed = false;
-  if (cut) {
+  if (topk || topp) {
     const int cbin = S.cbin, q = S.cq, ccnt = S.ccnt;
     Zk = S.Mcut + (unsigned long long)q * S.Wcut;
     // kept tokens: those before the cut bin plus the bin's quota

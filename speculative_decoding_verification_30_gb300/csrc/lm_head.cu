@@ -5,15 +5,14 @@
 // output projection that ends a decode step ("Apple Silikon İçin Cihaz Üstü
 // Çıkarımı Optimize Etme", perplexity.coolkeypoint.com, decode section).
 //
-// One CTA per 128 x 128 output tile. Both operands are K-major and staged by TMA
+// One CTA per 128 x 256 output tile. Both operands are K-major and staged by TMA
 // (128-byte swizzle, one 64-element K slice per stage) into a 4-stage ring; one
-// thread issues tcgen05.mma (M = 128, N = 128, K = 16) into a 128-column TMEM
+// thread issues tcgen05.mma (M = 128, N = 256, K = 16) into a 256-column TMEM
 // accumulator; the four warps read it back with tcgen05.ld (warp w owns TMEM lanes
 // 32w..32w+31, i.e. those output rows) and store fp32 rows. Every wait is bounded:
 // a timeout sets the caller's flag, the CTA lets its issued copies land and frees
 // its TMEM before it returns.
 //
-// Not yet run on a GPU: compiled for sm_103a, exercised only by the argument checks.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -24,10 +23,10 @@
 
 namespace svlm {
 
-constexpr int BM = 128, BN = 128, BK = 64;   // BK bf16 = 128 bytes: one swizzle row
+constexpr int BM = 128, BN = 256, BK = 64;   // BK bf16 = 128 bytes: one swizzle row
 constexpr int NS = 4;                          // pipeline stages
-constexpr int STAGE_A = BM * BK * 2, STAGE_B = BN * BK * 2;   // 16 KB each
-constexpr int TMEM_COLS = BN;                  // fp32 accumulator, 128 lanes x 128 columns
+constexpr int STAGE_A = BM * BK * 2, STAGE_B = BN * BK * 2;   // 16 KB and 32 KB
+constexpr int TMEM_COLS = BN;                  // fp32 accumulator, 128 lanes x 256 columns
 constexpr uint64_t WAIT_NS = 200ull * 1000 * 1000;
 
 struct __align__(8) Ctl {
@@ -119,7 +118,9 @@ __global__ void __launch_bounds__(128, 1)
   unsigned char* sB = smem + NS * STAGE_A;
   Ctl& C = *reinterpret_cast<Ctl*>(smem + NS * (STAGE_A + STAGE_B));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  // consecutive CTAs take the M tiles of one N tile, so a W tile is read from HBM
+  // once and served to the other M tiles from L2
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
   const int nk = d / BK;
 
   if (tid == 0) {
@@ -267,7 +268,8 @@ sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int
                               int32_t* flag, void* stream) {
   using namespace svlm;
   if (!hidden || !weight || !logits || !flag) return SV_ERR_NULL;
-  if (M < 1 || M > 65535 * BM || N < 1 || d < BK || d > 65536 || d % BK) return SV_ERR_SHAPE;
+  if (M < 1 || M > 2147483647 - BM || N < 1 || N > 65535 * BN || d < BK || d > 65536 || d % BK)
+    return SV_ERR_SHAPE;
   if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(logits, 4) || !aligned(flag, 4))
     return SV_ERR_ALIGN;
   CUtensorMap mh, mw;
@@ -280,7 +282,7 @@ sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int
         return cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
       }) != cudaSuccess)
     return SV_ERR_CUDA;
-  const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  const dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((N + BN - 1) / BN));
   lm_head_kernel<<<grid, 128, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(mh, mw, logits, M, N, d, flag);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -2452,10 +2452,6 @@ int kf_trace_copy(unsigned long long* host, size_t n) {
   if (n > 1024 * 8) n = 1024 * 8;
   return cudaMemcpyFromSymbol(host, g_kftrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
 }
-int kc_trace_copy(unsigned long long* host, size_t n) {
-  if (n > 4096 * 8) n = 4096 * 8;
-  return cudaMemcpyFromSymbol(host, g_kctrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
-}
 int kh_trace_copy(unsigned long long* host, size_t n) {
   if (n > 4096 * 8) n = 4096 * 8;
   return cudaMemcpyFromSymbol(host, g_khtrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;

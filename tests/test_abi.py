@@ -91,7 +91,7 @@ def test_lm_head_entry_points_validate_before_launching():
         return lib.spec_lm_head_logits(h, w, M, N, d, z, f, None)
     assert lm(h=None) == 1 and lm(z=None) == 1 and lm(f=None) == 1
     assert lm(M=0) == 2 and lm(N=0) == 2 and lm(d=0) == 2 and lm(d=96) == 2 and lm(d=65600) == 2
-    assert lm(M=65535 * 128 + 1) == 2
+    assert lm(N=65535 * 256 + 1) == 2 and lm(M=2**31 - 128) == 2
     assert lm(h=A + 8) == 6 and lm(w=A + 4) == 6 and lm(z=A + 2) == 6
 
     wsb = sv.spec_verify_workspace_bytes(2, 2)
