@@ -30,8 +30,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_NAME = "keyhist_kernel"     # dominant kernel of sampled bf16 workloads
-CLUSTER_KERNEL = "sv_kernel"       # dominant kernel of sampled fp32 workloads
+KERNEL_NAME = "keyhist_kernel"     # dominant kernel of sampled bf16 batches
+FP32_KERNEL = "fstream_kernel"     # dominant kernel of sampled fp32 batches
+CLUSTER_KERNEL = "sv_kernel"       # dominant kernel of small batches
 GREEDY_KERNEL = "greedy_kernel"    # dominant kernel of temperature-0 workloads
 
 
@@ -74,20 +75,20 @@ def dominant_kernel(workload: str) -> str:
     w = WORKLOADS[workload]
     if workload == "greedy":
         return GREEDY_KERNEL
-    keyhist = str(w.dtype).endswith("bfloat16") and w.B * (w.K + 1) >= 16
-    return KERNEL_NAME if keyhist else CLUSTER_KERNEL
+    if w.B * (w.K + 1) < 16:
+        return CLUSTER_KERNEL
+    return KERNEL_NAME if str(w.dtype).endswith("bfloat16") else FP32_KERNEL
 
 
 def launches_per_call(workload: str) -> int:
     """Kernels one spec_verify call launches on this workload's 16-byte aligned rows:
-    greedy_kernel, then (with draft logits) keyhist_kernel for bf16 rows and the
-    cluster kernel sv_kernel."""
+    greedy_kernel, then (with draft logits and at least 16 rows) keyhist_kernel for
+    bf16 rows or fstream_kernel for fp32 rows, then the cluster kernel sv_kernel."""
     from speculative_decoding_verification_30_gb300.workloads import WORKLOADS
     w = WORKLOADS[workload]
     if workload == "greedy":
         return 1                                   # no draft logits: greedy_kernel alone
-    keyhist = str(w.dtype).endswith("bfloat16") and w.B * (w.K + 1) >= 16
-    return 3 if keyhist else 2
+    return 3 if w.B * (w.K + 1) >= 16 else 2
 
 
 def profiled_traffic(workload: str):

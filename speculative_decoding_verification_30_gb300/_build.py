@@ -10,7 +10,7 @@ LIB = os.path.join(HERE, "libspec_verify.so")
 SOURCES = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "spec_verify_noalloc.cu"),
            os.path.join(CSRC, "telemetry.cu"), os.path.join(CSRC, "lm_head.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(CSRC, "keyhist.cuh"),
-                  os.path.join(CSRC, "launch_cache.h"),
+                  os.path.join(CSRC, "launch_cache.h"), os.path.join(CSRC, "fstream.cuh"),
                   os.path.join(os.path.dirname(HERE), "include", "spec_verify.h"),
                   os.path.join(os.path.dirname(HERE), "include", "spec_lm_head.h")]
 

@@ -1,0 +1,832 @@
+// fstream.cuh -- one-CTA-per-row verify path for sampled sequences with fp32 rows.
+//
+// Included by spec_verify.cu after keyhist.cuh. It shares that path's workspace
+// (row results KhRow, tickets, kept-token lists, hand-back flags, work counter)
+// and its per-token arithmetic (kh_w weights, kh_kept, kh_elem, fixed-point
+// masses, the exact 128-bit inverse-CDF crossing test).
+//
+// A persistent grid of FT-thread CTAs (two per SM) takes the rows of the batch's
+// sampled sequences from a work counter, sequence-major. Per row, by its
+// truncation parameters:
+//   top-k (0 < k <= 256): the k-th largest of the threads' first-wave maxima is
+//     at most the row's k-th largest logit, so every top-k token lies at or above
+//     it; the stream lists those logits as composite keys (order key << 32 | ~id,
+//     so descending keys are logit descending, id ascending); the list is sorted
+//     and its first k entries are the top-k set; a top-p cut falls inside them.
+//   no truncation: the stream sums the weights 2^((z - m_t) c) with a per-thread
+//     running maximum m_t (the sum is rescaled when m_t grows).
+//   top-p only: the stream adds each weight 2^((z - R) c) (R = first-wave maximum)
+//     to a per-thread bin by its binade (shared memory, no atomics); the bin where
+//     the exclusive mass first exceeds P * Z is then read again from L2 and split
+//     into 256 sub-bins by the weight's top mantissa bits (counts and exact
+//     fixed-point masses); the crossing sub-bin's logits are listed, sorted and
+//     walked to the exact cut.
+// The row's result (cut logit, id cut, 2^44 / kept mass, maximum, c) and the
+// probability of the sequence's drafted token at that position go to the
+// workspace. The CTA that finishes a sequence's last row runs the acceptance
+// tests in order and draws the replacement from (p - q)+ or the bonus token from
+// p_K by an inverse CDF in token-id order, over the listed kept tokens when the
+// target row has a list, else over the whole rows (from L2).
+//
+// Rows this path does not serve (top-k above 256, a list or bin that overflows,
+// weights out of range) hand their sequence to the cluster kernel, as the bf16
+// path does.
+#pragma once
+
+namespace sv {
+
+constexpr int FT = 512;                      // threads per CTA
+constexpr int FWARP = FT / 32;
+constexpr int FPF = 4;                       // float4 vectors per thread and load wave
+constexpr int FLCAP = 4096;                  // listed candidates (u64 composite keys)
+constexpr int FNB = 48;                      // coarse weight bins (one binade each)
+constexpr int FB_TOP = 142;                  // bin = FB_TOP - exponent field of the weight
+constexpr int FNSUB = 256;                   // sub-bins of the crossing bin
+constexpr int FKMAX = 256;                   // largest top_k served here
+constexpr int FMAXBLK = 128;                 // 32-vector blocks per warp range (V <= 262144)
+constexpr size_t FS_SMEM = (size_t)FNB * FT * 4;   // bins | list | sampling block sums
+
+struct FsShared {
+  unsigned long long s64[FWARP];
+  unsigned long long s64b[FWARP];
+  uint32_t s32[FWARP];
+  float fmax[FWARP];
+  uint32_t cmax;                             // first-wave maximum (order key)
+  uint32_t lcount;                           // candidates pushed
+  uint32_t rflags;                           // row flags raised during the stream
+  uint32_t hsel[2];                          // radix select: digit, remaining rank
+  int item, last, flags, nacc, tok;
+  uint32_t llen[17];
+  uint32_t flag[16];
+  float pz[16], qz[16];
+  unsigned long long binm[FNB];
+  uint32_t dh[256];                          // radix-select digit counts / sub-bin counts
+  unsigned long long smass[FNSUB];
+  unsigned long long mabove;                 // exclusive mass before the crossing sub-bin
+  int jstar, sstar, ncut;
+  float zt;
+  int idcut;
+  unsigned long long zkept;
+};
+
+constexpr uint32_t FS_OVER = 8u;             // a weight beyond the bins (hand back)
+
+__device__ __forceinline__ float4 fs_ld(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float4 fs_ld_l2(const float4* p) { return __ldcg(p); }
+__device__ __forceinline__ float fs_at(const float4& v, int e) {
+  return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+}
+// Coarse bin of a weight e = 2^x (x relative to the first-wave maximum): FB_TOP
+// minus e's exponent field, so bin j holds x in [15 - j, 16 - j); x >= 16 is out
+// of range (*over), everything below the last bin's binade joins it.
+__device__ __forceinline__ int fs_bin(float e, uint32_t* over) {
+  const int b = FB_TOP - (int)(__float_as_uint(e) >> 23);
+  if (b < 0) *over = 1u;
+  return min(max(b, 0), FNB - 1);
+}
+
+// k-th largest (1-based, k <= FT) of the CTA's per-thread 32-bit keys, by four
+// rounds of 8-bit digits (most significant first). Every thread returns it.
+__device__ __noinline__ uint32_t fs_kth_key(uint32_t key, int k, FsShared& S) {
+  const int tid = threadIdx.x, l = lane_id();
+  uint32_t prefix = 0u, pmask = 0u;
+  uint32_t kk = (uint32_t)k;
+  for (int r = 0; r < 4; ++r) {
+    const int sh = 24 - 8 * r;
+    for (int i = tid; i < 256; i += FT) S.dh[i] = 0u;
+    __syncthreads();
+    if ((key & pmask) == prefix) atomicAdd(&S.dh[(key >> sh) & 255u], 1u);
+    __syncthreads();
+    if (tid < 32) {
+      // lane l holds digits 255 - 8l down to 248 - 8l
+      uint32_t c8[8], s = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c8[j] = S.dh[255 - 8 * l - j];
+        s += c8[j];
+      }
+      uint32_t incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (l >= o) incl += t;
+      }
+      const uint32_t excl = incl - s;
+      if (excl < kk && kk <= incl) {
+        uint32_t run = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run + c8[j] >= kk) {
+            S.hsel[0] = (uint32_t)(255 - 8 * l - j);
+            S.hsel[1] = kk - run;
+            break;
+          }
+          run += c8[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= S.hsel[0] << sh;
+    pmask |= 255u << sh;
+    kk = S.hsel[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Sorts a[0, n) descending in place (n a power of two, entries past the data 0).
+__device__ __noinline__ void fs_sort_desc(unsigned long long* a, int n) {
+  __syncthreads();
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n / 2; i += FT) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const unsigned long long x = a[lo], y = a[hi];
+        if (desc ? x < y : x > y) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ __forceinline__ float fs_key_value(unsigned long long e) { return key_to_float((uint32_t)(e >> 32)); }
+__device__ __forceinline__ int fs_key_id(unsigned long long e) { return (int)~(uint32_t)e; }
+
+// Pushes the logits of vector v that are >= thr as composite keys (one atomic per
+// vector with candidates; nothing is written past FLCAP).
+__device__ __forceinline__ void fs_push(const float4& x, int v, float thr, FsShared& S,
+                                        unsigned long long* list) {
+  uint32_t mk = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) mk |= (uint32_t)(fs_at(x, e) >= thr) << e;
+  if (!mk) return;
+  uint32_t slot = atomicAdd(&S.lcount, (uint32_t)__popc(mk));
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (!((mk >> e) & 1u)) continue;
+    if (slot < (uint32_t)FLCAP)
+      list[slot] = ((unsigned long long)okey(fs_at(x, e)) << 32) | (uint32_t)~(uint32_t)(4 * v + e);
+    ++slot;
+  }
+}
+
+// Row classes.
+constexpr int FC_TOPK = 0, FC_ALL = 1, FC_TOPP = 2;
+
+// Streams the row once (double-buffered waves of FPF vectors per thread).
+// Returns this thread's maximum; *nan is set on NaN or +inf. Top-k rows list the
+// logits >= *thr (set from the first wave); no-truncation rows leave the thread's
+// running maximum and sum in *mt / *st; top-p rows fill the bins.
+template <int CLS>
+__device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float c, FsShared& S,
+                                        unsigned long long* list, float* bins, float* thr, float* mt,
+                                        float* st, float* Rout, bool* nan) {
+  const int tid = threadIdx.x, l = lane_id();
+  float4 cur[FPF], nxt[FPF];
+  const float4 NEG = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+  for (int p = 0; p < FPF; ++p) {
+    const int q = tid + p * FT;
+    cur[p] = q < nv ? fs_ld(src + q) : NEG;
+  }
+  float tmax = -INFINITY;
+  bool bad = false;
+#pragma unroll
+  for (int p = 0; p < FPF; ++p)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float z = fs_at(cur[p], e);
+      tmax = fmaxf(tmax, z);
+      bad |= !(z == z) || z == INFINITY;
+    }
+  // first-wave block maximum R; top-k threshold: k-th largest thread maximum
+  float fm = tmax;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, o));
+  __syncthreads();
+  if (tid == 0) {
+    S.cmax = okey(-INFINITY);
+    S.lcount = 0u;
+    S.rflags = 0u;
+  }
+  __syncthreads();
+  if (l == 0) atomicMax(&S.cmax, okey(fm));
+  __syncthreads();
+  const float R = key_to_float(S.cmax);
+  *Rout = R;
+  float th = -INFINITY;
+  if (CLS == FC_TOPK) th = key_to_float(fs_kth_key(okey(tmax), k, S));
+  *thr = th;
+  const float nRc = -(R * c);
+  float m_t = -INFINITY, s_t = 0.0f;
+  uint32_t over = 0u;
+  for (int q0 = tid; q0 < nv; q0 += FPF * FT) {
+#pragma unroll
+    for (int p = 0; p < FPF; ++p) {
+      const int q = q0 + FPF * FT + p * FT;
+      nxt[p] = q < nv ? fs_ld(src + q) : NEG;
+    }
+#pragma unroll
+    for (int p = 0; p < FPF; ++p) {
+      const int q = q0 + p * FT;
+      if (q >= nv) continue;
+      const float4 x = cur[p];
+      const float vm = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+      tmax = fmaxf(tmax, vm);
+      bad |= !(x.x == x.x) || !(x.y == x.y) || !(x.z == x.z) || !(x.w == x.w) || vm == INFINITY;
+      if (CLS == FC_TOPK) {
+        if (vm >= th) fs_push(x, q, th, S, list);
+      } else if (CLS == FC_ALL) {
+        if (vm > m_t) {
+          s_t = m_t > -INFINITY ? s_t * ex2_approx((m_t - vm) * c) : 0.0f;
+          m_t = vm;
+        }
+        const float nmc = -(m_t * c);
+        s_t += (ex2_approx(fmaf(x.x, c, nmc)) + ex2_approx(fmaf(x.y, c, nmc))) +
+               (ex2_approx(fmaf(x.z, c, nmc)) + ex2_approx(fmaf(x.w, c, nmc)));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float w = ex2_approx(fmaf(fs_at(x, e), c, nRc));
+          float* b = bins + fs_bin(w, &over) * FT + tid;
+          *b += w;
+        }
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < FPF; ++p) cur[p] = nxt[p];
+  }
+  if (over) atomicOr(&S.rflags, FS_OVER);
+  *mt = m_t;
+  *st = s_t;
+  *nan = bad;
+  return tmax;
+}
+
+// Second and third passes of a top-p row (from L2): sub-bin histogram of coarse
+// bin j (PASS 2), or the list of sub-bin s of bin j (PASS 3).
+template <int PASS>
+__device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float nRc, float scale, int j,
+                                       int s, FsShared& S, unsigned long long* list) {
+  const int tid = threadIdx.x;
+  float4 cur[FPF], nxt[FPF];
+  const float4 NEG = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  uint32_t over = 0u;
+#pragma unroll
+  for (int p = 0; p < FPF; ++p) {
+    const int q = tid + p * FT;
+    cur[p] = q < nv ? fs_ld_l2(src + q) : NEG;
+  }
+  for (int q0 = tid; q0 < nv; q0 += FPF * FT) {
+#pragma unroll
+    for (int p = 0; p < FPF; ++p) {
+      const int q = q0 + FPF * FT + p * FT;
+      nxt[p] = q < nv ? fs_ld_l2(src + q) : NEG;
+    }
+#pragma unroll
+    for (int p = 0; p < FPF; ++p) {
+      const int q = q0 + p * FT;
+      if (q >= nv) continue;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float z = fs_at(cur[p], e);
+        const float w = ex2_approx(fmaf(z, c, nRc));
+        if (fs_bin(w, &over) != j) continue;
+        const int sb = (int)((__float_as_uint(w) >> 15) & 255u);
+        if (PASS == 2) {
+          atomicAdd(&S.dh[sb], 1u);
+          atomicAdd(&S.smass[sb], fix_pow2(w * scale, FIX));
+        } else if (sb == s) {
+          const uint32_t slot = atomicAdd(&S.lcount, 1u);
+          if (slot < (uint32_t)FLCAP)
+            list[slot] = ((unsigned long long)okey(z) << 32) | (uint32_t)~(uint32_t)(4 * q + e);
+        }
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < FPF; ++p) cur[p] = nxt[p];
+  }
+}
+
+__device__ __forceinline__ int fs_pow2(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+// One fp32 row: stream, cut, normaliser, and the probability of the drafted token
+// d (-1: none). Top-k rows list their kept tokens in glist (ids, no order). The
+// result is returned in every thread; pad[0] holds p(d) as float bits, pad[1] the
+// list length or KH_NOLIST.
+__device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, float topP, int d,
+                                     uint32_t* glist, FsShared& S) {
+  const int tid = threadIdx.x, l = lane_id(), w = warp_id();
+  const int nv = V / 4;
+  const float4* src = reinterpret_cast<const float4*>(row);
+  const float c = __fdiv_rn(KH_LOG2E, T);
+  const bool topk = k > 0 && k < V;
+  const bool topp = topP < 1.0f;
+  const int cls = topk ? FC_TOPK : (topp ? FC_TOPP : FC_ALL);
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(kh_dyn);
+  float* bins = reinterpret_cast<float*>(kh_dyn);
+  KhRow res;
+  res.c = c;
+  res.zt = -INFINITY;
+  res.idcut = V;
+  res.invZ = 0.0f;
+  res.flags = 0u;
+  res.pad[0] = 0u;
+  res.pad[1] = KH_NOLIST;
+  if (topk && k > FKMAX) {
+    res.m = 0.0f;
+    res.flags = KH_BAIL;
+    return res;
+  }
+  if (cls == FC_TOPP) {
+    __syncthreads();
+    for (int j = 0; j < FNB; ++j) bins[j * FT + tid] = 0.0f;
+    __syncthreads();
+  }
+  float thr, mt, st, R;
+  bool nan;
+  float tm;
+  if (cls == FC_TOPK) tm = fs_stream<FC_TOPK>(src, nv, k, c, S, list, bins, &thr, &mt, &st, &R, &nan);
+  else if (cls == FC_ALL) tm = fs_stream<FC_ALL>(src, nv, k, c, S, list, bins, &thr, &mt, &st, &R, &nan);
+  else tm = fs_stream<FC_TOPP>(src, nv, k, c, S, list, bins, &thr, &mt, &st, &R, &nan);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+  if (l == 0) S.fmax[w] = tm;
+  const bool anynan = __syncthreads_or(nan ? 1 : 0) != 0;
+  float m = S.fmax[0];
+#pragma unroll
+  for (int i = 1; i < KWARP; ++i) m = fmaxf(m, S.fmax[i]);
+  res.m = m;
+  if (anynan || !(m > -INFINITY)) {
+    res.flags = KH_ERR;
+    return res;
+  }
+  if (S.rflags & FS_OVER) {
+    res.flags = KH_BAIL;
+    return res;
+  }
+  unsigned long long Zk = 0ull;
+  if (cls == FC_ALL) {
+    // sum of the threads' running sums, each moved to the frame of m
+    unsigned long long t = mt > -INFINITY ? fix_pow2(st * ex2_approx((mt - m) * c), FIX) : 0ull;
+    t = warp_sum(t);
+    __syncthreads();
+    if (l == 0) S.s64[w] = t;
+    __syncthreads();
+    for (int i = 0; i < KWARP; ++i) Zk += S.s64[i];
+  } else if (cls == FC_TOPK) {
+    const uint32_t nl = S.lcount;
+    if (nl > (uint32_t)FLCAP || nl < (uint32_t)k) {
+      res.flags = KH_BAIL;
+      return res;
+    }
+    const int n2 = fs_pow2((int)nl);
+    for (int i = (int)nl + tid; i < n2; i += FT) list[i] = 0ull;
+    fs_sort_desc(list, n2);
+    // the top k in order; their exact fixed-point weights and exclusive sums
+    unsigned long long wk = 0ull;
+    if (tid < k) wk = fix_pow2(kh_w(fs_key_value(list[tid]), m, c), FIX);
+    unsigned long long ZL1;
+    const unsigned long long ex = kh_below<unsigned long long>(wk, S.s64, &ZL1);
+    int nkeep = k;
+    if (topp) {
+      const unsigned long long Y = mass_threshold(topP, ZL1);
+      // kept iff the exclusive mass <= Y: a prefix of the k entries
+      nkeep = __syncthreads_count(tid < k && ex <= Y);
+    }
+    if (tid == nkeep - 1) {
+      S.zt = fs_key_value(list[tid]);
+      S.idcut = fs_key_id(list[tid]);
+      S.zkept = ex + wk;
+    }
+    if (glist)
+      for (int i = tid; i < nkeep; i += FT) glist[i] = (uint32_t)fs_key_id(list[i]);
+    __syncthreads();
+    res.zt = S.zt;
+    res.idcut = S.idcut;
+    res.pad[1] = (uint32_t)nkeep;
+    Zk = S.zkept;
+  } else {
+    // top-p: bin masses in the frame of m; warp w sums bins w and w + 16
+    const float scale = ex2_approx((R - m) * c);
+    for (int j = w; j < FNB; j += KWARP) {
+      unsigned long long t = 0ull;
+      for (int i = l; i < FT; i += 32) t += fix_pow2(bins[j * FT + i] * scale, FIX);
+      t = warp_sum(t);
+      if (l == 0) S.binm[j] = t;
+    }
+    __syncthreads();
+    unsigned long long Z = 0ull;
+    for (int j = 0; j < FNB; ++j) Z += S.binm[j];
+    const unsigned long long Y = mass_threshold(topP, Z);
+    // the bin where the exclusive mass first exceeds Y
+    int js = -1;
+    unsigned long long above = 0ull;
+    for (int j = 0; j < FNB; ++j) {
+      if (above + S.binm[j] > Y) {
+        js = j;
+        break;
+      }
+      above += S.binm[j];
+    }
+    if (js < 0 || js == FNB - 1) {
+      res.flags = KH_BAIL;
+      return res;
+    }
+    // sub-bins of bin js (counts, exact masses) from L2
+    __syncthreads();
+    for (int i = tid; i < FNSUB; i += FT) {
+      S.dh[i] = 0u;
+      S.smass[i] = 0ull;
+    }
+    __syncthreads();
+    const float nRc = -(R * c);
+    fs_refine<2>(src, nv, c, nRc, scale, js, 0, S, list);
+    __syncthreads();
+    if (tid == 0) {
+      int ss = -1;
+      unsigned long long cum = above;
+      for (int sb = FNSUB - 1; sb >= 0; --sb) {
+        if (cum + S.smass[sb] > Y) {
+          ss = sb;
+          break;
+        }
+        cum += S.smass[sb];
+      }
+      S.sstar = ss;
+      S.mabove = cum;
+      S.lcount = 0u;
+    }
+    __syncthreads();
+    const int ss = S.sstar;
+    if (ss < 0) {
+      res.flags = KH_BAIL;                   // rounding left the crossing outside the bin
+      return res;
+    }
+    fs_refine<3>(src, nv, c, nRc, scale, js, ss, S, list);
+    __syncthreads();
+    const uint32_t nl = S.lcount;
+    if (nl > (uint32_t)FLCAP || nl == 0u) {
+      res.flags = KH_BAIL;
+      return res;
+    }
+    const int n2 = fs_pow2((int)nl);
+    for (int i = (int)nl + tid; i < n2; i += FT) list[i] = 0ull;
+    fs_sort_desc(list, n2);
+    // walk the sorted entries: kept while the exclusive mass <= Y (a prefix, at
+    // least the first entry); their weights as the sub-bin masses summed them
+    if (tid == 0) {
+      unsigned long long ex = S.mabove;
+      int last = 0;
+      for (int i = 0; i < (int)nl; ++i) {
+        if (ex > Y) break;
+        last = i;
+        ex += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
+      }
+      S.zt = fs_key_value(list[last]);
+      S.idcut = fs_key_id(list[last]);
+      S.zkept = ex;
+    }
+    __syncthreads();
+    res.zt = S.zt;
+    res.idcut = S.idcut;
+    Zk = S.zkept;
+  }
+  if (Zk == 0ull) {
+    res.flags = KH_BAIL;
+    return res;
+  }
+  res.invZ = __fdiv_rn(17592186044416.0f, (float)Zk);   // 2^44 / Z
+  if (d >= 0) {
+    const float zd = __ldg(row + d);
+    const float pd = kh_kept(zd, d, res.zt, res.idcut) ? __fmul_rn(kh_w(zd, m, c), res.invZ) : 0.0f;
+    res.pad[0] = __float_as_uint(pd);
+  }
+  return res;
+}
+
+// Fixed-point (2^-40) residual and target masses of the 4 tokens of vector v.
+__device__ __forceinline__ void fs_vec(const float4* sp, const float4* sq, int v, bool paired, const KhW& tp,
+                                       const KhW& tq, unsigned long long* R, unsigned long long* Pm) {
+  const float4 a = __ldcg(sp + v);
+  const float4 b = paired ? __ldcg(sq + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  unsigned long long ra = 0, pa = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float r, p;
+    kh_elem(fs_at(a, e), fs_at(b, e), 4 * v + e, paired, tp, tq, &r, &p);
+    ra += fixr(r);
+    pa += fixr(p);
+  }
+  *R = ra;
+  *Pm = pa;
+}
+
+// Inverse CDF in token-id order over (p - q)+ (paired) or p, over whole fp32 rows
+// (from L2): the smallest id j whose running sum S_j satisfies S_j * 2^24 > kv * S
+// (S the total); when the residual mass is 0 the target p is used. Warps sum
+// contiguous ranges per 32-vector block; warp 0 locates the crossing block with
+// lane-parallel scans and walks it. -1 if no token qualifies.
+__device__ __noinline__ int fs_sample_full(const float4* sp, const float4* sq, int nv, bool paired, KhW tp,
+                                           KhW tq, uint32_t kv, FsShared& S) {
+  const int w = warp_id(), l = lane_id();
+  const int cw = (nv + FWARP - 1) / FWARP;
+  const int nb = (cw + 31) / 32;
+  const int a0 = min(w * cw, nv), a1 = min(a0 + cw, nv);
+  unsigned long long* bR = reinterpret_cast<unsigned long long*>(kh_dyn);
+  unsigned long long* bP = bR + FWARP * FMAXBLK;
+  unsigned long long tR = 0, tP = 0;
+  for (int j = 0; j < nb; ++j) {
+    const int v = a0 + j * 32 + l;
+    unsigned long long r = 0, p = 0;
+    if (v < a1) fs_vec(sp, sq, v, paired, tp, tq, &r, &p);
+    p = kh_wsum(p);
+    r = paired ? kh_wsum(r) : p;
+    if (l == 0) {
+      bR[w * FMAXBLK + j] = r;
+      bP[w * FMAXBLK + j] = p;
+    }
+    tR += r;
+    tP += p;
+  }
+  __syncthreads();
+  if (l == 0) {
+    S.s64[w] = tR;
+    S.s64b[w] = tP;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const unsigned long long oR = l < FWARP ? S.s64[l] : 0ull, oP = l < FWARP ? S.s64b[l] : 0ull;
+    const unsigned long long SR = warp_sum(oR), SP = warp_sum(oP);
+    const bool useR = SR > 0ull;
+    const unsigned long long St = useR ? SR : SP;
+    const unsigned long long* bv = useR ? bR : bP;
+    const unsigned long long own = useR ? oR : oP;
+    unsigned long long incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (l >= o) incl += t;
+    }
+    const uint32_t bw = __ballot_sync(0xffffffffu, l < FWARP && mul_gt(incl, 1ull << 24, kv, St));
+    int tok = -1;
+    if (bw) {
+      const int ww = __ffs(bw) - 1;
+      unsigned long long acc = __shfl_sync(0xffffffffu, incl - own, ww);
+      const int wa0 = min(ww * cw, nv), wa1 = min(wa0 + cw, nv);
+      // blocks of warp ww: lane l holds blocks 4l .. 4l+3
+      unsigned long long b4[4], bs = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        b4[u] = 4 * l + u < nb ? bv[ww * FMAXBLK + 4 * l + u] : 0ull;
+        bs += b4[u];
+      }
+      unsigned long long bi = bs;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, bi, o);
+        if (l >= o) bi += t;
+      }
+      const uint32_t bl = __ballot_sync(0xffffffffu, mul_gt(acc + bi, 1ull << 24, kv, St));
+      if (bl) {
+        const int lb = __ffs(bl) - 1;
+        acc += __shfl_sync(0xffffffffu, bi - bs, lb);
+        int jb = 4 * lb;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          const unsigned long long bu = __shfl_sync(0xffffffffu, b4[u], lb);
+          if (jb == 4 * lb + u && !mul_gt(acc + bu, 1ull << 24, kv, St)) {
+            acc += bu;
+            ++jb;
+          }
+        }
+        // the block: one vector per lane, in id order
+        const int v = wa0 + jb * 32 + l;
+        unsigned long long r = 0, p = 0;
+        if (v < wa1) fs_vec(sp, sq, v, paired, tp, tq, &r, &p);
+        const unsigned long long mine = useR ? r : p;
+        unsigned long long ci = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long t = __shfl_up_sync(0xffffffffu, ci, o);
+          if (l >= o) ci += t;
+        }
+        const uint32_t hit = __ballot_sync(0xffffffffu, v < wa1 && mul_gt(acc + ci, 1ull << 24, kv, St));
+        if (hit && l == __ffs(hit) - 1) {
+          const float4 a = __ldcg(sp + v);
+          const float4 bq = paired ? __ldcg(sq + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          unsigned long long run = acc + ci - mine;
+          for (int e = 0; e < 4 && tok < 0; ++e) {
+            float rr, pp;
+            kh_elem(fs_at(a, e), fs_at(bq, e), 4 * v + e, paired, tp, tq, &rr, &pp);
+            run += fixr(useR ? rr : pp);
+            if (mul_gt(run, 1ull << 24, kv, St)) tok = 4 * v + e;
+          }
+        }
+        tok = __reduce_max_sync(0xffffffffu, tok);
+      }
+    }
+    if (l == 0) S.tok = tok;
+  }
+  __syncthreads();
+  return S.tok;
+}
+
+// The inverse CDF of fs_sample_full over a target row whose kept tokens are
+// listed (L <= 256 ids, any order): only those carry p > 0, so the sums run over
+// the list sorted by id.
+__device__ __noinline__ int fs_sample_list(const float* zp_row, const float* zq_row, const uint32_t* glist,
+                                           int L, bool paired, KhW tp, KhW tq, uint32_t kv, FsShared& S) {
+  const int tid = threadIdx.x;
+  uint32_t* ids = kh_dyn;                                          // [FKMAX]
+  unsigned long long* wr = reinterpret_cast<unsigned long long*>(kh_dyn + FKMAX);   // sorted r
+  unsigned long long* wp = wr + FKMAX;                             // sorted p
+  uint32_t* sid = reinterpret_cast<uint32_t*>(wp + FKMAX);         // sorted ids
+  for (int e = tid; e < L; e += FT) ids[e] = __ldcg(glist + e);
+  __syncthreads();
+  for (int e = tid; e < L; e += FT) {
+    const int id = (int)ids[e];
+    const float zp = __ldcg(zp_row + id);
+    const float zq = paired ? __ldcg(zq_row + id) : 0.0f;
+    float r, p;
+    kh_elem(zp, zq, id, paired, tp, tq, &r, &p);
+    int rank = 0;
+    for (int f = 0; f < L; ++f) rank += (int)(ids[f] < (uint32_t)id);
+    wr[rank] = fixr(r);
+    wp[rank] = fixr(p);
+    sid[rank] = (uint32_t)id;
+  }
+  __syncthreads();
+  const unsigned long long r1 = tid < L ? wr[tid] : 0ull, p1 = tid < L ? wp[tid] : 0ull;
+  unsigned long long SR, SP;
+  const unsigned long long xr = kh_below<unsigned long long>(r1, S.s64, &SR);
+  const unsigned long long xp = kh_below<unsigned long long>(p1, S.s64b, &SP);
+  const bool useR = SR > 0ull;
+  const unsigned long long St = useR ? SR : SP;
+  if (tid == 0) S.tok = -1;
+  __syncthreads();
+  const unsigned long long run = useR ? xr : xp, own = useR ? r1 : p1;
+  if (tid < L && !mul_gt(run, 1ull << 24, kv, St) && mul_gt(run + own, 1ull << 24, kv, St)) S.tok = (int)sid[tid];
+  __syncthreads();
+  return S.tok;
+}
+
+// Clears sequence b's kept-token lists (their lengths are in S.llen).
+__device__ __noinline__ void fs_clear_lists(const Params& P, int b, const FsShared& S) {
+  for (int r = 0; r <= P.K; ++r) {
+    const uint32_t L = S.llen[r];
+    if (L == KH_NOLIST || L == 0u) continue;
+    uint32_t* gl = P.ws_lists + ((size_t)b * (P.K + 1) + r) * KH_KCAP;
+    for (uint32_t e = threadIdx.x; e < L && e < (uint32_t)KH_KCAP; e += FT) gl[e] = 0u;
+  }
+}
+
+// The sequence's rows are all done: acceptance in order from the drafted tokens'
+// probabilities the row CTAs left, then the replacement or bonus token; writes
+// the outputs (or hands the sequence to the cluster kernel) and re-arms the
+// ticket, leaving the workspace zeroed.
+__device__ __noinline__ void fs_finalize(const Params& P, int b, FsShared& S) {
+  const int K = P.K, R2 = 2 * K + 1, tid = threadIdx.x;
+  const KhRow* rr = P.ws_rowres + (size_t)b * R2;
+  const float* tgt = static_cast<const float*>(P.rows0) + (size_t)b * (K + 1) * P.V;
+  const float* drf = static_cast<const float*>(P.rows1) + (size_t)b * K * P.V;
+  if (tid < 32) {
+    uint32_t f = 0;
+    for (int r = tid; r < R2; r += 32) f |= __ldcg(&rr[r].flags);
+    if (tid <= K) S.llen[tid] = __ldcg(&rr[tid].pad[1]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) f |= __shfl_xor_sync(0xffffffffu, f, o);
+    if (tid < K && !(f & (KH_ERR | KH_BAIL))) {
+      const float p = __uint_as_float(__ldcg(&rr[tid].pad[0]));
+      const float q = __uint_as_float(__ldcg(&rr[K + 1 + tid].pad[0]));
+      uint32_t ku, kv;
+      philox_uniform_bits(P.seed, philox_offset_of(P), (uint32_t)b, (uint32_t)tid, &ku, &kv);
+      S.flag[tid] = __fmul_rn((float)ku * 5.9604644775390625e-08f, q) < p ? 1u : 0u;
+    }
+    if (tid == 0) S.flags = (int)f;
+  }
+  __syncthreads();
+  const int flags = S.flags;
+  if (tid == 0) {
+    int n = K;
+    if (!(flags & (KH_ERR | KH_BAIL)))
+      for (int i = 0; i < K; ++i)
+        if (!S.flag[i]) {
+          n = i;
+          break;
+        }
+    S.nacc = n;
+  }
+  __syncthreads();
+  const int n = S.nacc;
+  if (flags & KH_BAIL) {
+    // the cluster kernel serves the sequence and clears the flag
+    if (tid == 0) {
+      P.ws_fb[b] = 1u;
+      atomicOr(P.ws_work, 1u);
+      P.ws_tickets[b] = 0u;
+    }
+    fs_clear_lists(P, b, S);
+    __syncthreads();
+    uint4* rz = reinterpret_cast<uint4*>(P.ws_rowres + (size_t)b * R2);
+    for (int t = tid; t < 2 * R2; t += FT) rz[t] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  int tok = -1;
+  if (!(flags & KH_ERR)) {
+    const bool paired = n < K;
+    const KhRow tp = kh_load_row(rr + n);
+    const KhRow tq = paired ? kh_load_row(rr + K + 1 + n) : tp;
+    uint32_t ku, kv;
+    philox_uniform_bits(P.seed, philox_offset_of(P), (uint32_t)b, (uint32_t)n, &ku, &kv);
+    const float* zp = tgt + (size_t)n * P.V;
+    const float* zq = paired ? drf + (size_t)n * P.V : zp;
+    const uint32_t L = tp.pad[1];
+    if (L != KH_NOLIST) {
+      tok = fs_sample_list(zp, zq, P.ws_lists + ((size_t)b * (K + 1) + n) * KH_KCAP, (int)L, paired,
+                           kh_wof(tp), kh_wof(tq), kv, S);
+    } else {
+      tok = fs_sample_full(reinterpret_cast<const float4*>(zp), reinterpret_cast<const float4*>(zq), P.V / 4,
+                           paired, kh_wof(tp), kh_wof(tq), kv, S);
+    }
+  }
+  if (tid == 0) {
+    const bool bad = (flags & KH_ERR) || tok < 0;
+    int32_t* ot = P.out_tokens + (size_t)b * (K + 1);
+    for (int q = 0; q <= K; ++q)
+      ot[q] = bad ? -1 : (q < n ? P.dtok[(size_t)b * K + q] : (q == n ? tok : -1));
+    P.out_n[b] = bad ? -1 : n;
+    P.ws_tickets[b] = 0u;
+  }
+  fs_clear_lists(P, b, S);
+  __syncthreads();
+  uint4* rz = reinterpret_cast<uint4*>(P.ws_rowres + (size_t)b * R2);
+  for (int t = tid; t < 2 * R2; t += FT) rz[t] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Persistent CTAs take rows of the batch's sampled fp32 sequences from a work
+// counter (sequence-major). Rows of other sequences are skipped.
+__global__ void __launch_bounds__(FT, 2) fstream_kernel(const Params P, int nitems) {
+  __shared__ FsShared S;
+  // the cluster kernel may launch now; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int tid = threadIdx.x;
+  const int K = P.K, R2 = 2 * K + 1;
+  while (true) {
+    if (tid == 0) S.item = (int)atomicAdd(P.ws_fnext, 1u);
+    __syncthreads();
+    const int item = S.item;
+    __syncthreads();
+    if (item >= nitems) break;
+    const int b = item / R2, r = item - b * R2;
+    if (!fast_seq(P, b)) continue;
+    const bool target = r <= K;
+    const float* row = target ? static_cast<const float*>(P.rows0) + ((size_t)b * (K + 1) + r) * P.V
+                              : static_cast<const float*>(P.rows1) + ((size_t)b * K + (r - K - 1)) * P.V;
+    // the drafted token whose probability this row gives (target rows i < K, draft rows)
+    const int pos = target ? r : r - K - 1;
+    const int d = pos < K ? P.dtok[(size_t)b * K + pos] : -1;
+    uint32_t* glist = target ? P.ws_lists + ((size_t)b * (K + 1) + r) * KH_KCAP : nullptr;
+    const KhRow res = fs_row(row, P.V, P.temp[b], P.topk[b], P.topp[b], d, glist, S);
+    if (tid == 0) {
+      uint4* dst = reinterpret_cast<uint4*>(P.ws_rowres + item);
+      // a draft row never keeps a list: the sampling list is the target row's
+      const uint32_t len = target ? res.pad[1] : KH_NOLIST;
+      dst[0] = make_uint4(__float_as_uint(res.zt), __float_as_uint(res.invZ), __float_as_uint(res.m),
+                          __float_as_uint(res.c));
+      dst[1] = make_uint4((uint32_t)res.idcut, res.flags, res.pad[0], len);
+      __threadfence();
+      S.last = atomicAdd(&P.ws_tickets[b], 1u) == (unsigned int)(R2 - 1);
+      if (S.last) __threadfence();
+    }
+    __syncthreads();
+    if (S.last) fs_finalize(P, b, S);
+    __syncthreads();
+  }
+  // finish only after greedy_kernel (launched before, possibly still running)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(P.ws_fdone, 1u) == gridDim.x - 1u) {
+      *P.ws_fnext = 0u;
+      *P.ws_fdone = 0u;
+    }
+  }
+}
+
+}  // namespace sv

@@ -94,7 +94,7 @@ struct Params {
   unsigned int* ws_done;        // cluster-kernel CTAs finished (resets ws_work)
   int greedy_split;             // temperature-0 verify units go to greedy_kernel
   int greedy_only;              // no draft logits: greedy_kernel serves the whole batch
-  int fast_split;               // sampled bf16 sequences go to keyhist_kernel
+  int fast_split;               // sampled sequences go to keyhist_kernel (bf16) or fstream_kernel (fp32)
   KhRow* ws_rowres;             // keyhist_kernel: per-row results [B][2K+1]
   unsigned int* ws_fb;          // keyhist_kernel: 1 = sequence handed to the cluster kernel
   unsigned int* ws_fnext;       // keyhist_kernel: work counter
@@ -361,6 +361,7 @@ __device__ __forceinline__ unsigned long long mass_threshold(float P, unsigned l
 
 }  // namespace sv
 #include "keyhist.cuh"
+#include "fstream.cuh"
 namespace sv {
 
 // --------------------------------------------------------- block helpers
@@ -2229,7 +2230,7 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
     // sampled bf16 sequences: one-pass key-histogram kernel, one CTA per row;
     // batches of fewer units than the cluster kernel runs clusters keep each
     // row spread over a cluster of SMs instead
-    p.fast_split = (dtype == SV_BF16 && draft_logits != nullptr && (long long)B * (K + 1) >= 16) ? 1 : 0;
+    p.fast_split = (draft_logits != nullptr && (long long)B * (K + 1) >= 16) ? 1 : 0;
     const int PV = 16 / (int)es;
     const int cmax = GV * NT * PV;
     const int G = (V + cmax - 1) / cmax;
@@ -2249,8 +2250,14 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
     p.greedy_split = 1;
     if (p.greedy_only) return SV_OK;
     if (p.fast_split) {
+      // sampled sequences, one CTA per row: the key-histogram kernel for bf16 rows,
+      // the fp32 streaming kernel for fp32 rows
+      const bool bf = dtype == SV_BF16;
+      void (*fk)(const Params, int) = bf ? keyhist_kernel : fstream_kernel;
+      const size_t fsm = bf ? KH_SMEM : FS_SMEM;
       int kblocks = 0;
-      if (keyhist_grid(keyhist_kernel, &kblocks) != cudaSuccess) return SV_ERR_CUDA;
+      if (resident_grid(reinterpret_cast<const void*>(fk), KT, fsm, &kblocks) != cudaSuccess)
+        return SV_ERR_CUDA;
       const int kitems = B * (2 * K + 1);
       const int kgrid = kitems < kblocks ? kitems : kblocks;
       // starts while greedy_kernel runs (it reads nothing greedy_kernel writes, and
@@ -2258,14 +2265,14 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
       cudaLaunchConfig_t kc = {};
       kc.gridDim = dim3((unsigned)kgrid, 1, 1);
       kc.blockDim = dim3(KT, 1, 1);
-      kc.dynamicSmemBytes = KH_SMEM;
+      kc.dynamicSmemBytes = fsm;
       kc.stream = st;
       cudaLaunchAttribute ka[1];
       ka[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       ka[0].val.programmaticStreamSerializationAllowed = 1;
       kc.attrs = ka;
       kc.numAttrs = 1;
-      if (cudaLaunchKernelEx(&kc, keyhist_kernel, p, kitems) != cudaSuccess) return SV_ERR_CUDA;
+      if (cudaLaunchKernelEx(&kc, fk, p, kitems) != cudaSuccess) return SV_ERR_CUDA;
     }
   }
   return do_launch(MODE_VERIFY, dtype, p, g, st);
