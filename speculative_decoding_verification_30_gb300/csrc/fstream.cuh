@@ -40,7 +40,7 @@ constexpr int FWARP = FT / 32;
 constexpr int FPF = 4;                       // float4 vectors per thread and load wave
 constexpr int FLCAP = 4096;                  // listed candidates (u64 composite keys)
 constexpr int FNB = 48;                      // coarse weight bins (one binade each)
-constexpr int FB_TOP = 142;                  // bin = FB_TOP - exponent field of the weight
+constexpr int FB_TOP = 150;                  // bin = FB_TOP - exponent field of the weight
 constexpr int FNSUB = 256;                   // sub-bins of the crossing bin
 constexpr int FKMAX = 256;                   // largest top_k served here
 constexpr int FMAXBLK = 128;                 // 32-vector blocks per warp range (V <= 262144)
@@ -71,20 +71,38 @@ struct FsShared {
 
 constexpr uint32_t FS_OVER = 8u;             // a weight beyond the bins (hand back)
 
-__device__ __forceinline__ float4 fs_ld(const float4* p) {
+// Streaming load with an L2 eviction policy: rows that are read again (a top-p
+// row's refinement passes, a full-row sampling pass) stay in L2 ahead of rows
+// read once.
+__device__ __forceinline__ float4 fs_ld(const float4* p, uint64_t pol) {
   float4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return v;
 }
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ float4 fs_ld_l2(const float4* p) { return __ldcg(p); }
+// Asks L2 to fetch bytes [p, p + n) of global memory (16-byte aligned, n a
+// multiple of 16), in 32 KB pieces spread over the calling warp's lanes.
+__device__ __forceinline__ void fs_prefetch_l2(const void* p, size_t n) {
+  const char* c = static_cast<const char*>(p);
+  for (size_t off = (size_t)lane_id() * 32768u; off < n; off += 32u * 32768u) {
+    const uint32_t sz = (uint32_t)min((size_t)32768u, n - off);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(sz) : "memory");
+  }
+}
+
 __device__ __forceinline__ float fs_at(const float4& v, int e) {
   return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
 }
 // Coarse bin of a weight e = 2^x (x relative to the first-wave maximum): FB_TOP
-// minus e's exponent field, so bin j holds x in [15 - j, 16 - j); x >= 16 is out
-// of range (*over), everything below the last bin's binade joins it.
+// minus e's exponent field, so bin j holds x in [23 - j, 24 - j); x >= 24 is out
+// of range (*over), everything below the last bin's binade (x < -23) joins it.
 __device__ __forceinline__ int fs_bin(float e, uint32_t* over) {
   const int b = FB_TOP - (int)(__float_as_uint(e) >> 23);
   if (b < 0) *over = 1u;
@@ -137,6 +155,58 @@ __device__ __noinline__ uint32_t fs_kth_key(uint32_t key, int k, FsShared& S) {
     kk = S.hsel[1];
     __syncthreads();
   }
+  return prefix;
+}
+
+// Value key (upper 32 bits) of the k-th largest of the n composites a[0, n)
+// (k <= n), by four rounds of 8-bit digits over the list. Every thread returns it.
+__device__ __noinline__ uint32_t fs_kth_listed(const unsigned long long* a, int n, int k, FsShared& S) {
+  const int tid = threadIdx.x, l = lane_id();
+  uint32_t prefix = 0u, pmask = 0u;
+  uint32_t kk = (uint32_t)k;
+  for (int r = 0; r < 4; ++r) {
+    const int sh = 24 - 8 * r;
+    __syncthreads();
+    for (int i = tid; i < 256; i += FT) S.dh[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += FT) {
+      const uint32_t key = (uint32_t)(a[i] >> 32);
+      if ((key & pmask) == prefix) atomicAdd(&S.dh[(key >> sh) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      uint32_t c8[8], s = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c8[j] = S.dh[255 - 8 * l - j];
+        s += c8[j];
+      }
+      uint32_t incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (l >= o) incl += t;
+      }
+      const uint32_t excl = incl - s;
+      if (excl < kk && kk <= incl) {
+        uint32_t run = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run + c8[j] >= kk) {
+            S.hsel[0] = (uint32_t)(255 - 8 * l - j);
+            S.hsel[1] = kk - run;
+            break;
+          }
+          run += c8[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= S.hsel[0] << sh;
+    pmask |= 255u << sh;
+    kk = S.hsel[1];
+  }
+  __syncthreads();
   return prefix;
 }
 
@@ -193,12 +263,15 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
                                         unsigned long long* list, float* bins, float* thr, float* mt,
                                         float* st, float* Rout, bool* nan) {
   const int tid = threadIdx.x, l = lane_id();
+  // top-k rows are read once (their kept tokens are listed); the others are read
+  // again by refinement or sampling passes
+  const uint64_t pol = CLS == FC_TOPK ? policy_evict_first() : policy_evict_last();
   float4 cur[FPF], nxt[FPF];
   const float4 NEG = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
   for (int p = 0; p < FPF; ++p) {
     const int q = tid + p * FT;
-    cur[p] = q < nv ? fs_ld(src + q) : NEG;
+    cur[p] = q < nv ? fs_ld(src + q, pol) : NEG;
   }
   float tmax = -INFINITY;
   bool bad = false;
@@ -210,6 +283,12 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
       tmax = fmaxf(tmax, z);
       bad |= !(z == z) || z == INFINITY;
     }
+  // the second wave is in flight while the block agrees on R and the threshold
+#pragma unroll
+  for (int p = 0; p < FPF; ++p) {
+    const int q = tid + FPF * FT + p * FT;
+    nxt[p] = q < nv ? fs_ld(src + q, pol) : NEG;
+  }
   // first-wave block maximum R; top-k threshold: k-th largest thread maximum
   float fm = tmax;
 #pragma unroll
@@ -232,11 +311,6 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
   float m_t = -INFINITY, s_t = 0.0f;
   uint32_t over = 0u;
   for (int q0 = tid; q0 < nv; q0 += FPF * FT) {
-#pragma unroll
-    for (int p = 0; p < FPF; ++p) {
-      const int q = q0 + FPF * FT + p * FT;
-      nxt[p] = q < nv ? fs_ld(src + q) : NEG;
-    }
 #pragma unroll
     for (int p = 0; p < FPF; ++p) {
       const int q = q0 + p * FT;
@@ -266,6 +340,11 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
     }
 #pragma unroll
     for (int p = 0; p < FPF; ++p) cur[p] = nxt[p];
+#pragma unroll
+    for (int p = 0; p < FPF; ++p) {
+      const int q = q0 + 2 * FPF * FT + p * FT;
+      nxt[p] = q < nv ? fs_ld(src + q, pol) : NEG;
+    }
   }
   if (over) atomicOr(&S.rflags, FS_OVER);
   *mt = m_t;
@@ -275,11 +354,13 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
 }
 
 // Second and third passes of a top-p row (from L2): sub-bin histogram of coarse
-// bin j (PASS 2), or the list of sub-bin s of bin j (PASS 3).
+// bin j with the bin's logits listed (PASS 2), or the list of sub-bin s of bin j
+// (PASS 3). List slots are taken per warp; nothing is written past FLCAP.
 template <int PASS>
 __device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float nRc, float scale, int j,
                                        int s, FsShared& S, unsigned long long* list) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, l = lane_id();
+  const uint32_t below = (1u << l) - 1u;
   float4 cur[FPF], nxt[FPF];
   const float4 NEG = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   uint32_t over = 0u;
@@ -288,7 +369,9 @@ __device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float
     const int q = tid + p * FT;
     cur[p] = q < nv ? fs_ld_l2(src + q) : NEG;
   }
-  for (int q0 = tid; q0 < nv; q0 += FPF * FT) {
+  // warp-uniform trip count (the ballots below need every lane)
+  for (int qb = tid - l; qb < nv; qb += FPF * FT) {
+    const int q0 = qb + l;
 #pragma unroll
     for (int p = 0; p < FPF; ++p) {
       const int q = q0 + FPF * FT + p * FT;
@@ -297,19 +380,25 @@ __device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float
 #pragma unroll
     for (int p = 0; p < FPF; ++p) {
       const int q = q0 + p * FT;
-      if (q >= nv) continue;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float z = fs_at(cur[p], e);
         const float w = ex2_approx(fmaf(z, c, nRc));
-        if (fs_bin(w, &over) != j) continue;
+        const bool inb = q < nv && fs_bin(w, &over) == j;
         const int sb = (int)((__float_as_uint(w) >> 15) & 255u);
-        if (PASS == 2) {
+        if (PASS == 2 && inb) {
           atomicAdd(&S.dh[sb], 1u);
           atomicAdd(&S.smass[sb], fix_pow2(w * scale, FIX));
-        } else if (sb == s) {
-          const uint32_t slot = atomicAdd(&S.lcount, 1u);
-          if (slot < (uint32_t)FLCAP)
+        }
+        const bool want = PASS == 2 ? inb : (inb && sb == s);
+        const uint32_t mk = __ballot_sync(0xffffffffu, want);
+        if (mk) {
+          const int ld = __ffs(mk) - 1;
+          uint32_t base = 0u;
+          if (l == ld) base = atomicAdd(&S.lcount, (uint32_t)__popc(mk));
+          base = __shfl_sync(0xffffffffu, base, ld);
+          const uint32_t slot = base + (uint32_t)__popc(mk & below);
+          if (want && slot < (uint32_t)FLCAP)
             list[slot] = ((unsigned long long)okey(z) << 32) | (uint32_t)~(uint32_t)(4 * q + e);
         }
       }
@@ -372,6 +461,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
 #pragma unroll
   for (int i = 1; i < KWARP; ++i) m = fmaxf(m, S.fmax[i]);
   res.m = m;
+  KH_MARK(S.item, 1);
   if (anynan || !(m > -INFINITY)) {
     res.flags = KH_ERR;
     return res;
@@ -395,9 +485,42 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
       res.flags = KH_BAIL;
       return res;
     }
-    const int n2 = fs_pow2((int)nl);
-    for (int i = (int)nl + tid; i < n2; i += FT) list[i] = 0ull;
-    fs_sort_desc(list, n2);
+    // the k-th largest logit key; the candidates at or above it (the top k plus any
+    // further ties of that key) ranked by composite key: rank < k is the top k
+    const uint32_t kth = fs_kth_listed(list, (int)nl, k, S);
+    KH_MARK(S.item, 2);
+    unsigned long long* cand = list + FLCAP;
+    if (tid == 0) S.ncut = 0;
+    __syncthreads();
+    for (int i = tid; i < (int)nl; i += FT) {
+      const unsigned long long e = list[i];
+      if ((uint32_t)(e >> 32) >= kth) {
+        const uint32_t slot = atomicAdd((uint32_t*)&S.ncut, 1u);
+        if (slot < (uint32_t)FLCAP) cand[slot] = e;
+      }
+    }
+    __syncthreads();
+    const int nc = S.ncut;
+    if (nc > FLCAP) {
+      res.flags = KH_BAIL;
+      return res;
+    }
+    if (nc <= 1024) {
+      // rank by counting (composite keys are distinct)
+      for (int i = tid; i < nc; i += FT) {
+        const unsigned long long e = cand[i];
+        int rank = 0;
+        for (int j = 0; j < nc; ++j) rank += (int)(cand[j] > e);
+        if (rank < k) list[rank] = e;
+      }
+    } else {
+      // many ties of the k-th key: sort the candidates
+      const int n2 = fs_pow2(nc);
+      for (int i = nc + tid; i < n2; i += FT) cand[i] = 0ull;
+      fs_sort_desc(cand, n2);
+      for (int i = tid; i < k; i += FT) list[i] = cand[i];
+    }
+    __syncthreads();
     // the top k in order; their exact fixed-point weights and exclusive sums
     unsigned long long wk = 0ull;
     if (tid < k) wk = fix_pow2(kh_w(fs_key_value(list[tid]), m, c), FIX);
@@ -448,29 +571,32 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
       res.flags = KH_BAIL;
       return res;
     }
-    // sub-bins of bin js (counts, exact masses) from L2
+    // sub-bins of bin js (counts, exact masses) from L2; the bin's logits listed
     __syncthreads();
     for (int i = tid; i < FNSUB; i += FT) {
       S.dh[i] = 0u;
       S.smass[i] = 0ull;
     }
+    if (tid == 0) S.lcount = 0u;
     __syncthreads();
     const float nRc = -(R * c);
     fs_refine<2>(src, nv, c, nRc, scale, js, 0, S, list);
     __syncthreads();
+    KH_MARK(S.item, 2);
     if (tid == 0) {
       int ss = -1;
       unsigned long long cum = above;
       for (int sb = FNSUB - 1; sb >= 0; --sb) {
-        if (cum + S.smass[sb] > Y) {
+        const unsigned long long sm = S.smass[sb];
+        if (cum + sm > Y) {
           ss = sb;
           break;
         }
-        cum += S.smass[sb];
+        cum += sm;
       }
       S.sstar = ss;
       S.mabove = cum;
-      S.lcount = 0u;
+      S.ncut = 0;
     }
     __syncthreads();
     const int ss = S.sstar;
@@ -478,29 +604,62 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
       res.flags = KH_BAIL;                   // rounding left the crossing outside the bin
       return res;
     }
-    fs_refine<3>(src, nv, c, nRc, scale, js, ss, S, list);
-    __syncthreads();
-    const uint32_t nl = S.lcount;
+    const uint32_t nbin = S.lcount;
+    uint32_t nl;
+    unsigned long long* sel = list;
+    if (nbin <= (uint32_t)FLCAP) {
+      // the crossing sub-bin's entries of the listed bin
+      sel = list + FLCAP;
+      for (int i = tid; i < (int)nbin; i += FT) {
+        const unsigned long long e = list[i];
+        const float wv = ex2_approx(fmaf(fs_key_value(e), c, nRc));
+        if ((int)((__float_as_uint(wv) >> 15) & 255u) == ss) sel[atomicAdd((uint32_t*)&S.ncut, 1u)] = e;
+      }
+      __syncthreads();
+      nl = (uint32_t)S.ncut;
+    } else {
+      // too many to list: list the crossing sub-bin in a third pass
+      __syncthreads();
+      if (tid == 0) S.lcount = 0u;
+      __syncthreads();
+      fs_refine<3>(src, nv, c, nRc, scale, js, ss, S, list);
+      __syncthreads();
+      nl = S.lcount;
+    }
     if (nl > (uint32_t)FLCAP || nl == 0u) {
       res.flags = KH_BAIL;
       return res;
     }
     const int n2 = fs_pow2((int)nl);
-    for (int i = (int)nl + tid; i < n2; i += FT) list[i] = 0ull;
-    fs_sort_desc(list, n2);
-    // walk the sorted entries: kept while the exclusive mass <= Y (a prefix, at
-    // least the first entry); their weights as the sub-bin masses summed them
-    if (tid == 0) {
-      unsigned long long ex = S.mabove;
-      int last = 0;
-      for (int i = 0; i < (int)nl; ++i) {
-        if (ex > Y) break;
-        last = i;
-        ex += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
-      }
+    for (int i = (int)nl + tid; i < n2; i += FT) sel[i] = 0ull;
+    fs_sort_desc(sel, n2);
+    list = sel;
+    KH_MARK(S.item, 3);
+    // the sorted entries are kept while their exclusive mass is <= Y (a prefix, at
+    // least the first entry); their weights as the sub-bin masses summed them.
+    // Thread t takes entries [t e, t e + e) in order; a scan gives its offset.
+    const int ept = ((int)nl + FT - 1) / FT;
+    const int i0 = min(tid * ept, (int)nl), i1 = min(i0 + ept, (int)nl);
+    unsigned long long own = 0ull;
+    for (int i = i0; i < i1; ++i) own += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
+    if (tid == 0) S.jstar = 0;
+    unsigned long long wtot;
+    unsigned long long ex = S.mabove + kh_below<unsigned long long>(own, S.s64, &wtot);
+    int lastk = -1;
+    unsigned long long zk = 0ull;
+    for (int i = i0; i < i1; ++i) {
+      if (ex > Y) break;
+      lastk = i;
+      ex += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
+      zk = ex;
+    }
+    if (lastk > 0) atomicMax(&S.jstar, lastk);
+    __syncthreads();
+    const int last = S.jstar;
+    if (lastk == last) {
       S.zt = fs_key_value(list[last]);
       S.idcut = fs_key_id(list[last]);
-      S.zkept = ex;
+      S.zkept = zk;
     }
     __syncthreads();
     res.zt = S.zt;
@@ -520,63 +679,62 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
   return res;
 }
 
-// Fixed-point (2^-40) residual and target masses of the 4 tokens of vector v.
-__device__ __forceinline__ void fs_vec(const float4* sp, const float4* sq, int v, bool paired, const KhW& tp,
-                                       const KhW& tq, unsigned long long* R, unsigned long long* Pm) {
-  const float4 a = __ldcg(sp + v);
-  const float4 b = paired ? __ldcg(sq + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  unsigned long long ra = 0, pa = 0;
+// Fixed-point (2^-40) mass of the 4 tokens of vector v: the residual (p - q)+
+// (RES; target logits a, draft logits b) or the target probability p.
+template <bool RES>
+__device__ __forceinline__ unsigned long long fs_vec_mass(const float4& a, const float4& b, int v, const KhW& tp,
+                                                          const KhW& tq) {
+  unsigned long long acc = 0;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     float r, p;
-    kh_elem(fs_at(a, e), fs_at(b, e), 4 * v + e, paired, tp, tq, &r, &p);
-    ra += fixr(r);
-    pa += fixr(p);
+    kh_elem(fs_at(a, e), fs_at(b, e), 4 * v + e, RES, tp, tq, &r, &p);
+    acc += fixr(RES ? r : p);
   }
-  *R = ra;
-  *Pm = pa;
+  return acc;
 }
 
-// Inverse CDF in token-id order over (p - q)+ (paired) or p, over whole fp32 rows
-// (from L2): the smallest id j whose running sum S_j satisfies S_j * 2^24 > kv * S
-// (S the total); when the residual mass is 0 the target p is used. Warps sum
-// contiguous ranges per 32-vector block; warp 0 locates the crossing block with
-// lane-parallel scans and walks it. -1 if no token qualifies.
-__device__ __noinline__ int fs_sample_full(const float4* sp, const float4* sq, int nv, bool paired, KhW tp,
-                                           KhW tq, uint32_t kv, FsShared& S) {
+// One inverse-CDF pass over whole fp32 rows (from L2) for the residual (RES) or
+// the target p: the smallest id j whose running mass S_j satisfies
+// S_j * 2^24 > kv * S (S the total). Warps sum contiguous ranges per 32-vector
+// block; warp 0 locates the crossing block with lane-parallel scans and walks it.
+// -1 if no token qualifies, -2 if the total mass is 0.
+template <bool RES>
+__device__ __noinline__ int fs_sample_pass(const float4* sp, const float4* sq, int nv, KhW tp, KhW tq, uint32_t kv,
+                                           FsShared& S) {
   const int w = warp_id(), l = lane_id();
   const int cw = (nv + FWARP - 1) / FWARP;
   const int nb = (cw + 31) / 32;
   const int a0 = min(w * cw, nv), a1 = min(a0 + cw, nv);
-  unsigned long long* bR = reinterpret_cast<unsigned long long*>(kh_dyn);
-  unsigned long long* bP = bR + FWARP * FMAXBLK;
-  unsigned long long tR = 0, tP = 0;
-  for (int j = 0; j < nb; ++j) {
-    const int v = a0 + j * 32 + l;
-    unsigned long long r = 0, p = 0;
-    if (v < a1) fs_vec(sp, sq, v, paired, tp, tq, &r, &p);
-    p = kh_wsum(p);
-    r = paired ? kh_wsum(r) : p;
-    if (l == 0) {
-      bR[w * FMAXBLK + j] = r;
-      bP[w * FMAXBLK + j] = p;
+  unsigned long long* bm = reinterpret_cast<unsigned long long*>(kh_dyn);
+  const float4 NEG = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  unsigned long long tot = 0;
+  constexpr int U = 4;                         // blocks whose vectors are in flight at once
+  for (int j0 = 0; j0 < nb; j0 += U) {
+    float4 av[U], bv4[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = a0 + (j0 + u) * 32 + l;
+      const bool in = j0 + u < nb && v < a1;
+      av[u] = in ? __ldcg(sp + v) : NEG;
+      bv4[u] = in && RES ? __ldcg(sq + v) : NEG;
     }
-    tR += r;
-    tP += p;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (j0 + u >= nb) break;
+      const int v = a0 + (j0 + u) * 32 + l;
+      unsigned long long x = v < a1 ? fs_vec_mass<RES>(av[u], bv4[u], v, tp, tq) : 0ull;
+      x = kh_wsum(x);
+      if (l == 0) bm[w * FMAXBLK + j0 + u] = x;
+      tot += x;
+    }
   }
   __syncthreads();
-  if (l == 0) {
-    S.s64[w] = tR;
-    S.s64b[w] = tP;
-  }
+  if (l == 0) S.s64[w] = tot;
   __syncthreads();
   if (w == 0) {
-    const unsigned long long oR = l < FWARP ? S.s64[l] : 0ull, oP = l < FWARP ? S.s64b[l] : 0ull;
-    const unsigned long long SR = warp_sum(oR), SP = warp_sum(oP);
-    const bool useR = SR > 0ull;
-    const unsigned long long St = useR ? SR : SP;
-    const unsigned long long* bv = useR ? bR : bP;
-    const unsigned long long own = useR ? oR : oP;
+    const unsigned long long own = l < FWARP ? S.s64[l] : 0ull;
+    const unsigned long long St = warp_sum(own);
     unsigned long long incl = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -584,8 +742,8 @@ __device__ __noinline__ int fs_sample_full(const float4* sp, const float4* sq, i
       if (l >= o) incl += t;
     }
     const uint32_t bw = __ballot_sync(0xffffffffu, l < FWARP && mul_gt(incl, 1ull << 24, kv, St));
-    int tok = -1;
-    if (bw) {
+    int tok = St == 0ull ? -2 : -1;
+    if (St != 0ull && bw) {
       const int ww = __ffs(bw) - 1;
       unsigned long long acc = __shfl_sync(0xffffffffu, incl - own, ww);
       const int wa0 = min(ww * cw, nv), wa1 = min(wa0 + cw, nv);
@@ -593,7 +751,7 @@ __device__ __noinline__ int fs_sample_full(const float4* sp, const float4* sq, i
       unsigned long long b4[4], bs = 0;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        b4[u] = 4 * l + u < nb ? bv[ww * FMAXBLK + 4 * l + u] : 0ull;
+        b4[u] = 4 * l + u < nb ? bm[ww * FMAXBLK + 4 * l + u] : 0ull;
         bs += b4[u];
       }
       unsigned long long bi = bs;
@@ -617,9 +775,12 @@ __device__ __noinline__ int fs_sample_full(const float4* sp, const float4* sq, i
         }
         // the block: one vector per lane, in id order
         const int v = wa0 + jb * 32 + l;
-        unsigned long long r = 0, p = 0;
-        if (v < wa1) fs_vec(sp, sq, v, paired, tp, tq, &r, &p);
-        const unsigned long long mine = useR ? r : p;
+        float4 a = NEG, bq = NEG;
+        if (v < wa1) {
+          a = __ldcg(sp + v);
+          if (RES) bq = __ldcg(sq + v);
+        }
+        const unsigned long long mine = v < wa1 ? fs_vec_mass<RES>(a, bq, v, tp, tq) : 0ull;
         unsigned long long ci = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -628,13 +789,11 @@ __device__ __noinline__ int fs_sample_full(const float4* sp, const float4* sq, i
         }
         const uint32_t hit = __ballot_sync(0xffffffffu, v < wa1 && mul_gt(acc + ci, 1ull << 24, kv, St));
         if (hit && l == __ffs(hit) - 1) {
-          const float4 a = __ldcg(sp + v);
-          const float4 bq = paired ? __ldcg(sq + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           unsigned long long run = acc + ci - mine;
           for (int e = 0; e < 4 && tok < 0; ++e) {
             float rr, pp;
-            kh_elem(fs_at(a, e), fs_at(bq, e), 4 * v + e, paired, tp, tq, &rr, &pp);
-            run += fixr(useR ? rr : pp);
+            kh_elem(fs_at(a, e), fs_at(bq, e), 4 * v + e, RES, tp, tq, &rr, &pp);
+            run += fixr(RES ? rr : pp);
             if (mul_gt(run, 1ull << 24, kv, St)) tok = 4 * v + e;
           }
         }
@@ -645,6 +804,20 @@ __device__ __noinline__ int fs_sample_full(const float4* sp, const float4* sq, i
   }
   __syncthreads();
   return S.tok;
+}
+
+// Inverse CDF in token-id order over (p - q)+ (paired) or p, over whole fp32 rows:
+// when the residual mass is 0 the target p is used. -1 if no token qualifies.
+__device__ __noinline__ int fs_sample_full(const float4* sp, const float4* sq, int nv, bool paired, KhW tp,
+                                           KhW tq, uint32_t kv, FsShared& S) {
+  if (warp_id() == 0) {
+    // both rows were streamed a while ago: fetch them back at full width
+    fs_prefetch_l2(sp, (size_t)nv * 16u);
+    if (paired) fs_prefetch_l2(sq, (size_t)nv * 16u);
+  }
+  int tok = paired ? fs_sample_pass<true>(sp, sq, nv, tp, tq, kv, S) : -2;
+  if (tok == -2) tok = fs_sample_pass<false>(sp, sq, nv, tp, tq, kv, S);
+  return tok < 0 ? -1 : tok;
 }
 
 // The inverse CDF of fs_sample_full over a target row whose kept tokens are
@@ -705,6 +878,7 @@ __device__ __noinline__ void fs_finalize(const Params& P, int b, FsShared& S) {
   const KhRow* rr = P.ws_rowres + (size_t)b * R2;
   const float* tgt = static_cast<const float*>(P.rows0) + (size_t)b * (K + 1) * P.V;
   const float* drf = static_cast<const float*>(P.rows1) + (size_t)b * K * P.V;
+  KF_MARK(b, 0);
   if (tid < 32) {
     uint32_t f = 0;
     for (int r = tid; r < R2; r += 32) f |= __ldcg(&rr[r].flags);
@@ -757,6 +931,9 @@ __device__ __noinline__ void fs_finalize(const Params& P, int b, FsShared& S) {
     const float* zp = tgt + (size_t)n * P.V;
     const float* zq = paired ? drf + (size_t)n * P.V : zp;
     const uint32_t L = tp.pad[1];
+    KF_MARK(b, 1);
+    KF_SET(b, 4, L != KH_NOLIST ? 1ull : 0ull);
+    KF_SET(b, 5, (unsigned long long)n);
     if (L != KH_NOLIST) {
       tok = fs_sample_list(zp, zq, P.ws_lists + ((size_t)b * (K + 1) + n) * KH_KCAP, (int)L, paired,
                            kh_wof(tp), kh_wof(tq), kv, S);
@@ -764,6 +941,7 @@ __device__ __noinline__ void fs_finalize(const Params& P, int b, FsShared& S) {
       tok = fs_sample_full(reinterpret_cast<const float4*>(zp), reinterpret_cast<const float4*>(zq), P.V / 4,
                            paired, kh_wof(tp), kh_wof(tq), kv, S);
     }
+    KF_MARK(b, 2);
   }
   if (tid == 0) {
     const bool bad = (flags & KH_ERR) || tok < 0;
@@ -802,7 +980,18 @@ __global__ void __launch_bounds__(FT, 2) fstream_kernel(const Params P, int nite
     const int pos = target ? r : r - K - 1;
     const int d = pos < K ? P.dtok[(size_t)b * K + pos] : -1;
     uint32_t* glist = target ? P.ws_lists + ((size_t)b * (K + 1) + r) * KH_KCAP : nullptr;
+    KH_MARK(item, 0);
     const KhRow res = fs_row(row, P.V, P.temp[b], P.topk[b], P.topp[b], d, glist, S);
+    KH_MARK(item, 4);
+#ifdef SV_TRACE
+    if (tid == 0 && item < 8192) {
+      uint32_t smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      const int k = P.topk[b];
+      const int cls = (k > 0 && k < P.V) ? FC_TOPK : (P.topp[b] < 1.0f ? FC_TOPP : FC_ALL);
+      g_khtrace[item * 8 + 7] = smid | ((unsigned long long)cls << 16) | ((unsigned long long)res.flags << 20);
+    }
+#endif
     if (tid == 0) {
       uint4* dst = reinterpret_cast<uint4*>(P.ws_rowres + item);
       // a draft row never keeps a list: the sampling list is the target row's
@@ -815,7 +1004,11 @@ __global__ void __launch_bounds__(FT, 2) fstream_kernel(const Params P, int nite
       if (S.last) __threadfence();
     }
     __syncthreads();
-    if (S.last) fs_finalize(P, b, S);
+    if (S.last) {
+      KH_MARK(item, 5);
+      fs_finalize(P, b, S);
+      KH_MARK(item, 6);
+    }
     __syncthreads();
   }
   // finish only after greedy_kernel (launched before, possibly still running)

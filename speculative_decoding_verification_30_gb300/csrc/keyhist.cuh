@@ -48,10 +48,10 @@ constexpr float KH_LIST_BITS = 12.0f;                     // listed: weight >= 2
 #ifdef SV_TRACE
 // Phase timestamps per row item (trace builds): 0 fetched, 1 streamed, 2 swept,
 // 3 cut found, 4 row done, 5 finalize start, 6 finalize end, 7 SM id.
-__device__ unsigned long long g_khtrace[4096 * 8];
+__device__ unsigned long long g_khtrace[8192 * 8];
 #define KH_MARK(item, k)                                                   \
   do {                                                                     \
-    if (threadIdx.x == 0 && (item) >= 0 && (item) < 4096) g_khtrace[(item) * 8 + (k)] = global_timer_ns(); \
+    if (threadIdx.x == 0 && (item) >= 0 && (item) < 8192) g_khtrace[(item) * 8 + (k)] = global_timer_ns(); \
   } while (0)
 // Per-sequence finalize timestamps: 0 start, 1 acceptance done, 2 first sampling
 // pass done, 3 end; 4 = redo, 5 = n.
@@ -1333,7 +1333,7 @@ __global__ void __launch_bounds__(KT, 2) keyhist_kernel(const Params P, int nite
     if (!fast_seq(P, b)) continue;
     KH_MARK(item, 0);
 #ifdef SV_TRACE
-    if (tid == 0 && item < 4096) {
+    if (tid == 0 && item < 8192) {
       uint32_t smid;
       asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
       g_khtrace[item * 8 + 7] = smid;

@@ -2445,7 +2445,7 @@ int sv_trace_reset(void) {
   return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
 }
 int kh_trace_reset(void) {
-  static unsigned long long zero[4096 * 8];
+  static unsigned long long zero[8192 * 8];
   if (cudaMemcpyToSymbol(g_khtrace, zero, sizeof(zero)) != cudaSuccess) return 1;
   if (cudaMemcpyToSymbol(g_khheavy, zero, sizeof(unsigned long long)) != cudaSuccess) return 1;
   return cudaMemcpyToSymbol(g_kftrace, zero, 1024 * 8 * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
@@ -2460,7 +2460,7 @@ int kf_trace_copy(unsigned long long* host, size_t n) {
   return cudaMemcpyFromSymbol(host, g_kftrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
 }
 int kh_trace_copy(unsigned long long* host, size_t n) {
-  if (n > 4096 * 8) n = 4096 * 8;
+  if (n > 8192 * 8) n = 8192 * 8;
   return cudaMemcpyFromSymbol(host, g_khtrace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
 }
 int sv_trace_copy(unsigned long long* host, size_t n) {

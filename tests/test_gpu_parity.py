@@ -246,6 +246,30 @@ def test_verify_edge_shapes(dtype, V, K):
     assert not rep.bad_mismatches, rep.bad_mismatches
 
 
+def test_verify_top_k_with_many_ties_at_the_kth_logit():
+    # fp32 rows whose k-th largest logit is shared by hundreds or thousands of
+    # tokens: the kept set is split by token id (ties ranked by ascending id)
+    V, K, B = 8192, 2, 8
+    g = torch.Generator().manual_seed(77)
+    tgt = torch.randn(B, K + 1, V, generator=g) - 6.0
+    drf = torch.randn(B, K, V, generator=g) - 6.0
+    for s in range(B):
+        ties = [3000, 500, 3000, 40, 1500, 700, 3000, 4000][s]
+        idx = torch.randperm(V, generator=g)
+        tgt[s, :, idx[:50]] = 2.0 + torch.rand(K + 1, 50, generator=g)
+        tgt[s, :, idx[50:50 + ties]] = 1.0
+        drf[s, :, idx[:50 + ties]] = 1.5
+    dtok = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    T = torch.tensor([1.0, 0.7, 1.0, 1.2, 0.9, 1.0, 2.0, 1.0])
+    k = torch.tensor([60, 60, 45, 80, 200, 256, 120, 100], dtype=torch.int32)
+    P = torch.tensor([1.0, 1.0, 1.0, 0.9, 0.6, 1.0, 0.95, 1.0])
+    out, n = sv.spec_verify(tgt.to(DEV), drf.to(DEV), dtok.to(DEV), T.to(DEV), k.to(DEV),
+                            P.to(DEV), seed=8, offset=3)
+    res = oracle_verify(tgt, drf, dtok, T, k, P, 8, 3, parallel=False)
+    rep = compare(out.cpu(), n.cpu(), res, T)
+    assert not rep.bad_mismatches, rep.bad_mismatches
+
+
 def test_data_errors_are_reported_in_band():
     V, K, B = 64, 2, 9
     tgt = torch.randn(B, K + 1, V)
