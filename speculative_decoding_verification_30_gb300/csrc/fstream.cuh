@@ -43,6 +43,7 @@ constexpr int FNB = 48;                      // coarse weight bins (one binade e
 constexpr int FB_TOP = 150;                  // bin = FB_TOP - exponent field of the weight
 constexpr int FNSUB = 256;                   // sub-bins of the crossing bin
 constexpr int FKMAX = 256;                   // largest top_k served here
+constexpr int FOCAP = 256;                   // top-p logits above the bins (u64 composite keys)
 constexpr int FMAXBLK = 128;                 // 32-vector blocks per warp range (V <= 262144)
 constexpr size_t FS_SMEM = (size_t)FNB * FT * 4;   // bins | list | sampling block sums
 
@@ -67,8 +68,21 @@ struct FsShared {
   float zt;
   int idcut;
   unsigned long long zkept;
+  uint32_t ocount;                           // logits above the bins (top-p rows)
+  unsigned long long olist[FOCAP];
 };
 
+#ifdef SV_TRACE
+// trace builds: which hand-back a row took (bits 28..31 of its trace word)
+#define FS_WHY(code)                                                                    \
+  do {                                                                                  \
+    if (threadIdx.x == 0 && S.item < 8192) g_khtrace[S.item * 8 + 7] |= (unsigned long long)(code) << 28; \
+  } while (0)
+#else
+#define FS_WHY(code) \
+  do {               \
+  } while (0)
+#endif
 constexpr uint32_t FS_OVER = 8u;             // a weight beyond the bins (hand back)
 
 // Streaming load with an L2 eviction policy: rows that are read again (a top-p
@@ -298,6 +312,7 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
     S.cmax = okey(-INFINITY);
     S.lcount = 0u;
     S.rflags = 0u;
+    S.ocount = 0u;
   }
   __syncthreads();
   if (l == 0) atomicMax(&S.cmax, okey(fm));
@@ -332,9 +347,20 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float w = ex2_approx(fmaf(fs_at(x, e), c, nRc));
-          float* b = bins + fs_bin(w, &over) * FT + tid;
-          *b += w;
+          const float z = fs_at(x, e);
+          const float w = ex2_approx(fmaf(z, c, nRc));
+          const int bb = FB_TOP - (int)(__float_as_uint(w) >> 23);
+          if (bb >= 0) {
+            bins[min(bb, FNB - 1) * FT + tid] += w;
+          } else {
+            // above the bins (2^24 or more times the first-wave maximum's weight):
+            // listed, their masses are taken exactly after the stream
+            const uint32_t slot = atomicAdd(&S.ocount, 1u);
+            if (slot < (uint32_t)FOCAP)
+              S.olist[slot] = ((unsigned long long)okey(z) << 32) | (uint32_t)~(uint32_t)(4 * q + e);
+            else
+              over = 1u;
+          }
         }
       }
     }
@@ -384,7 +410,8 @@ __device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float
       for (int e = 0; e < 4; ++e) {
         const float z = fs_at(cur[p], e);
         const float w = ex2_approx(fmaf(z, c, nRc));
-        const bool inb = q < nv && fs_bin(w, &over) == j;
+        // bin j < FNB - 1 exactly (the listed logits above the bins excluded)
+        const bool inb = q < nv && FB_TOP - (int)(__float_as_uint(w) >> 23) == j;
         const int sb = (int)((__float_as_uint(w) >> 15) & 255u);
         if (PASS == 2 && inb) {
           atomicAdd(&S.dh[sb], 1u);
@@ -440,6 +467,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
   if (topk && k > FKMAX) {
     res.m = 0.0f;
     res.flags = KH_BAIL;
+    FS_WHY(1);
     return res;
   }
   if (cls == FC_TOPP) {
@@ -468,6 +496,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
   }
   if (S.rflags & FS_OVER) {
     res.flags = KH_BAIL;
+    FS_WHY(2);
     return res;
   }
   unsigned long long Zk = 0ull;
@@ -483,6 +512,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
     const uint32_t nl = S.lcount;
     if (nl > (uint32_t)FLCAP || nl < (uint32_t)k) {
       res.flags = KH_BAIL;
+      FS_WHY(3);
       return res;
     }
     // the k-th largest logit key; the candidates at or above it (the top k plus any
@@ -503,6 +533,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
     const int nc = S.ncut;
     if (nc > FLCAP) {
       res.flags = KH_BAIL;
+      FS_WHY(4);
       return res;
     }
     if (nc <= 1024) {
@@ -554,120 +585,149 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
       if (l == 0) S.binm[j] = t;
     }
     __syncthreads();
-    unsigned long long Z = 0ull;
+    // the logits above the bins, sorted, with exact masses in the frame of m
+    const int no = (int)S.ocount;            // <= FOCAP (more were handed back)
+    unsigned long long om = 0ull;
+    if (no > 0) {
+      const int n2 = fs_pow2(no);
+      for (int i = no + tid; i < n2; i += FT) S.olist[i] = 0ull;
+      fs_sort_desc(S.olist, n2);
+      if (tid < no) om = fix_pow2(kh_w(fs_key_value(S.olist[tid]), m, c), FIX);
+    }
+    unsigned long long OZ;
+    const unsigned long long oex = kh_below<unsigned long long>(om, S.s64, &OZ);
+    unsigned long long Z = OZ;
     for (int j = 0; j < FNB; ++j) Z += S.binm[j];
     const unsigned long long Y = mass_threshold(topP, Z);
-    // the bin where the exclusive mass first exceeds Y
-    int js = -1;
-    unsigned long long above = 0ull;
-    for (int j = 0; j < FNB; ++j) {
-      if (above + S.binm[j] > Y) {
-        js = j;
-        break;
+    if (OZ > Y) {
+      // the cut lies among them: kept while the exclusive mass is <= Y
+      const int nk = __syncthreads_count(tid < no && oex <= Y);
+      if (tid == nk - 1) {
+        S.zt = fs_key_value(S.olist[tid]);
+        S.idcut = fs_key_id(S.olist[tid]);
+        S.zkept = oex + om;
       }
-      above += S.binm[j];
-    }
-    if (js < 0 || js == FNB - 1) {
-      res.flags = KH_BAIL;
-      return res;
-    }
-    // sub-bins of bin js (counts, exact masses) from L2; the bin's logits listed
-    __syncthreads();
-    for (int i = tid; i < FNSUB; i += FT) {
-      S.dh[i] = 0u;
-      S.smass[i] = 0ull;
-    }
-    if (tid == 0) S.lcount = 0u;
-    __syncthreads();
-    const float nRc = -(R * c);
-    fs_refine<2>(src, nv, c, nRc, scale, js, 0, S, list);
-    __syncthreads();
-    KH_MARK(S.item, 2);
-    if (tid == 0) {
-      int ss = -1;
-      unsigned long long cum = above;
-      for (int sb = FNSUB - 1; sb >= 0; --sb) {
-        const unsigned long long sm = S.smass[sb];
-        if (cum + sm > Y) {
-          ss = sb;
+      __syncthreads();
+      res.zt = S.zt;
+      res.idcut = S.idcut;
+      Zk = S.zkept;
+    } else {
+      // the bin where the exclusive mass first exceeds Y
+      int js = -1;
+      unsigned long long above = OZ;
+      for (int j = 0; j < FNB; ++j) {
+        if (above + S.binm[j] > Y) {
+          js = j;
           break;
         }
-        cum += sm;
+        above += S.binm[j];
       }
-      S.sstar = ss;
-      S.mabove = cum;
-      S.ncut = 0;
-    }
-    __syncthreads();
-    const int ss = S.sstar;
-    if (ss < 0) {
-      res.flags = KH_BAIL;                   // rounding left the crossing outside the bin
-      return res;
-    }
-    const uint32_t nbin = S.lcount;
-    uint32_t nl;
-    unsigned long long* sel = list;
-    if (nbin <= (uint32_t)FLCAP) {
-      // the crossing sub-bin's entries of the listed bin
-      sel = list + FLCAP;
-      for (int i = tid; i < (int)nbin; i += FT) {
-        const unsigned long long e = list[i];
-        const float wv = ex2_approx(fmaf(fs_key_value(e), c, nRc));
-        if ((int)((__float_as_uint(wv) >> 15) & 255u) == ss) sel[atomicAdd((uint32_t*)&S.ncut, 1u)] = e;
+      if (js < 0 || js == FNB - 1) {
+        res.flags = KH_BAIL;
+        FS_WHY(5);
+        return res;
       }
+      // sub-bins of bin js (counts, exact masses) from L2; the bin's logits listed
       __syncthreads();
-      nl = (uint32_t)S.ncut;
-    } else {
-      // too many to list: list the crossing sub-bin in a third pass
-      __syncthreads();
+      for (int i = tid; i < FNSUB; i += FT) {
+        S.dh[i] = 0u;
+        S.smass[i] = 0ull;
+      }
       if (tid == 0) S.lcount = 0u;
       __syncthreads();
-      fs_refine<3>(src, nv, c, nRc, scale, js, ss, S, list);
+      const float nRc = -(R * c);
+      fs_refine<2>(src, nv, c, nRc, scale, js, 0, S, list);
       __syncthreads();
-      nl = S.lcount;
+      KH_MARK(S.item, 2);
+      if (tid == 0) {
+        int ss = -1;
+        unsigned long long cum = above;
+        for (int sb = FNSUB - 1; sb >= 0; --sb) {
+          const unsigned long long sm = S.smass[sb];
+          if (cum + sm > Y) {
+            ss = sb;
+            break;
+          }
+          cum += sm;
+        }
+        S.sstar = ss;
+        S.mabove = cum;
+        S.ncut = 0;
+      }
+      __syncthreads();
+      const int ss = S.sstar;
+      if (ss < 0) {
+        res.flags = KH_BAIL;                   // rounding left the crossing outside the bin
+        FS_WHY(6);
+        return res;
+      }
+      const uint32_t nbin = S.lcount;
+      uint32_t nl;
+      unsigned long long* sel = list;
+      if (nbin <= (uint32_t)FLCAP) {
+        // the crossing sub-bin's entries of the listed bin
+        sel = list + FLCAP;
+        for (int i = tid; i < (int)nbin; i += FT) {
+          const unsigned long long e = list[i];
+          const float wv = ex2_approx(fmaf(fs_key_value(e), c, nRc));
+          if ((int)((__float_as_uint(wv) >> 15) & 255u) == ss) sel[atomicAdd((uint32_t*)&S.ncut, 1u)] = e;
+        }
+        __syncthreads();
+        nl = (uint32_t)S.ncut;
+      } else {
+        // too many to list: list the crossing sub-bin in a third pass
+        __syncthreads();
+        if (tid == 0) S.lcount = 0u;
+        __syncthreads();
+        fs_refine<3>(src, nv, c, nRc, scale, js, ss, S, list);
+        __syncthreads();
+        nl = S.lcount;
+      }
+      if (nl > (uint32_t)FLCAP || nl == 0u) {
+        res.flags = KH_BAIL;
+        FS_WHY(7);
+        return res;
+      }
+      const int n2 = fs_pow2((int)nl);
+      for (int i = (int)nl + tid; i < n2; i += FT) sel[i] = 0ull;
+      fs_sort_desc(sel, n2);
+      list = sel;
+      KH_MARK(S.item, 3);
+      // the sorted entries are kept while their exclusive mass is <= Y (a prefix, at
+      // least the first entry); their weights as the sub-bin masses summed them.
+      // Thread t takes entries [t e, t e + e) in order; a scan gives its offset.
+      const int ept = ((int)nl + FT - 1) / FT;
+      const int i0 = min(tid * ept, (int)nl), i1 = min(i0 + ept, (int)nl);
+      unsigned long long own = 0ull;
+      for (int i = i0; i < i1; ++i) own += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
+      if (tid == 0) S.jstar = 0;
+      unsigned long long wtot;
+      unsigned long long ex = S.mabove + kh_below<unsigned long long>(own, S.s64, &wtot);
+      int lastk = -1;
+      unsigned long long zk = 0ull;
+      for (int i = i0; i < i1; ++i) {
+        if (ex > Y) break;
+        lastk = i;
+        ex += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
+        zk = ex;
+      }
+      if (lastk > 0) atomicMax(&S.jstar, lastk);
+      __syncthreads();
+      const int last = S.jstar;
+      if (lastk == last) {
+        S.zt = fs_key_value(list[last]);
+        S.idcut = fs_key_id(list[last]);
+        S.zkept = zk;
+      }
+      __syncthreads();
+      res.zt = S.zt;
+      res.idcut = S.idcut;
+      Zk = S.zkept;
     }
-    if (nl > (uint32_t)FLCAP || nl == 0u) {
-      res.flags = KH_BAIL;
-      return res;
-    }
-    const int n2 = fs_pow2((int)nl);
-    for (int i = (int)nl + tid; i < n2; i += FT) sel[i] = 0ull;
-    fs_sort_desc(sel, n2);
-    list = sel;
-    KH_MARK(S.item, 3);
-    // the sorted entries are kept while their exclusive mass is <= Y (a prefix, at
-    // least the first entry); their weights as the sub-bin masses summed them.
-    // Thread t takes entries [t e, t e + e) in order; a scan gives its offset.
-    const int ept = ((int)nl + FT - 1) / FT;
-    const int i0 = min(tid * ept, (int)nl), i1 = min(i0 + ept, (int)nl);
-    unsigned long long own = 0ull;
-    for (int i = i0; i < i1; ++i) own += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
-    if (tid == 0) S.jstar = 0;
-    unsigned long long wtot;
-    unsigned long long ex = S.mabove + kh_below<unsigned long long>(own, S.s64, &wtot);
-    int lastk = -1;
-    unsigned long long zk = 0ull;
-    for (int i = i0; i < i1; ++i) {
-      if (ex > Y) break;
-      lastk = i;
-      ex += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
-      zk = ex;
-    }
-    if (lastk > 0) atomicMax(&S.jstar, lastk);
-    __syncthreads();
-    const int last = S.jstar;
-    if (lastk == last) {
-      S.zt = fs_key_value(list[last]);
-      S.idcut = fs_key_id(list[last]);
-      S.zkept = zk;
-    }
-    __syncthreads();
-    res.zt = S.zt;
-    res.idcut = S.idcut;
-    Zk = S.zkept;
   }
   if (Zk == 0ull) {
     res.flags = KH_BAIL;
+    FS_WHY(8);
     return res;
   }
   res.invZ = __fdiv_rn(17592186044416.0f, (float)Zk);   // 2^44 / Z
@@ -989,7 +1049,7 @@ __global__ void __launch_bounds__(FT, 2) fstream_kernel(const Params P, int nite
       asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
       const int k = P.topk[b];
       const int cls = (k > 0 && k < P.V) ? FC_TOPK : (P.topp[b] < 1.0f ? FC_TOPP : FC_ALL);
-      g_khtrace[item * 8 + 7] = smid | ((unsigned long long)cls << 16) | ((unsigned long long)res.flags << 20);
+      g_khtrace[item * 8 + 7] |= smid | ((unsigned long long)cls << 16) | ((unsigned long long)res.flags << 20);
     }
 #endif
     if (tid == 0) {

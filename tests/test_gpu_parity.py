@@ -270,6 +270,41 @@ def test_verify_top_k_with_many_ties_at_the_kth_logit():
     assert not rep.bad_mismatches, rep.bad_mismatches
 
 
+def test_verify_top_p_with_maximum_far_above_the_first_wave():
+    # fp32 top-p rows whose first 8192 logits are far below the row maximum: logits
+    # 2^24 or more times heavier than the first wave's maximum are handled apart
+    # from the binned bulk; the cut lies among them (P small), below them (many
+    # tokens between), or they are too many and the row is served another way
+    V, K, B = 32768, 2, 8
+    g = torch.Generator().manual_seed(91)
+    tgt = torch.randn(B, K + 1, V, generator=g) * 0.3
+    drf = torch.randn(B, K, V, generator=g) * 0.3
+    ln2 = math.log(2.0)
+    for s in range(B):
+        idx = 8192 + torch.randperm(V - 8192, generator=g)
+        mode = s % 4
+        for x in (tgt[s], drf[s]):
+            if mode == 0:        # three tokens 30-45 binades up: the cut among them
+                x[:, idx[:3]] = torch.tensor([45.0, 40.0, 30.0]) * ln2
+            elif mode == 1:      # one token 25 binades up, 10000 tokens 20 binades up
+                x[:, idx[:1]] = 25.0 * ln2
+                x[:, idx[1:10001]] = 20.0 * ln2 + 0.3 * torch.randn(x.shape[0], 10000, generator=g)
+            elif mode == 2:      # 300 tokens 30 binades up (more than are listed)
+                x[:, idx[:300]] = 30.0 * ln2 + 0.1 * torch.randn(x.shape[0], 300, generator=g)
+            else:                # the bulk 10 binades up, a ramp of single tokens above
+                x[:, idx[:2000]] = 10.0 * ln2 + torch.randn(x.shape[0], 2000, generator=g)
+                x[:, idx[2000:2040]] = torch.arange(40, dtype=torch.float32) * 0.8 * ln2
+    dtok = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    T = torch.ones(B)
+    k = torch.zeros(B, dtype=torch.int32)
+    P = torch.tensor([0.5, 0.9, 0.95, 0.8, 0.99, 0.7, 0.6, 0.95])
+    out, n = sv.spec_verify(tgt.to(DEV), drf.to(DEV), dtok.to(DEV), T.to(DEV), k.to(DEV),
+                            P.to(DEV), seed=4, offset=12)
+    res = oracle_verify(tgt, drf, dtok, T, k, P, 4, 12, parallel=False)
+    rep = compare(out.cpu(), n.cpu(), res, T)
+    assert not rep.bad_mismatches, rep.bad_mismatches
+
+
 def test_data_errors_are_reported_in_band():
     V, K, B = 64, 2, 9
     tgt = torch.randn(B, K + 1, V)
