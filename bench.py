@@ -83,12 +83,15 @@ def dominant_kernel(workload: str) -> str:
 def launches_per_call(workload: str) -> int:
     """Kernels one spec_verify call launches on this workload's 16-byte aligned rows:
     greedy_kernel, then (with draft logits and at least 16 rows) keyhist_kernel for
-    bf16 rows or fstream_kernel for fp32 rows, then the cluster kernel sv_kernel."""
+    bf16 rows or fs_order_kernel and fstream_kernel for fp32 rows, then the cluster
+    kernel sv_kernel."""
     from speculative_decoding_verification_30_gb300.workloads import WORKLOADS
     w = WORKLOADS[workload]
     if workload == "greedy":
         return 1                                   # no draft logits: greedy_kernel alone
-    return 3 if w.B * (w.K + 1) >= 16 else 2
+    if w.B * (w.K + 1) < 16:
+        return 2
+    return 3 if str(w.dtype).endswith("bfloat16") else 4
 
 
 def profiled_traffic(workload: str):

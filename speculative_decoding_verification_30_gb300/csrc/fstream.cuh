@@ -114,14 +114,11 @@ __device__ __forceinline__ void fs_prefetch_l2(const void* p, size_t n) {
 __device__ __forceinline__ float fs_at(const float4& v, int e) {
   return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
 }
-// Coarse bin of a weight e = 2^x (x relative to the first-wave maximum): FB_TOP
-// minus e's exponent field, so bin j holds x in [23 - j, 24 - j); x >= 24 is out
-// of range (*over), everything below the last bin's binade (x < -23) joins it.
-__device__ __forceinline__ int fs_bin(float e, uint32_t* over) {
-  const int b = FB_TOP - (int)(__float_as_uint(e) >> 23);
-  if (b < 0) *over = 1u;
-  return min(max(b, 0), FNB - 1);
-}
+// Coarse bin of a weight w = 2^y (y = (z - R) c relative to the first-wave
+// maximum R), from w's exponent field: bin j holds w in [2^(23 - j), 2^(24 - j)),
+// a negative value is above the bins (w >= 2^24), and everything below the last
+// bin's binade joins that bin. Both passes over a row bin by this one formula.
+__device__ __forceinline__ int fs_bin_of(float w) { return FB_TOP - (int)(__float_as_uint(w) >> 23); }
 
 // k-th largest (1-based, k <= FT) of the CTA's per-thread 32-bit keys, by four
 // rounds of 8-bit digits (most significant first). Every thread returns it.
@@ -268,6 +265,23 @@ __device__ __forceinline__ void fs_push(const float4& x, int v, float thr, FsSha
 // Row classes.
 constexpr int FC_TOPK = 0, FC_ALL = 1, FC_TOPP = 2;
 
+// Lists the logits of vector v whose weight 2^((z - R) c) lies above the bins
+// (2^24 or more times the first-wave maximum's): their masses are taken exactly
+// after the stream. Sets *over when the list is full.
+__device__ __noinline__ void fs_push_over(float4 x, int v, float c, float nRc, FsShared& S,
+                                          uint32_t* over) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float z = fs_at(x, e);
+    if (fs_bin_of(ex2_approx(fmaf(z, c, nRc))) >= 0) continue;
+    const uint32_t slot = atomicAdd(&S.ocount, 1u);
+    if (slot < (uint32_t)FOCAP)
+      S.olist[slot] = ((unsigned long long)okey(z) << 32) | (uint32_t)~(uint32_t)(4 * v + e);
+    else
+      *over = 1u;
+  }
+}
+
 // Streams the row once (double-buffered waves of FPF vectors per thread).
 // Returns this thread's maximum; *nan is set on NaN or +inf. Top-k rows list the
 // logits >= *thr (set from the first wave); no-truncation rows leave the thread's
@@ -345,23 +359,15 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
         s_t += (ex2_approx(fmaf(x.x, c, nmc)) + ex2_approx(fmaf(x.y, c, nmc))) +
                (ex2_approx(fmaf(x.z, c, nmc)) + ex2_approx(fmaf(x.w, c, nmc)));
       } else {
+        bool ov = false;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float z = fs_at(x, e);
-          const float w = ex2_approx(fmaf(z, c, nRc));
-          const int bb = FB_TOP - (int)(__float_as_uint(w) >> 23);
-          if (bb >= 0) {
-            bins[min(bb, FNB - 1) * FT + tid] += w;
-          } else {
-            // above the bins (2^24 or more times the first-wave maximum's weight):
-            // listed, their masses are taken exactly after the stream
-            const uint32_t slot = atomicAdd(&S.ocount, 1u);
-            if (slot < (uint32_t)FOCAP)
-              S.olist[slot] = ((unsigned long long)okey(z) << 32) | (uint32_t)~(uint32_t)(4 * q + e);
-            else
-              over = 1u;
-          }
+          const float w = ex2_approx(fmaf(fs_at(x, e), c, nRc));
+          const int bb = fs_bin_of(w);
+          ov |= bb < 0;
+          bins[min(max(bb, 0), FNB - 1) * FT + tid] += bb >= 0 ? w : 0.0f;
         }
+        if (ov) fs_push_over(x, q, c, nRc, S, &over);
       }
     }
 #pragma unroll
@@ -387,9 +393,9 @@ __device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float
                                        int s, FsShared& S, unsigned long long* list) {
   const int tid = threadIdx.x, l = lane_id();
   const uint32_t below = (1u << l) - 1u;
+  const float ylo = (float)(22 - j) + 0.99f, yhi = (float)(24 - j) + 0.01f;
   float4 cur[FPF], nxt[FPF];
   const float4 NEG = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  uint32_t over = 0u;
 #pragma unroll
   for (int p = 0; p < FPF; ++p) {
     const int q = tid + p * FT;
@@ -406,18 +412,31 @@ __device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float
 #pragma unroll
     for (int p = 0; p < FPF; ++p) {
       const int q = q0 + p * FT;
+      // bin j < FNB - 1 exactly (the listed logits above the bins excluded); the
+      // weight is formed only for logits whose y lies within 0.01 of the bin's
+      // binade (ex2's rounding moves a weight across a binade only within ~1e-6)
+      uint32_t m4 = 0u;
+      float w4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float y = fmaf(fs_at(cur[p], e), c, nRc);
+        w4[e] = 0.0f;
+        if (q < nv && y >= ylo && y < yhi) {
+          w4[e] = ex2_approx(y);
+          m4 |= (uint32_t)(fs_bin_of(w4[e]) == j) << e;
+        }
+      }
+      if (!__any_sync(0xffffffffu, m4 != 0u)) continue;
+      const bool lfull = PASS == 2 && *reinterpret_cast<volatile uint32_t*>(&S.lcount) > (uint32_t)FLCAP;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float z = fs_at(cur[p], e);
-        const float w = ex2_approx(fmaf(z, c, nRc));
-        // bin j < FNB - 1 exactly (the listed logits above the bins excluded)
-        const bool inb = q < nv && FB_TOP - (int)(__float_as_uint(w) >> 23) == j;
+        const bool inb = (m4 >> e) & 1u;
+        const float w = w4[e];
         const int sb = (int)((__float_as_uint(w) >> 15) & 255u);
-        if (PASS == 2 && inb) {
-          atomicAdd(&S.dh[sb], 1u);
-          atomicAdd(&S.smass[sb], fix_pow2(w * scale, FIX));
-        }
-        const bool want = PASS == 2 ? inb : (inb && sb == s);
+        if (PASS == 2 && inb) atomicAdd(&S.smass[sb], fix_pow2(w * scale, FIX));
+        // (pass 2 stops listing once the bin has overflowed the list: pass 3 runs)
+        const bool want = PASS == 2 ? inb && !lfull : (inb && sb == s);
         const uint32_t mk = __ballot_sync(0xffffffffu, want);
         if (mk) {
           const int ld = __ffs(mk) - 1;
@@ -627,12 +646,9 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
         FS_WHY(5);
         return res;
       }
-      // sub-bins of bin js (counts, exact masses) from L2; the bin's logits listed
+      // sub-bins of bin js (exact masses) from L2; the bin's logits listed
       __syncthreads();
-      for (int i = tid; i < FNSUB; i += FT) {
-        S.dh[i] = 0u;
-        S.smass[i] = 0ull;
-      }
+      for (int i = tid; i < FNSUB; i += FT) S.smass[i] = 0ull;
       if (tid == 0) S.lcount = 0u;
       __syncthreads();
       const float nRc = -(R * c);
@@ -1017,8 +1033,40 @@ __device__ __noinline__ void fs_finalize(const Params& P, int b, FsShared& S) {
   for (int t = tid; t < 2 * R2; t += FT) rz[t] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Processing-order class of sequence b for fstream_kernel: 0 top-p without
+// top-k (two or three passes per row and a full-row sample), 1 no truncation
+// (one pass, full-row sample), 2 top-k (one pass, listed sample), 3 not served.
+__device__ __forceinline__ int fs_seq_class(const Params& P, int b) {
+  if (!fast_seq(P, b)) return 3;
+  const int k = P.topk[b];
+  if (k > 0 && k < P.V) return 2;
+  return P.topp[b] < 1.0f ? 0 : 1;
+}
+
+// The batch's sequences in processing order, heaviest class first (so that the
+// last rows handed out are short ones and the CTAs finish close together); the
+// order within a class is immaterial (results depend on the sequence alone).
+__global__ void __launch_bounds__(1024) fs_order_kernel(const Params P) {
+  __shared__ uint32_t cnt[4], next[4];
+  const int tid = threadIdx.x;
+  if (tid < 4) cnt[tid] = 0u;
+  __syncthreads();
+  for (int b = tid; b < P.B; b += blockDim.x) atomicAdd(&cnt[fs_seq_class(P, b)], 1u);
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t a = 0u;
+    for (int c = 0; c < 4; ++c) {
+      next[c] = a;
+      a += cnt[c];
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < P.B; b += blockDim.x) P.ws_perm[atomicAdd(&next[fs_seq_class(P, b)], 1u)] = b;
+}
+
 // Persistent CTAs take rows of the batch's sampled fp32 sequences from a work
-// counter (sequence-major). Rows of other sequences are skipped.
+// counter, sequence by sequence in the order fs_order_kernel set. Rows of other
+// sequences are skipped.
 __global__ void __launch_bounds__(FT, 2) fstream_kernel(const Params P, int nitems) {
   __shared__ FsShared S;
   // the cluster kernel may launch now; it waits for this grid before reading
@@ -1031,7 +1079,8 @@ __global__ void __launch_bounds__(FT, 2) fstream_kernel(const Params P, int nite
     const int item = S.item;
     __syncthreads();
     if (item >= nitems) break;
-    const int b = item / R2, r = item - b * R2;
+    const int pos_b = item / R2, r = item - pos_b * R2;
+    const int b = P.ws_perm[pos_b];
     if (!fast_seq(P, b)) continue;
     const bool target = r <= K;
     const float* row = target ? static_cast<const float*>(P.rows0) + ((size_t)b * (K + 1) + r) * P.V
@@ -1053,7 +1102,7 @@ __global__ void __launch_bounds__(FT, 2) fstream_kernel(const Params P, int nite
     }
 #endif
     if (tid == 0) {
-      uint4* dst = reinterpret_cast<uint4*>(P.ws_rowres + item);
+      uint4* dst = reinterpret_cast<uint4*>(P.ws_rowres + (size_t)b * R2 + r);
       // a draft row never keeps a list: the sampling list is the target row's
       const uint32_t len = target ? res.pad[1] : KH_NOLIST;
       dst[0] = make_uint4(__float_as_uint(res.zt), __float_as_uint(res.invZ), __float_as_uint(res.m),
@@ -1073,9 +1122,15 @@ __global__ void __launch_bounds__(FT, 2) fstream_kernel(const Params P, int nite
   }
   // finish only after greedy_kernel (launched before, possibly still running)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the last CTA to leave re-arms the work counter and clears the order
   if (tid == 0) {
     __threadfence();
-    if (atomicAdd(P.ws_fdone, 1u) == gridDim.x - 1u) {
+    S.last = atomicAdd(P.ws_fdone, 1u) == gridDim.x - 1u;
+  }
+  __syncthreads();
+  if (S.last) {
+    for (int i = tid; i < P.B; i += FT) P.ws_perm[i] = 0;
+    if (tid == 0) {
       *P.ws_fnext = 0u;
       *P.ws_fdone = 0u;
     }

@@ -100,6 +100,7 @@ struct Params {
   unsigned int* ws_fnext;       // keyhist_kernel: work counter
   unsigned int* ws_fdone;       // keyhist_kernel: CTAs finished
   uint32_t* ws_lists;           // keyhist_kernel: kept-token ids of target rows [B][K+1][256]
+  int* ws_perm;                 // fstream_kernel: sequences in processing order [B]
   const uint64_t* offset_ptr;   // Philox offset in device memory (spec_verify_step), else NULL
 };
 
@@ -2149,7 +2150,10 @@ extern "C" {
 
 // Workspace layout: [units u64 x B(K+1)][tickets u32 x B, padded to 16][error u32,
 // padded to 16][greedy best u64 x B(K+1)][greedy chunk counters u32 x B(K+1)]
-// [greedy flags u32 x B(K+1)]; all of it zero between calls.
+// [greedy flags u32 x B(K+1)], padded to 16; then for the per-row kernels
+// [hand-back flags u32 x B, padded][row results x B(2K+1)][work counter, CTAs
+// done: 16 bytes][kept-token lists u32 x B(K+1) x 256][sequence order i32 x B,
+// padded]; all of it zero between calls.
 size_t spec_verify_workspace_bytes(int B, int K) {
   if (B < 1 || K < 1) return 0;
   const size_t rows = (size_t)B * (K + 1);
@@ -2157,7 +2161,7 @@ size_t spec_verify_workspace_bytes(int B, int K) {
   const size_t head = rows * 8 + tickets + 16 + rows * 8 + rows * 4 + rows * 4;
   // keyhist_kernel: hand-back flags, row results, work counter, kept-token lists
   return ((head + 15) & ~(size_t)15) + tickets + (size_t)B * (2 * K + 1) * sizeof(KhRow) + 16 +
-         rows * KH_KCAP * sizeof(uint32_t);
+         rows * KH_KCAP * sizeof(uint32_t) + tickets;
 }
 
 static sv_status verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dtype,
@@ -2219,6 +2223,7 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
     p.ws_fnext = reinterpret_cast<unsigned int*>(w4);
     p.ws_fdone = reinterpret_cast<unsigned int*>(w4 + 4);
     p.ws_lists = reinterpret_cast<uint32_t*>(w4 + 16);
+    p.ws_perm = reinterpret_cast<int*>(w4 + 16 + rows * KH_KCAP * sizeof(uint32_t));
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // temperature-0 units: streaming reduction; the cluster kernel takes the rest
@@ -2242,6 +2247,12 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
         cudaSuccess)
       return SV_ERR_CUDA;
     const unsigned grid = (unsigned)(nitems < (long long)gblocks ? nitems : (long long)gblocks);
+    // fp32 rows: the sampled sequences' processing order for fstream_kernel, set
+    // before the step's other kernels start (they launch after this one ends)
+    if (dtype == SV_F32 && p.fast_split && !p.greedy_only) {
+      fs_order_kernel<<<1, 1024, 0, st>>>(p);
+      if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    }
     if (dtype == SV_BF16)
       greedy_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(p, G, chunk, (int)nitems, p.ws_best, p.ws_rflag, p.ws_rcnt);
     else

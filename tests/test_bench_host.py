@@ -44,7 +44,7 @@ def test_dominant_kernel_and_launches_per_call():
     assert bench.dominant_kernel("greedy") == bench.GREEDY_KERNEL
     assert bench.launches_per_call("greedy") == 1
     assert bench.dominant_kernel("mixed") == bench.FP32_KERNEL      # fp32 rows, B (K+1) = 3072
-    assert bench.launches_per_call("mixed") == 3    # greedy, fp32 streaming, cluster
+    assert bench.launches_per_call("mixed") == 4    # order, greedy, fp32 streaming, cluster
     assert bench.dominant_kernel("mtp_decode") == bench.CLUSTER_KERNEL   # B (K+1) = 2 rows
 
 
