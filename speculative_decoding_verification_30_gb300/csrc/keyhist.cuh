@@ -163,8 +163,6 @@ struct KhShared {
   uint32_t cmax;                       // collection: running block maximum (order-preserving key)
   uint32_t ccount;                     // collection: candidates pushed
   uint32_t gcount;                     // collection: kept tokens written out
-  unsigned long long ztail;            // uncounted logits: mass in the frame of m (2^-44)
-  uint32_t ntail, tbad;                // and their count; NaN among them
   uint32_t flag[16];
   float pz[16], qz[16];                // p(d), and q(d) if d is kept
   uint32_t ku[16];
@@ -245,9 +243,6 @@ __device__ __forceinline__ uint4 kh_ld(const uint4* p) {
 }
 __device__ __forceinline__ uint4 kh_ld_l2(const uint4* p) { return __ldcg(p); }
 
-__device__ __forceinline__ float kh_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float kh_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
-
 // Counts the 8 logits of one vector; returns their packed maximum.
 __device__ __forceinline__ __nv_bfloat162 kh_count8(uint32_t* hist, const uint4& w) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -300,26 +295,13 @@ __device__ __forceinline__ void kh_collect(const uint4& w, int v, __nv_bfloat162
   }
 }
 
-// Logits far below the running maximum are not counted: their weights, at most
-// 2^-KH_TAIL_BITS of the row maximum's each, are summed per thread instead (one
-// exp2 each, no atomics). Such a logit lies below m - KH_TAIL_BITS / c, so a cut
-// at or above that value is found in the histogram alone; the tail adds to Z.
-constexpr float KH_TAIL_BITS = 24.0f;
-// A thread's tail: sum of 2^((z - M) c) over its uncounted logits, with M the
-// largest logit the thread has seen (the frame moves up with it), and their count.
-struct KhTail {
-  float M, s;
-  uint32_t n;
-};
-
-// Streams one row (nv 16-byte vectors) into the histogram and the thread's tail;
-// returns this thread's maximum (NaN is ignored here: it reaches a NaN bin or the
-// tail sum). A logit at or above theta = M - KH_TAIL_BITS / c is counted, M being
-// the thread's running maximum seeded with the first load wave's block maximum.
-// COLLECT: also lists the candidates of kh_collect.
+// Streams one row (nv 16-byte vectors) into the histogram; returns this
+// thread's maximum (NaN is ignored here: NaN bins are checked afterwards).
+// COLLECT: also lists the candidates of kh_collect (threshold seeded by the
+// block maximum of the first load wave).
 template <bool COLLECT>
-__device__ __forceinline__ float kh_stream(const uint4* src, int nv, uint32_t* hist, float D, float c,
-                                           KhShared& S, unsigned long long* list, KhTail* tail) {
+__device__ __forceinline__ float kh_stream(const uint4* src, int nv, uint32_t* hist, float D,
+                                           KhShared& S, unsigned long long* list) {
   const int tid = threadIdx.x;
   uint4 buf[KH_PF];
   const uint32_t NEG2 = 0xFF80FF80u;
@@ -330,36 +312,31 @@ __device__ __forceinline__ float kh_stream(const uint4* src, int nv, uint32_t* h
   }
   __nv_bfloat162 m2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0xFF80u),
                                          __ushort_as_bfloat16((unsigned short)0xFF80u));
-  // first-wave block maximum: the collection threshold and the tail frame's seed
-  __nv_bfloat162 f2 = m2;
+  float theta = -INFINITY;
+  if (COLLECT) {
+    __nv_bfloat162 f2 = m2;
 #pragma unroll
-  for (int p = 0; p < KH_PF; ++p) {
-    __nv_bfloat162 a, b, cc, d;
-    memcpy(&a, &buf[p].x, 4);
-    memcpy(&b, &buf[p].y, 4);
-    memcpy(&cc, &buf[p].z, 4);
-    memcpy(&d, &buf[p].w, 4);
-    f2 = __hmax2(f2, __hmax2(__hmax2(a, b), __hmax2(cc, d)));
-  }
-  float fm = fmaxf(__low2float(f2), __high2float(f2));
+    for (int p = 0; p < KH_PF; ++p) {
+      __nv_bfloat162 a, b, c, d;
+      memcpy(&a, &buf[p].x, 4);
+      memcpy(&b, &buf[p].y, 4);
+      memcpy(&c, &buf[p].z, 4);
+      memcpy(&d, &buf[p].w, 4);
+      f2 = __hmax2(f2, __hmax2(__hmax2(a, b), __hmax2(c, d)));
+    }
+    float fm = fmaxf(__low2float(f2), __high2float(f2));
 #pragma unroll
-  for (int o = 16; o; o >>= 1) fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, o));
-  if (tid == 0) {
-    S.cmax = okey(-INFINITY);
-    S.ccount = 0u;
-    S.gcount = 0u;
-    S.ztail = 0ull;
-    S.ntail = 0u;
-    S.tbad = 0u;
+    for (int o = 16; o; o >>= 1) fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, o));
+    if (tid == 0) {
+      S.cmax = okey(-INFINITY);
+      S.ccount = 0u;
+      S.gcount = 0u;
+    }
+    __syncthreads();
+    if (lane_id() == 0) atomicMax(&S.cmax, okey(fm));
+    __syncthreads();
+    theta = key_to_float(S.cmax) - D;
   }
-  __syncthreads();
-  if (lane_id() == 0) atomicMax(&S.cmax, okey(fm));
-  __syncthreads();
-  const float R = key_to_float(S.cmax);
-  float theta = COLLECT ? R - D : -INFINITY;
-  const float DT = __fdiv_rn(KH_TAIL_BITS, c);
-  float M = R, th = R - DT, ts = 0.0f;
-  uint32_t tn = 0u;
   for (int q0 = tid; q0 < nv; q0 += KH_PF * KT) {
 #pragma unroll
     for (int p = 0; p < KH_PF; ++p) {
@@ -368,50 +345,12 @@ __device__ __forceinline__ float kh_stream(const uint4* src, int nv, uint32_t* h
         const uint4 w = buf[p];
         const int qn = q + KH_PF * KT;
         if (qn < nv) buf[p] = kh_ld(src + qn);
-        __nv_bfloat162 a, b, cc, d;
-        memcpy(&a, &w.x, 4);
-        memcpy(&b, &w.y, 4);
-        memcpy(&cc, &w.z, 4);
-        memcpy(&d, &w.w, 4);
-        const __nv_bfloat162 vm2 = __hmax2(__hmax2(a, b), __hmax2(cc, d));
+        const __nv_bfloat162 vm2 = kh_count8(hist, w);
         m2 = __hmax2(m2, vm2);
-        const float vm = fmaxf(__low2float(vm2), __high2float(vm2));
-        if (vm > M) {
-          // move the tail's frame up to the new maximum
-          ts *= ex2_approx((M - vm) * c);
-          M = vm;
-          th = M - DT;
-        }
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-        const float nMc = -(M * c);
-        if (vm < th) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float z = (e & 1) ? kh_hi(ws[e >> 1]) : kh_lo(ws[e >> 1]);
-            ts += ex2_approx(fmaf(z, c, nMc));
-          }
-          tn += 8u;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t bits = (e & 1) ? ws[e >> 1] >> 16 : ws[e >> 1] & 0xFFFFu;
-            const float z = __uint_as_float(bits << 16);
-            if (z >= th) {
-              const uint32_t i = kh_bin(bits);
-              atomicAdd(&hist[i >> 1], 1u << ((i & 1u) << 4));
-            } else {
-              ts += ex2_approx(fmaf(z, c, nMc));
-              ++tn;
-            }
-          }
-        }
         if (COLLECT) kh_collect(w, q, vm2, D, &theta, S, list);
       }
     }
   }
-  tail->M = M;
-  tail->s = ts;
-  tail->n = tn;
   return fmaxf(__low2float(m2), __high2float(m2));
 }
 
@@ -607,9 +546,8 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   rmass[tid] = 0ull;
   const float c = __fdiv_rn(KH_LOG2E, T);
   const float D = __fdiv_rn(KH_LIST_BITS, c);                    // z >= m - D: weight >= 2^-12
-  KhTail tl;
-  float mt = target ? kh_stream<true>(src, nv, hist, D, c, S, clist, &tl)
-                    : kh_stream<false>(src, nv, hist, D, c, S, clist, &tl);
+  float mt = target ? kh_stream<true>(src, nv, hist, D, S, clist)
+                    : kh_stream<false>(src, nv, hist, D, S, clist);
 #pragma unroll
   for (int o = 16; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
   if (l == 0) S.fmax[w] = mt;
@@ -618,22 +556,6 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   float m = S.fmax[0];
 #pragma unroll
   for (int i = 1; i < KWARP; ++i) m = fmaxf(m, S.fmax[i]);
-  // the tail in the frame of m, summed over the block (fixed point)
-  const float DT = __fdiv_rn(KH_TAIL_BITS, c);
-  {
-    const float tw = tl.n ? tl.s * ex2_approx((tl.M - m) * c) : 0.0f;
-    const bool tbad = !(tw >= 0.0f && tw < INFINITY);
-    unsigned long long zt = tbad ? 0ull : fix_pow2(tw, FIX);
-    uint32_t nt = tl.n;
-    zt = warp_sum(zt);
-    nt = warp_sum(nt);
-    const uint32_t anyt = __ballot_sync(0xffffffffu, tbad);
-    if (l == 0) {
-      if (zt) atomicAdd(&S.ztail, zt);
-      if (nt) atomicAdd(&S.ntail, nt);
-      if (anyt) S.tbad = 1u;
-    }
-  }
 
   // sweep, words interleaved over the threads (occupied bins cluster in a few
   // value ranges): counts and fixed-point masses, added to the word's thread range
@@ -679,14 +601,12 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   for (int wd = (KH_NW / 4) * 4 + tid; wd < KH_NW; wd += KT)
     if (hist[wd]) sweep_word(wd, hist[wd]);
   flush();
-  int anyb = __syncthreads_or((int)bad);
-  anyb |= (int)S.tbad;
+  const int anyb = __syncthreads_or((int)bad);
   const uint32_t cnt = rcnt[tid];
   const unsigned long long mass = anyb ? 0ull : rmass[tid];
   uint32_t ctot, cab;
-  unsigned long long ZH, mab;
-  kh_above2(cnt, mass, S, &cab, &ctot, &mab, &ZH);
-  const unsigned long long Ztot = ZH + S.ztail;   // Z: counted and summed logits
+  unsigned long long Ztot, mab;
+  kh_above2(cnt, mass, S, &cab, &ctot, &mab, &Ztot);
   KH_MARK(item, 2);
 
   KhRow res;
@@ -699,11 +619,10 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
   res.pad[0] = 0u;
   res.pad[1] = KH_NOLIST;
   if (anyb || !(m > -INFINITY)) res.flags = KH_ERR;
-  else if (ctot + S.ntail != (uint32_t)V) res.flags = KH_BAIL;
+  else if (ctot != (uint32_t)V) res.flags = KH_BAIL;
   const bool topk = k > 0 && k < V;
   const bool topp = topP < 1.0f;
   unsigned long long ZL1 = Ztot;
-  if (res.flags == 0u && topk && ctot < (uint32_t)k) res.flags = KH_BAIL;   // k-th among the summed
   if (res.flags == 0u && topk) {
     // the bin holding the k-th token in (logit desc, id asc) order
     if (cab < (uint32_t)k && (uint32_t)k <= cab + cnt) {
@@ -721,7 +640,6 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
     // the bin where the exclusive mass first exceeds Y = the largest integer
     // below P * Z(L1); tokens with exclusive mass <= Y are kept
     const unsigned long long Y = mass_threshold(topP, ZL1);
-    if (Y >= ZH) res.flags = KH_BAIL;                // the cut lies among the summed logits
     __syncthreads();
     if (mab <= Y && Y < mab + mass) {
       S.wq = tid;
@@ -729,18 +647,12 @@ __device__ __noinline__ KhRow kh_row(const __nv_bfloat16* row, int V, float T, i
       S.rq = (int)cab;
     }
     __syncthreads();
-    if (w == 0 && res.flags == 0u) {
+    if (w == 0) {
       kh_walk(hist, S.wq, (uint32_t)S.rq, S.acc, true, 0u, Y, m, c, S);
       __syncwarp();
       if (l == 0) S.cq = (int)((Y - S.Mcut) / S.Wcut) + 1;
     }
     __syncthreads();
-  }
-  // every logit at or above m - KH_TAIL_BITS / c was counted: a cut bin there saw
-  // all of the row's tokens on or above it
-  if (res.flags == 0u && (topk || topp)) {
-    const float vlow = S.cbin == KH_OFF ? -__uint_as_float(KH_TSPLIT << 16) : kh_value(S.cbin);
-    if (!(vlow >= m - DT)) res.flags = KH_BAIL;
   }
   // the histogram is not read again for this row
   for (int wd = tid; wd < KH_NW; wd += KT) hist[wd] = 0u;
@@ -830,6 +742,8 @@ __device__ __forceinline__ void kh_elem(float zp, float zq, int id, bool paired,
     *p = pp;
   }
 }
+__device__ __forceinline__ float kh_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float kh_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
 // Fixed-point (2^-40) residual and target masses of the 8 tokens of vector v
 // (target logits a already loaded), for a vector holding a token of the

@@ -1792,7 +1792,8 @@ __global__ void __launch_bounds__(NT, 2) sv_kernel(const Params P) {
 // lowest id); NaN / +inf set the row's flag. The last CTA to finish writes the
 // sequences' outputs. Items of other sequences raise the cluster kernel's work
 // flag.
-constexpr int GV = 6;          // 16-byte vectors per thread and item (at most)
+constexpr int GV = 4;          // 16-byte vectors per thread and wave
+constexpr int GW = 6;          // waves per item (at most)
 
 // A greedy sequence once all its rows are reduced: the accepted prefix and the
 // token from the K+1 rows' (max, argmax) slots, which are cleared for the next call.
@@ -1824,28 +1825,52 @@ __device__ void greedy_finalize_seq(const Params& P, int b, unsigned long long* 
   P.out_n[b] = err ? -1 : nacc;
 }
 
+// Geometry of greedy item `item` (row chunk): its row, whether the row belongs
+// to a temperature-0 sequence, its first vector and its vector count (0 for rows
+// of other sequences, which are not read here).
 template <typename DT>
-__device__ __forceinline__ void greedy_load(const Params& P, int item, int G, int chunk, uint4* w,
-                                            int* row_out, bool* ok_out) {
+__device__ __forceinline__ void greedy_item(const Params& P, int item, int G, int chunk, int* row_out,
+                                            bool* ok_out, const uint4** v_out, int* nv_out, int* l0_out) {
+  constexpr int PV = 16 / (int)sizeof(DT);
   const int row = item / G, c = item - row * G;
   const bool ok = greedy_seq(P, row / (P.K + 1));
+  const int l0 = c * chunk, l1 = min(l0 + chunk, P.V);
   *row_out = row;
   *ok_out = ok;
+  *v_out = reinterpret_cast<const uint4*>(static_cast<const DT*>(P.rows0) + (size_t)row * P.V) + l0 / PV;
+  *nv_out = ok ? (l1 - l0) / PV : 0;
+  *l0_out = l0;
+}
+// One wave of an item: vectors w0 + tid + q NT (q < GV), -inf past the chunk.
+template <typename DT>
+__device__ __forceinline__ void greedy_wave(const uint4* v, int nv, int w0, uint4* x) {
   constexpr uint32_t NEG = sizeof(DT) == 2 ? 0xFF80FF80u : 0xFF800000u;
-  const int l0 = c * chunk, l1 = min(l0 + chunk, P.V);
-  constexpr int PV = 16 / (int)sizeof(DT);
-  const uint4* v = reinterpret_cast<const uint4*>(static_cast<const DT*>(P.rows0) + (size_t)row * P.V) + l0 / PV;
-  const int nv = ok ? (l1 - l0) / PV : 0;
 #pragma unroll
   for (int q = 0; q < GV; ++q) {
-    const int vi = (int)threadIdx.x + q * NT;
+    const int vi = w0 + (int)threadIdx.x + q * NT;
     if (vi < nv) {
       asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(w[q].x), "=r"(w[q].y), "=r"(w[q].z), "=r"(w[q].w)
+                   : "=r"(x[q].x), "=r"(x[q].y), "=r"(x[q].z), "=r"(x[q].w)
                    : "l"(v + vi));
     } else {
-      w[q] = make_uint4(NEG, NEG, NEG, NEG);
+      x[q] = make_uint4(NEG, NEG, NEG, NEG);
     }
+  }
+}
+// Maximum of one 16-byte vector (NaN if it holds one).
+template <typename DT>
+__device__ __forceinline__ float greedy_vmax(const uint4& x) {
+  if constexpr (sizeof(DT) == 2) {
+    __nv_bfloat162 a, bb, cc, dd;
+    memcpy(&a, &x.x, 4);
+    memcpy(&bb, &x.y, 4);
+    memcpy(&cc, &x.z, 4);
+    memcpy(&dd, &x.w, 4);
+    const __nv_bfloat162 v2 = __hmax2_nan(__hmax2_nan(a, bb), __hmax2_nan(cc, dd));
+    return fmax_nan(__low2float(v2), __high2float(v2));
+  } else {
+    return fmax_nan(fmax_nan(__uint_as_float(x.x), __uint_as_float(x.y)),
+                    fmax_nan(__uint_as_float(x.z), __uint_as_float(x.w)));
   }
 }
 
@@ -1855,12 +1880,17 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
                                                      unsigned int* rflag, unsigned int* done) {
   const int tid = threadIdx.x;
   constexpr int PV = 16 / (int)sizeof(DT);
+  constexpr int WV = GV * NT;                  // vectors per wave
   uint4 cur[GV], nxt[GV];
   // the step's later kernels may launch now; they wait for this grid where needed
   asm volatile("griddepcontrol.launch_dependents;");
-  int item = blockIdx.x, row = 0, nrow = 0;
-  bool ok = false, nok = false;
-  if (item < nitems) greedy_load<DT>(P, item, G, chunk, cur, &row, &ok);
+  int item = blockIdx.x, wave = 0, row = 0, nv = 0, l0 = 0;
+  bool ok = false;
+  const uint4* v = nullptr;
+  if (item < nitems) {
+    greedy_item<DT>(P, item, G, chunk, &row, &ok, &v, &nv, &l0);
+    greedy_wave<DT>(v, nv, 0, cur);
+  }
   // a batch without temperature-0 sequences: only the cluster kernel's work
   // flag is left to set (for sequences keyhist_kernel does not serve)
   // (checked only by CTAs whose first row is not on the greedy path)
@@ -1874,80 +1904,88 @@ __global__ void __launch_bounds__(NT) greedy_kernel(const Params P, int G, int c
     if (__syncthreads_or(other ? 1 : 0) && tid == 0) atomicOr(P.ws_work, 1u);
     return;
   }
+  // the CTA's (item, wave) pairs form one stream: the next pair's loads are in
+  // flight while the current one is reduced. Per thread: the running maximum,
+  // the first vector holding it (and its contents), and a NaN flag.
+  float mt = -INFINITY;
+  int vb = -1;
+  uint4 wb = make_uint4(0u, 0u, 0u, 0u);
+  bool nanf = false;
+  int nrow = row, nnv = nv, nl0 = l0;
+  bool nok = ok;
+  const uint4* nvp = v;
   while (item < nitems) {
-    const int next = item + (int)gridDim.x;
-    if (next < nitems) greedy_load<DT>(P, next, G, chunk, nxt, &nrow, &nok);
-    if (!ok) {
-      // rows of sampled sequences: the cluster kernel has work unless they all
-      // go to keyhist_kernel (which raises the flag itself when it hands one back)
-      if (!P.greedy_only && tid == 0 && item - row * G == 0 &&
-          !(P.fast_split && fast_seq(P, row / (P.K + 1))) &&
-          *reinterpret_cast<volatile unsigned int*>(P.ws_work) == 0u)
-        atomicOr(P.ws_work, 1u);
-    } else {
-      const int l0 = (item - row * G) * chunk;
-      // per-vector maxima, then the thread maximum; the lowest index holding it
-      // is looked up only in the first vector whose maximum equals it
-      float vm[GV];
-      float m = -INFINITY;
+    int nitem = item, nwave = wave + 1;
+    if (nwave * WV >= nv) {
+      nitem = item + (int)gridDim.x;
+      nwave = 0;
+      if (nitem < nitems) greedy_item<DT>(P, nitem, G, chunk, &nrow, &nok, &nvp, &nnv, &nl0);
+    }
+    if (nitem < nitems) greedy_wave<DT>(nitem == item ? v : nvp, nitem == item ? nv : nnv, nwave * WV, nxt);
+    if (ok) {
 #pragma unroll
       for (int q = 0; q < GV; ++q) {
-        if constexpr (sizeof(DT) == 2) {
-          __nv_bfloat162 a, bb, cc, dd;
-          memcpy(&a, &cur[q].x, 4);
-          memcpy(&bb, &cur[q].y, 4);
-          memcpy(&cc, &cur[q].z, 4);
-          memcpy(&dd, &cur[q].w, 4);
-          const __nv_bfloat162 v2 = __hmax2_nan(__hmax2_nan(a, bb), __hmax2_nan(cc, dd));
-          vm[q] = fmax_nan(__low2float(v2), __high2float(v2));
-        } else {
-          vm[q] = fmax_nan(fmax_nan(__uint_as_float(cur[q].x), __uint_as_float(cur[q].y)),
-                           fmax_nan(__uint_as_float(cur[q].z), __uint_as_float(cur[q].w)));
+        const int vi = wave * WV + tid + q * NT;
+        const float vm = greedy_vmax<DT>(cur[q]);
+        nanf |= vm != vm;
+        if (vi < nv && vm > mt) {
+          mt = vm;
+          vb = vi;
+          wb = cur[q];
         }
-        m = fmax_nan(m, vm[q]);
       }
-      uint32_t idx = UINT_MAX;
-      if (m > -INFINITY && m < INFINITY) {
-        int qf = GV;
+    }
+    if (nitem != item) {
+      if (ok) {
+        // the lowest index holding the maximum: within the first vector holding it
+        uint32_t idx = UINT_MAX;
+        if (vb >= 0 && mt < INFINITY) {
+          const uint32_t ws[4] = {wb.x, wb.y, wb.z, wb.w};
+          const uint32_t base = (uint32_t)(l0 + vb * PV);
 #pragma unroll
-        for (int q = GV - 1; q >= 0; --q)
-          if (vm[q] == m) qf = q;
-        uint4 w = cur[0];
-#pragma unroll
-        for (int q = 1; q < GV; ++q)
-          if (q == qf) w = cur[q];
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-        const uint32_t base = (uint32_t)(l0 + (tid + qf * NT) * PV);
-#pragma unroll
-        for (int h = 3; h >= 0; --h) {
-          if constexpr (sizeof(DT) == 2) {
-            if (__uint_as_float(ws[h] & 0xFFFF0000u) == m) idx = base + 2 * h + 1;
-            if (__uint_as_float(ws[h] << 16) == m) idx = base + 2 * h;
-          } else {
-            if (__uint_as_float(ws[h]) == m) idx = base + h;
+          for (int h = 3; h >= 0; --h) {
+            if constexpr (sizeof(DT) == 2) {
+              if (__uint_as_float(ws[h] & 0xFFFF0000u) == mt) idx = base + 2 * h + 1;
+              if (__uint_as_float(ws[h] << 16) == mt) idx = base + 2 * h;
+            } else {
+              if (__uint_as_float(ws[h]) == mt) idx = base + h;
+            }
           }
         }
-      }
-      const bool bad = (m != m) || m == INFINITY;
-      unsigned long long key = idx != UINT_MAX ? (((unsigned long long)okey(m) << 32) | (uint32_t)~idx) : 0ull;
+        const bool bad = nanf || mt == INFINITY;
+        unsigned long long key = idx != UINT_MAX ? (((unsigned long long)okey(mt) << 32) | (uint32_t)~idx) : 0ull;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const unsigned long long o2 = __shfl_xor_sync(0xffffffffu, key, o);
-        key = o2 > key ? o2 : key;
+        for (int o = 16; o; o >>= 1) {
+          const unsigned long long o2 = __shfl_xor_sync(0xffffffffu, key, o);
+          key = o2 > key ? o2 : key;
+        }
+        // one merge per warp and item, without a reply (the row's slot takes the
+        // largest key); no block barrier, so every warp keeps its loads flowing
+        const bool wbad = __any_sync(0xffffffffu, bad);
+        if (lane_id() == 0) {
+          if (wbad) atomicOr(&rflag[row], 1u);
+          else if (key) atomicMax(&best[row], key);
+        }
+      } else if (!P.greedy_only && tid == 0 && item - row * G == 0 &&
+                 !(P.fast_split && fast_seq(P, row / (P.K + 1))) &&
+                 *reinterpret_cast<volatile unsigned int*>(P.ws_work) == 0u) {
+        // rows of sampled sequences: the cluster kernel has work unless they all
+        // go to keyhist_kernel (which raises the flag itself when it hands one back)
+        atomicOr(P.ws_work, 1u);
       }
-      // one merge per warp and item, without a reply (the row's slot takes the
-      // largest key); no block barrier, so every warp keeps its loads flowing
-      const bool wbad = __any_sync(0xffffffffu, bad);
-      if (lane_id() == 0) {
-        if (wbad) atomicOr(&rflag[row], 1u);
-        else if (key) atomicMax(&best[row], key);
-      }
+      mt = -INFINITY;
+      vb = -1;
+      nanf = false;
+      row = nrow;
+      ok = nok;
+      v = nvp;
+      nv = nnv;
+      l0 = nl0;
     }
 #pragma unroll
     for (int q = 0; q < GV; ++q) cur[q] = nxt[q];
-    row = nrow;
-    ok = nok;
-    item = next;
+    item = nitem;
+    wave = nwave;
   }
   // the last CTA to finish writes the greedy sequences' outputs
   __shared__ int last_cta;
@@ -2237,7 +2275,7 @@ static sv_status verify_impl(const void* target_logits, const void* draft_logits
     // row spread over a cluster of SMs instead
     p.fast_split = (draft_logits != nullptr && (long long)B * (K + 1) >= 16) ? 1 : 0;
     const int PV = 16 / (int)es;
-    const int cmax = GV * NT * PV;
+    const int cmax = GW * GV * NT * PV;
     const int G = (V + cmax - 1) / cmax;
     int chunk = (V + G - 1) / G;
     chunk = (chunk + PV - 1) / PV * PV;
