@@ -44,6 +44,9 @@ constexpr int FB_TOP = 150;                  // bin = FB_TOP - exponent field of
 constexpr int FNSUB = 256;                   // sub-bins of the crossing bin
 constexpr int FKMAX = 256;                   // largest top_k served here
 constexpr int FOCAP = 256;                   // top-p logits above the bins (u64 composite keys)
+constexpr int FRS = 4;                       // bulk-copy ring: stages
+constexpr int FRV = 1024;                    // bulk-copy ring: 16-byte vectors per stage (16 KB)
+constexpr int FRP = FRV / FT;                // vectors per thread and stage
 constexpr int FMAXBLK = 128;                 // 32-vector blocks per warp range (V <= 262144)
 constexpr size_t FS_SMEM = (size_t)FNB * FT * 4;   // bins | list | sampling block sums
 
@@ -68,6 +71,8 @@ struct FsShared {
   float zt;
   int idcut;
   unsigned long long zkept;
+  unsigned long long rfull[FRS];             // bulk-copy ring: stage filled
+  uint32_t rtimeout;                         // a ring wait gave up
   uint32_t ocount;                           // logits above the bins (top-p rows)
   unsigned long long olist[FOCAP];
 };
@@ -327,6 +332,7 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
     S.lcount = 0u;
     S.rflags = 0u;
     S.ocount = 0u;
+    S.rtimeout = 0u;
   }
   __syncthreads();
   if (l == 0) atomicMax(&S.cmax, okey(fm));
@@ -379,6 +385,118 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
     }
   }
   if (over) atomicOr(&S.rflags, FS_OVER);
+  *mt = m_t;
+  *st = s_t;
+  *nan = bad;
+  return tmax;
+}
+
+// One pass over a top-k or untruncated row through a ring of FRS shared-memory
+// stages of 16 KB, filled by bulk copies (one thread issues them; FRS - 1 stages
+// stay in flight while the CTA reads one), so that a CTA keeps 48 KB of the row in
+// flight without registers. Same results as fs_stream<CLS>: the thread maximum,
+// the first two stages' block maximum R, the top-k threshold and candidate list,
+// or the running (max, sum). Every wait is bounded; on a timeout the row is marked
+// (S.rtimeout) after the copies in flight have landed.
+template <int CLS>
+__device__ __noinline__ float fs_stream_ring(const float4* src, int nv, int k, float c, FsShared& S,
+                                             unsigned long long* list, float4* ring, float* thr, float* mt,
+                                             float* st, float* Rout, bool* nan) {
+  const int tid = threadIdx.x, l = lane_id();
+  const int nst = (nv + FRV - 1) / FRV;
+  const uint64_t pol = CLS == FC_TOPK ? policy_evict_first() : policy_evict_last();
+  // the previous row's writes to this shared memory come before the bulk copies
+  fence_proxy_async();
+  __syncthreads();
+  if (tid == 0) {
+    for (int s = 0; s < FRS; ++s) mbar_init(&S.rfull[s], 1);
+    fence_mbar_init();
+    S.cmax = okey(-INFINITY);
+    S.lcount = 0u;
+    S.rflags = 0u;
+    S.ocount = 0u;
+    S.rtimeout = 0u;
+  }
+  __syncthreads();
+  int issued = min(FRS, nst);                  // stages issued (thread 0's count)
+  if (tid == 0) {
+    for (int s = 0; s < issued; ++s) {
+      const uint32_t bytes = (uint32_t)min(FRV, nv - s * FRV) * 16u;
+      mbar_arrive_expect_tx(&S.rfull[s], bytes);
+      bulk_g2s(ring + (size_t)s * FRV, src + (size_t)s * FRV, bytes, &S.rfull[s], pol);
+    }
+  }
+  bool tmo = false;
+  // first two stages (16 logits per thread): block maximum R, top-k threshold
+  float tmax = -INFINITY;
+  bool bad = false;
+  for (int s = 0; s < 2 && s < nst; ++s) {
+    if (!mbar_wait_bounded(&S.rfull[s], 0u, WAIT_LIMIT_NS)) tmo = true;
+#pragma unroll
+    for (int p = 0; p < FRP; ++p) {
+      const int q = s * FRV + tid + p * FT;
+      if (q >= nv) continue;
+      const float4 x = ring[(size_t)s * FRV + tid + p * FT];
+      tmax = fmaxf(tmax, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
+    }
+  }
+  float fm = tmax;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, o));
+  if (l == 0) atomicMax(&S.cmax, okey(fm));
+  __syncthreads();
+  const float R = key_to_float(S.cmax);
+  *Rout = R;
+  float th = -INFINITY;
+  if (CLS == FC_TOPK) th = key_to_float(fs_kth_key(okey(tmax), k, S));
+  *thr = th;
+  float m_t = -INFINITY, s_t = 0.0f;
+  for (int s = 0; s < nst; ++s) {
+    const int slot = s % FRS;
+    if (s >= 2 && !mbar_wait_bounded(&S.rfull[slot], (uint32_t)((s / FRS) & 1), WAIT_LIMIT_NS)) tmo = true;
+    if (!tmo) {
+#pragma unroll
+      for (int p = 0; p < FRP; ++p) {
+        const int q = s * FRV + tid + p * FT;
+        if (q >= nv) continue;
+        const float4 x = ring[(size_t)slot * FRV + tid + p * FT];
+        const float vm = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+        tmax = fmaxf(tmax, vm);
+        bad |= !(x.x == x.x) || !(x.y == x.y) || !(x.z == x.z) || !(x.w == x.w) || vm == INFINITY;
+        if (CLS == FC_TOPK) {
+          if (vm >= th) fs_push(x, q, th, S, list);
+        } else {
+          if (vm > m_t) {
+            s_t = m_t > -INFINITY ? s_t * ex2_approx((m_t - vm) * c) : 0.0f;
+            m_t = vm;
+          }
+          const float nmc = -(m_t * c);
+          s_t += (ex2_approx(fmaf(x.x, c, nmc)) + ex2_approx(fmaf(x.y, c, nmc))) +
+                 (ex2_approx(fmaf(x.z, c, nmc)) + ex2_approx(fmaf(x.w, c, nmc)));
+        }
+      }
+    }
+    // the stage is read by every thread before it is filled again
+    if (__syncthreads_or(tmo ? 1 : 0)) {
+      tmo = true;
+      break;
+    }
+    if (tid == 0 && s + FRS < nst) {
+      const uint32_t bytes = (uint32_t)min(FRV, nv - (s + FRS) * FRV) * 16u;
+      mbar_arrive_expect_tx(&S.rfull[slot], bytes);
+      bulk_g2s(ring + (size_t)slot * FRV, src + (size_t)(s + FRS) * FRV, bytes, &S.rfull[slot], pol);
+      ++issued;
+    }
+  }
+  if (tmo) {
+    // let every copy this row issued land before the ring is reused
+    if (tid == 0) {
+      S.rtimeout = 1u;
+      for (int s = max(0, issued - FRS); s < issued; ++s)
+        mbar_wait_bounded(&S.rfull[s % FRS], (uint32_t)((s / FRS) & 1), WAIT_LIMIT_NS);
+    }
+    __syncthreads();
+  }
   *mt = m_t;
   *st = s_t;
   *nan = bad;
@@ -497,8 +615,11 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
   float thr, mt, st, R;
   bool nan;
   float tm;
-  if (cls == FC_TOPK) tm = fs_stream<FC_TOPK>(src, nv, k, c, S, list, bins, &thr, &mt, &st, &R, &nan);
-  else if (cls == FC_ALL) tm = fs_stream<FC_ALL>(src, nv, k, c, S, list, bins, &thr, &mt, &st, &R, &nan);
+  // top-k and untruncated rows stream through a bulk-copy ring placed after the
+  // candidate list (its first FLCAP entries)
+  float4* ring = reinterpret_cast<float4*>(list + FLCAP);
+  if (cls == FC_TOPK) tm = fs_stream_ring<FC_TOPK>(src, nv, k, c, S, list, ring, &thr, &mt, &st, &R, &nan);
+  else if (cls == FC_ALL) tm = fs_stream_ring<FC_ALL>(src, nv, k, c, S, list, ring, &thr, &mt, &st, &R, &nan);
   else tm = fs_stream<FC_TOPP>(src, nv, k, c, S, list, bins, &thr, &mt, &st, &R, &nan);
 #pragma unroll
   for (int o = 16; o; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
@@ -509,7 +630,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
   for (int i = 1; i < KWARP; ++i) m = fmaxf(m, S.fmax[i]);
   res.m = m;
   KH_MARK(S.item, 1);
-  if (anynan || !(m > -INFINITY)) {
+  if (anynan || !(m > -INFINITY) || S.rtimeout) {
     res.flags = KH_ERR;
     return res;
   }
