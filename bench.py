@@ -17,6 +17,7 @@ larger than L2 or the rotation spans more than twice L2).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -58,7 +59,9 @@ def measured_peak():
 # bytes are unchanged; other translation units do not affect those kernels.
 PROFILED_SOURCES = ("speculative_decoding_verification_30_gb300/csrc/spec_verify.cu",
                     "speculative_decoding_verification_30_gb300/csrc/keyhist.cuh",
+                    "speculative_decoding_verification_30_gb300/csrc/fstream.cuh",
                     "speculative_decoding_verification_30_gb300/csrc/sv_device.cuh",
+                    "speculative_decoding_verification_30_gb300/csrc/launch_cache.h",
                     "include/spec_verify.h")
 
 
@@ -289,6 +292,9 @@ def bench_gpu(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", lrank)
     w = WORKLOADS[args.workload]
+    if args.batch:
+        # a smaller batch of the same workload, for profiler captures
+        w = dataclasses.replace(w, B=args.batch)
     B, K, V = w.B, w.K, w.V
     greedy = args.workload == "greedy"
     sv.load()
@@ -374,7 +380,7 @@ def bench_gpu(args):
                    "parallelism": f"replicas x{ws}"},
         "achieved_GBps": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                     "frac": achieved / peak, "traffic": None if args.batch else profiled_traffic(w.name),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                      "alg_bytes_per_launch": alg_bytes,
                      "launch_ms": per_launch_ms, "kernel": dominant_kernel(w.name),
@@ -506,6 +512,8 @@ def main():
     ap.add_argument("--no-others", action="store_true",
                     help="skip the greedy, mixed and MTP-decode workloads measured after the headline")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size B (profiler captures on a small case)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
