@@ -10,9 +10,9 @@ the one sample per sequence). Boundary draws themselves are counted and reported
 their rate is a property of the input (about 2e-6 per acceptance draw, and far more
 for samples from a wide nucleus, where tokens carry ~1e-5 of mass each).
 
-About 1.2e5 draws: vocabulary 1024 (so the oracle finishes in seconds), mixed
-per-sequence temperature / top-k / top-p, fp32 rows (cluster kernel) and bf16 rows
-(key-histogram kernel), one call of 25,000 sequences each.
+More than 1e5 draws per dtype: vocabulary 1024 (so the oracle finishes in seconds),
+mixed per-sequence temperature / top-k / top-p, fp32 rows (row-streaming kernel)
+and bf16 rows (key-histogram kernel), 45,000 sequences each in calls of 2,500.
 """
 import pytest
 import torch
@@ -24,7 +24,7 @@ from tests.parity_util import ParityReport, compare, oracle_verify
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-B, K, V = 25_000, 2, 1024
+B, K, V = 45_000, 2, 1024
 CHUNK = 2_500
 
 
@@ -51,6 +51,6 @@ def test_forgiven_mismatches_stay_under_1e5_of_draws(dtype, report):
     rate = total.excused / total.draws
     print(f"{dtype}: {total}; forgiven-mismatch rate {rate:.2e}; "
           f"boundary-draw sequences {total.boundary / total.sequences:.2e} of sequences")
-    assert total.draws >= 50_000
+    assert total.draws >= 100_000
     assert not total.bad_mismatches, total.bad_mismatches[:3]
     assert total.excused < 1e-5 * total.draws, (total.excused, total.draws)
