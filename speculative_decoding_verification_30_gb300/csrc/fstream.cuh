@@ -6,21 +6,25 @@
 // masses, the exact 128-bit inverse-CDF crossing test).
 //
 // A persistent grid of FT-thread CTAs (two per SM) takes the rows of the batch's
-// sampled sequences from a work counter, sequence-major. Per row, by its
-// truncation parameters:
-//   top-k (0 < k <= 256): the k-th largest of the threads' first-wave maxima is
-//     at most the row's k-th largest logit, so every top-k token lies at or above
-//     it; the stream lists those logits as composite keys (order key << 32 | ~id,
-//     so descending keys are logit descending, id ascending); the list is sorted
-//     and its first k entries are the top-k set; a top-p cut falls inside them.
-//   no truncation: the stream sums the weights 2^((z - m_t) c) with a per-thread
-//     running maximum m_t (the sum is rescaled when m_t grows).
-//   top-p only: the stream adds each weight 2^((z - R) c) (R = first-wave maximum)
-//     to a per-thread bin by its binade (shared memory, no atomics); the bin where
-//     the exclusive mass first exceeds P * Z is then read again from L2 and split
-//     into 256 sub-bins by the weight's top mantissa bits (counts and exact
-//     fixed-point masses); the crossing sub-bin's logits are listed, sorted and
-//     walked to the exact cut.
+// sampled sequences from a work counter, sequence by sequence in the order
+// fs_order_kernel wrote (heaviest sequences first). Per row, by its truncation
+// parameters:
+//   top-k (0 < k <= 256): the row streams through a ring of bulk copies into
+//     shared memory; the k-th largest of the threads' maxima over the first two
+//     stages is at most the row's k-th largest logit, so every top-k token lies at
+//     or above it, and those logits are listed as composite keys (order key << 32
+//     | ~id, so descending keys are logit descending, id ascending). A radix select
+//     over the list finds the k-th key and ranking the candidates at or above it
+//     gives the top k in order; a top-p cut falls inside them.
+//   no truncation: the same ring; per-thread running sums of the weights
+//     2^((z - m_t) c) with a running maximum m_t (rescaled when m_t grows).
+//   top-p only: each weight 2^((z - R) c) (R = the first wave's maximum) goes to a
+//     per-thread bin by its binade (shared memory, no atomics); weights 2^24 or
+//     more above R are listed instead and given exact masses afterwards. The bin
+//     where the exclusive mass first exceeds P * Z is read again from L2, split
+//     into 256 sub-bins by the weight's top mantissa bits (exact fixed-point
+//     masses) with its logits listed on the way; the crossing sub-bin's logits are
+//     sorted and walked to the exact cut.
 // The row's result (cut logit, id cut, 2^44 / kept mass, maximum, c) and the
 // probability of the sequence's drafted token at that position go to the
 // workspace. The CTA that finishes a sequence's last row runs the acceptance
@@ -28,9 +32,9 @@
 // p_K by an inverse CDF in token-id order, over the listed kept tokens when the
 // target row has a list, else over the whole rows (from L2).
 //
-// Rows this path does not serve (top-k above 256, a list or bin that overflows,
-// weights out of range) hand their sequence to the cluster kernel, as the bf16
-// path does.
+// Rows this path does not serve (top-k above 256, a candidate list or crossing
+// sub-bin that overflows, more than 256 weights above the bins, a crossing in the
+// last bin) hand their sequence to the cluster kernel, as the bf16 path does.
 #pragma once
 
 namespace sv {
@@ -64,8 +68,8 @@ struct FsShared {
   uint32_t flag[16];
   float pz[16], qz[16];
   unsigned long long binm[FNB];
-  uint32_t dh[256];                          // radix-select digit counts / sub-bin counts
-  unsigned long long smass[FNSUB];
+  uint32_t dh[256];                          // radix-select digit counts
+  unsigned long long smass[FNSUB];           // exact masses of the crossing bin's sub-bins
   unsigned long long mabove;                 // exclusive mass before the crossing sub-bin
   int jstar, sstar, ncut;
   float zt;
@@ -125,10 +129,42 @@ __device__ __forceinline__ float fs_at(const float4& v, int e) {
 // bin's binade joins that bin. Both passes over a row bin by this one formula.
 __device__ __forceinline__ int fs_bin_of(float w) { return FB_TOP - (int)(__float_as_uint(w) >> 23); }
 
+// Warp 0 of a radix select: the digit (255 down to 0) whose count in S.dh holds
+// the kk-th largest key, and the rank left inside it, into S.hsel. Lane l holds
+// digits 255 - 8l down to 248 - 8l.
+__device__ __forceinline__ void fs_pick_digit(uint32_t kk, FsShared& S) {
+  const int l = lane_id();
+  uint32_t c8[8], s = 0u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c8[j] = S.dh[255 - 8 * l - j];
+    s += c8[j];
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (l >= o) incl += t;
+  }
+  const uint32_t excl = incl - s;
+  if (excl < kk && kk <= incl) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (run + c8[j] >= kk) {
+        S.hsel[0] = (uint32_t)(255 - 8 * l - j);
+        S.hsel[1] = kk - run;
+        break;
+      }
+      run += c8[j];
+    }
+  }
+}
+
 // k-th largest (1-based, k <= FT) of the CTA's per-thread 32-bit keys, by four
 // rounds of 8-bit digits (most significant first). Every thread returns it.
 __device__ __noinline__ uint32_t fs_kth_key(uint32_t key, int k, FsShared& S) {
-  const int tid = threadIdx.x, l = lane_id();
+  const int tid = threadIdx.x;
   uint32_t prefix = 0u, pmask = 0u;
   uint32_t kk = (uint32_t)k;
   for (int r = 0; r < 4; ++r) {
@@ -137,34 +173,7 @@ __device__ __noinline__ uint32_t fs_kth_key(uint32_t key, int k, FsShared& S) {
     __syncthreads();
     if ((key & pmask) == prefix) atomicAdd(&S.dh[(key >> sh) & 255u], 1u);
     __syncthreads();
-    if (tid < 32) {
-      // lane l holds digits 255 - 8l down to 248 - 8l
-      uint32_t c8[8], s = 0u;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c8[j] = S.dh[255 - 8 * l - j];
-        s += c8[j];
-      }
-      uint32_t incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (l >= o) incl += t;
-      }
-      const uint32_t excl = incl - s;
-      if (excl < kk && kk <= incl) {
-        uint32_t run = excl;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (run + c8[j] >= kk) {
-            S.hsel[0] = (uint32_t)(255 - 8 * l - j);
-            S.hsel[1] = kk - run;
-            break;
-          }
-          run += c8[j];
-        }
-      }
-    }
+    if (tid < 32) fs_pick_digit(kk, S);
     __syncthreads();
     prefix |= S.hsel[0] << sh;
     pmask |= 255u << sh;
@@ -177,7 +186,7 @@ __device__ __noinline__ uint32_t fs_kth_key(uint32_t key, int k, FsShared& S) {
 // Value key (upper 32 bits) of the k-th largest of the n composites a[0, n)
 // (k <= n), by four rounds of 8-bit digits over the list. Every thread returns it.
 __device__ __noinline__ uint32_t fs_kth_listed(const unsigned long long* a, int n, int k, FsShared& S) {
-  const int tid = threadIdx.x, l = lane_id();
+  const int tid = threadIdx.x;
   uint32_t prefix = 0u, pmask = 0u;
   uint32_t kk = (uint32_t)k;
   for (int r = 0; r < 4; ++r) {
@@ -190,33 +199,7 @@ __device__ __noinline__ uint32_t fs_kth_listed(const unsigned long long* a, int 
       if ((key & pmask) == prefix) atomicAdd(&S.dh[(key >> sh) & 255u], 1u);
     }
     __syncthreads();
-    if (tid < 32) {
-      uint32_t c8[8], s = 0u;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c8[j] = S.dh[255 - 8 * l - j];
-        s += c8[j];
-      }
-      uint32_t incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (l >= o) incl += t;
-      }
-      const uint32_t excl = incl - s;
-      if (excl < kk && kk <= incl) {
-        uint32_t run = excl;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (run + c8[j] >= kk) {
-            S.hsel[0] = (uint32_t)(255 - 8 * l - j);
-            S.hsel[1] = kk - run;
-            break;
-          }
-          run += c8[j];
-        }
-      }
-    }
+    if (tid < 32) fs_pick_digit(kk, S);
     __syncthreads();
     prefix |= S.hsel[0] << sh;
     pmask |= 255u << sh;
@@ -287,18 +270,16 @@ __device__ __noinline__ void fs_push_over(float4 x, int v, float c, float nRc, F
   }
 }
 
-// Streams the row once (double-buffered waves of FPF vectors per thread).
-// Returns this thread's maximum; *nan is set on NaN or +inf. Top-k rows list the
-// logits >= *thr (set from the first wave); no-truncation rows leave the thread's
-// running maximum and sum in *mt / *st; top-p rows fill the bins.
-template <int CLS>
-__device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float c, FsShared& S,
-                                        unsigned long long* list, float* bins, float* thr, float* mt,
-                                        float* st, float* Rout, bool* nan) {
+// One pass over a top-p row (double-buffered waves of FPF vectors per thread in
+// registers: the bins fill the shared memory). Returns this thread's maximum and
+// the first wave's block maximum R in *Rout; *nan is set on NaN or +inf. Each
+// weight 2^((z - R) c) is added to the thread's bin of its binade; weights above
+// the bins are listed (S.olist), and more than FOCAP of them raise FS_OVER.
+__device__ __noinline__ float fs_stream_topp(const float4* src, int nv, float c, FsShared& S, float* bins,
+                                             float* Rout, bool* nan) {
   const int tid = threadIdx.x, l = lane_id();
-  // top-k rows are read once (their kept tokens are listed); the others are read
-  // again by refinement or sampling passes
-  const uint64_t pol = CLS == FC_TOPK ? policy_evict_first() : policy_evict_last();
+  // read again by the refinement passes: kept in L2 ahead of rows read once
+  const uint64_t pol = policy_evict_last();
   float4 cur[FPF], nxt[FPF];
   const float4 NEG = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
@@ -316,13 +297,12 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
       tmax = fmaxf(tmax, z);
       bad |= !(z == z) || z == INFINITY;
     }
-  // the second wave is in flight while the block agrees on R and the threshold
+  // the second wave is in flight while the block agrees on R
 #pragma unroll
   for (int p = 0; p < FPF; ++p) {
     const int q = tid + FPF * FT + p * FT;
     nxt[p] = q < nv ? fs_ld(src + q, pol) : NEG;
   }
-  // first-wave block maximum R; top-k threshold: k-th largest thread maximum
   float fm = tmax;
 #pragma unroll
   for (int o = 16; o; o >>= 1) fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, o));
@@ -339,11 +319,7 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
   __syncthreads();
   const float R = key_to_float(S.cmax);
   *Rout = R;
-  float th = -INFINITY;
-  if (CLS == FC_TOPK) th = key_to_float(fs_kth_key(okey(tmax), k, S));
-  *thr = th;
   const float nRc = -(R * c);
-  float m_t = -INFINITY, s_t = 0.0f;
   uint32_t over = 0u;
   for (int q0 = tid; q0 < nv; q0 += FPF * FT) {
 #pragma unroll
@@ -354,27 +330,15 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
       const float vm = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
       tmax = fmaxf(tmax, vm);
       bad |= !(x.x == x.x) || !(x.y == x.y) || !(x.z == x.z) || !(x.w == x.w) || vm == INFINITY;
-      if (CLS == FC_TOPK) {
-        if (vm >= th) fs_push(x, q, th, S, list);
-      } else if (CLS == FC_ALL) {
-        if (vm > m_t) {
-          s_t = m_t > -INFINITY ? s_t * ex2_approx((m_t - vm) * c) : 0.0f;
-          m_t = vm;
-        }
-        const float nmc = -(m_t * c);
-        s_t += (ex2_approx(fmaf(x.x, c, nmc)) + ex2_approx(fmaf(x.y, c, nmc))) +
-               (ex2_approx(fmaf(x.z, c, nmc)) + ex2_approx(fmaf(x.w, c, nmc)));
-      } else {
-        bool ov = false;
+      bool ov = false;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float w = ex2_approx(fmaf(fs_at(x, e), c, nRc));
-          const int bb = fs_bin_of(w);
-          ov |= bb < 0;
-          bins[min(max(bb, 0), FNB - 1) * FT + tid] += bb >= 0 ? w : 0.0f;
-        }
-        if (ov) fs_push_over(x, q, c, nRc, S, &over);
+      for (int e = 0; e < 4; ++e) {
+        const float w = ex2_approx(fmaf(fs_at(x, e), c, nRc));
+        const int bb = fs_bin_of(w);
+        ov |= bb < 0;
+        bins[min(max(bb, 0), FNB - 1) * FT + tid] += bb >= 0 ? w : 0.0f;
       }
+      if (ov) fs_push_over(x, q, c, nRc, S, &over);
     }
 #pragma unroll
     for (int p = 0; p < FPF; ++p) cur[p] = nxt[p];
@@ -385,8 +349,6 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
     }
   }
   if (over) atomicOr(&S.rflags, FS_OVER);
-  *mt = m_t;
-  *st = s_t;
   *nan = bad;
   return tmax;
 }
@@ -394,13 +356,15 @@ __device__ __noinline__ float fs_stream(const float4* src, int nv, int k, float 
 // One pass over a top-k or untruncated row through a ring of FRS shared-memory
 // stages of 16 KB, filled by bulk copies (one thread issues them; FRS - 1 stages
 // stay in flight while the CTA reads one), so that a CTA keeps 48 KB of the row in
-// flight without registers. Same results as fs_stream<CLS>: the thread maximum,
-// the first two stages' block maximum R, the top-k threshold and candidate list,
-// or the running (max, sum). Every wait is bounded; on a timeout the row is marked
-// (S.rtimeout) after the copies in flight have landed.
+// flight without registers. Returns the thread maximum, with the first two
+// stages' block maximum R; top-k rows list the logits at or above the k-th
+// largest thread maximum of those stages, untruncated rows leave the thread's
+// running (max, sum) in *mt / *st.
+// Every wait is bounded; on a timeout the row is marked (S.rtimeout) after the
+// copies in flight have landed.
 template <int CLS>
 __device__ __noinline__ float fs_stream_ring(const float4* src, int nv, int k, float c, FsShared& S,
-                                             unsigned long long* list, float4* ring, float* thr, float* mt,
+                                             unsigned long long* list, float4* ring, float* mt,
                                              float* st, float* Rout, bool* nan) {
   const int tid = threadIdx.x, l = lane_id();
   const int nst = (nv + FRV - 1) / FRV;
@@ -449,7 +413,6 @@ __device__ __noinline__ float fs_stream_ring(const float4* src, int nv, int k, f
   *Rout = R;
   float th = -INFINITY;
   if (CLS == FC_TOPK) th = key_to_float(fs_kth_key(okey(tmax), k, S));
-  *thr = th;
   float m_t = -INFINITY, s_t = 0.0f;
   for (int s = 0; s < nst; ++s) {
     const int slot = s % FRS;
@@ -612,15 +575,15 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
     for (int j = 0; j < FNB; ++j) bins[j * FT + tid] = 0.0f;
     __syncthreads();
   }
-  float thr, mt, st, R;
+  float mt, st, R;
   bool nan;
   float tm;
   // top-k and untruncated rows stream through a bulk-copy ring placed after the
   // candidate list (its first FLCAP entries)
   float4* ring = reinterpret_cast<float4*>(list + FLCAP);
-  if (cls == FC_TOPK) tm = fs_stream_ring<FC_TOPK>(src, nv, k, c, S, list, ring, &thr, &mt, &st, &R, &nan);
-  else if (cls == FC_ALL) tm = fs_stream_ring<FC_ALL>(src, nv, k, c, S, list, ring, &thr, &mt, &st, &R, &nan);
-  else tm = fs_stream<FC_TOPP>(src, nv, k, c, S, list, bins, &thr, &mt, &st, &R, &nan);
+  if (cls == FC_TOPK) tm = fs_stream_ring<FC_TOPK>(src, nv, k, c, S, list, ring, &mt, &st, &R, &nan);
+  else if (cls == FC_ALL) tm = fs_stream_ring<FC_ALL>(src, nv, k, c, S, list, ring, &mt, &st, &R, &nan);
+  else tm = fs_stream_topp(src, nv, c, S, bins, &R, &nan);
 #pragma unroll
   for (int o = 16; o; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
   if (l == 0) S.fmax[w] = tm;
