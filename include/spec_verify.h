@@ -169,7 +169,9 @@ sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logit
                               void* stream /* cudaStream_t */);
 
 /* The truncated distribution of R independent rows, through the same device
- * code as spec_verify (a test and inspection hook).
+ * code as spec_verify (a test and inspection hook): bf16 rows, 16-byte aligned,
+ * R >= 16, through the key-histogram verify path's per-row code; otherwise, and
+ * for the rows that code hands back, the cluster kernel.
  *   logits [R, V] dtype; temperature/top_k/top_p [R] (per row);
  *   out_probs [R, V] float (written): p(x) = weight(x) / kept mass for kept
  *   tokens, 0 elsewhere; for temperature == 0 rows, 1 at the argmax.

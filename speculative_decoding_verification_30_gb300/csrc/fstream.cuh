@@ -123,6 +123,10 @@ __device__ __forceinline__ void fs_prefetch_l2(const void* p, size_t n) {
 __device__ __forceinline__ float fs_at(const float4& v, int e) {
   return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
 }
+// y = (z - R) c, the log2 weight of logit z against the reference R: formed as a
+// difference then a product (not z c - R c), so that a large |R c| adds no
+// rounding error; every pass over a row uses this one formula.
+__device__ __forceinline__ float fs_y(float z, float R, float c) { return __fmul_rn(__fsub_rn(z, R), c); }
 // Coarse bin of a weight w = 2^y (y = (z - R) c relative to the first-wave
 // maximum R), from w's exponent field: bin j holds w in [2^(23 - j), 2^(24 - j)),
 // a negative value is above the bins (w >= 2^24), and everything below the last
@@ -256,12 +260,12 @@ constexpr int FC_TOPK = 0, FC_ALL = 1, FC_TOPP = 2;
 // Lists the logits of vector v whose weight 2^((z - R) c) lies above the bins
 // (2^24 or more times the first-wave maximum's): their masses are taken exactly
 // after the stream. Sets *over when the list is full.
-__device__ __noinline__ void fs_push_over(float4 x, int v, float c, float nRc, FsShared& S,
+__device__ __noinline__ void fs_push_over(float4 x, int v, float c, float R, FsShared& S,
                                           uint32_t* over) {
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float z = fs_at(x, e);
-    if (fs_bin_of(ex2_approx(fmaf(z, c, nRc))) >= 0) continue;
+    if (fs_bin_of(ex2_approx(fs_y(z, R, c))) >= 0) continue;
     const uint32_t slot = atomicAdd(&S.ocount, 1u);
     if (slot < (uint32_t)FOCAP)
       S.olist[slot] = ((unsigned long long)okey(z) << 32) | (uint32_t)~(uint32_t)(4 * v + e);
@@ -319,7 +323,6 @@ __device__ __noinline__ float fs_stream_topp(const float4* src, int nv, float c,
   __syncthreads();
   const float R = key_to_float(S.cmax);
   *Rout = R;
-  const float nRc = -(R * c);
   uint32_t over = 0u;
   for (int q0 = tid; q0 < nv; q0 += FPF * FT) {
 #pragma unroll
@@ -333,12 +336,12 @@ __device__ __noinline__ float fs_stream_topp(const float4* src, int nv, float c,
       bool ov = false;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float w = ex2_approx(fmaf(fs_at(x, e), c, nRc));
+        const float w = ex2_approx(fs_y(fs_at(x, e), R, c));
         const int bb = fs_bin_of(w);
         ov |= bb < 0;
         bins[min(max(bb, 0), FNB - 1) * FT + tid] += bb >= 0 ? w : 0.0f;
       }
-      if (ov) fs_push_over(x, q, c, nRc, S, &over);
+      if (ov) fs_push_over(x, q, c, R, S, &over);
     }
 #pragma unroll
     for (int p = 0; p < FPF; ++p) cur[p] = nxt[p];
@@ -433,9 +436,8 @@ __device__ __noinline__ float fs_stream_ring(const float4* src, int nv, int k, f
             s_t = m_t > -INFINITY ? s_t * ex2_approx((m_t - vm) * c) : 0.0f;
             m_t = vm;
           }
-          const float nmc = -(m_t * c);
-          s_t += (ex2_approx(fmaf(x.x, c, nmc)) + ex2_approx(fmaf(x.y, c, nmc))) +
-                 (ex2_approx(fmaf(x.z, c, nmc)) + ex2_approx(fmaf(x.w, c, nmc)));
+          s_t += (ex2_approx(fs_y(x.x, m_t, c)) + ex2_approx(fs_y(x.y, m_t, c))) +
+                 (ex2_approx(fs_y(x.z, m_t, c)) + ex2_approx(fs_y(x.w, m_t, c)));
         }
       }
     }
@@ -470,7 +472,7 @@ __device__ __noinline__ float fs_stream_ring(const float4* src, int nv, int k, f
 // bin j with the bin's logits listed (PASS 2), or the list of sub-bin s of bin j
 // (PASS 3). List slots are taken per warp; nothing is written past FLCAP.
 template <int PASS>
-__device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float nRc, float scale, int j,
+__device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float R, float scale, int j,
                                        int s, FsShared& S, unsigned long long* list) {
   const int tid = threadIdx.x, l = lane_id();
   const uint32_t below = (1u << l) - 1u;
@@ -500,7 +502,7 @@ __device__ __noinline__ void fs_refine(const float4* src, int nv, float c, float
       float w4[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float y = fmaf(fs_at(cur[p], e), c, nRc);
+        const float y = fs_y(fs_at(cur[p], e), R, c);
         w4[e] = 0.0f;
         if (q < nv && y >= ylo && y < yhi) {
           w4[e] = ex2_approx(y);
@@ -735,8 +737,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
       for (int i = tid; i < FNSUB; i += FT) S.smass[i] = 0ull;
       if (tid == 0) S.lcount = 0u;
       __syncthreads();
-      const float nRc = -(R * c);
-      fs_refine<2>(src, nv, c, nRc, scale, js, 0, S, list);
+      fs_refine<2>(src, nv, c, R, scale, js, 0, S, list);
       __syncthreads();
       KH_MARK(S.item, 2);
       if (tid == 0) {
@@ -769,7 +770,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
         sel = list + FLCAP;
         for (int i = tid; i < (int)nbin; i += FT) {
           const unsigned long long e = list[i];
-          const float wv = ex2_approx(fmaf(fs_key_value(e), c, nRc));
+          const float wv = ex2_approx(fs_y(fs_key_value(e), R, c));
           if ((int)((__float_as_uint(wv) >> 15) & 255u) == ss) sel[atomicAdd((uint32_t*)&S.ncut, 1u)] = e;
         }
         __syncthreads();
@@ -779,7 +780,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
         __syncthreads();
         if (tid == 0) S.lcount = 0u;
         __syncthreads();
-        fs_refine<3>(src, nv, c, nRc, scale, js, ss, S, list);
+        fs_refine<3>(src, nv, c, R, scale, js, ss, S, list);
         __syncthreads();
         nl = S.lcount;
       }
@@ -799,7 +800,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
       const int ept = ((int)nl + FT - 1) / FT;
       const int i0 = min(tid * ept, (int)nl), i1 = min(i0 + ept, (int)nl);
       unsigned long long own = 0ull;
-      for (int i = i0; i < i1; ++i) own += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
+      for (int i = i0; i < i1; ++i) own += fix_pow2(ex2_approx(fs_y(fs_key_value(list[i]), R, c)) * scale, FIX);
       if (tid == 0) S.jstar = 0;
       unsigned long long wtot;
       unsigned long long ex = S.mabove + kh_below<unsigned long long>(own, S.s64, &wtot);
@@ -808,7 +809,7 @@ __device__ __noinline__ KhRow fs_row(const float* row, int V, float T, int k, fl
       for (int i = i0; i < i1; ++i) {
         if (ex > Y) break;
         lastk = i;
-        ex += fix_pow2(ex2_approx(fmaf(fs_key_value(list[i]), c, nRc)) * scale, FIX);
+        ex += fix_pow2(ex2_approx(fs_y(fs_key_value(list[i]), R, c)) * scale, FIX);
         zk = ex;
       }
       if (lastk > 0) atomicMax(&S.jstar, lastk);

@@ -104,7 +104,7 @@ def _probs_case(rows, T, k, P):
     return worst, cut_near
 
 
-@pytest.mark.parametrize("name,B", [("tiny", 4), ("mtp_decode", 16), ("nucleus_batch", 4),
+@pytest.mark.parametrize("name,B", [("tiny", 16), ("mtp_decode", 16), ("nucleus_batch", 4),
                                     ("mixed", 4)])
 @pytest.mark.parametrize("side", ["target", "draft"])
 def test_truncated_probs_match_oracle(name, B, side):
@@ -134,6 +134,28 @@ def test_truncated_probs_edge_shapes(dtype, V):
               (0.8, V - 1, 1.0), (1.0, 0, 0.5)]
     T = torch.tensor([p[0] for p in params])
     k = torch.tensor([p[1] for p in params], dtype=torch.int32)
+    P = torch.tensor([p[2] for p in params])
+    worst, cut_b = _probs_case(rows, T, k, P)
+    assert worst < PROB_TOL, worst
+
+
+@pytest.mark.parametrize("V", [4, 1000, 4096, 151_936])
+def test_truncated_probs_fp32_rows_edge_cases(V):
+    # 24 fp32 rows: ties, -inf, a top-k cut inside a run of equal logits, a maximum
+    # far above the first load wave, flat rows, tiny and large temperatures
+    g = torch.Generator().manual_seed(V + 5)
+    rows = torch.randn(24, V, generator=g) * 2
+    rows[1] = torch.round(rows[1])                                   # many ties
+    rows[2, : V // 2] = -float("inf")
+    rows[3] = torch.randn(V, generator=g) * 0.05                     # flat
+    if V > 8:
+        rows[4, -3:] = 60.0                                          # far above the first wave
+        rows[5, V // 3: V // 3 + V // 4] = 1.5                       # a long run of equal logits
+    params = [(1.0, 0, 0.9), (0.7, 5, 1.0), (1.3, 0, 0.8), (0.5, 3, 0.5), (2.0, V, 0.99),
+              (1.0, 1, 1.0), (0.9, 0, 0.05), (1e-3, 0, 1.0), (50.0, 0, 0.9), (1.0, 2, 0.999),
+              (0.8, V - 1, 1.0), (1.0, 0, 0.5)] * 2
+    T = torch.tensor([p[0] for p in params])
+    k = torch.tensor([p[1] for p in params], dtype=torch.int32)   # k = V - 1 > 256: handed back
     P = torch.tensor([p[2] for p in params])
     worst, cut_b = _probs_case(rows, T, k, P)
     assert worst < PROB_TOL, worst
@@ -303,6 +325,33 @@ def test_verify_top_p_with_maximum_far_above_the_first_wave():
     res = oracle_verify(tgt, drf, dtok, T, k, P, 4, 12, parallel=False)
     rep = compare(out.cpu(), n.cpu(), res, T)
     assert not rep.bad_mismatches, rep.bad_mismatches
+
+
+def test_verify_fp32_large_logits_and_small_temperatures():
+    # fp32 rows offset by hundreds and low temperatures: (z - m) c must not pick up
+    # the rounding of z c and m c separately (|m c| reaches 1e5 here)
+    V, K, B = 8192, 2, 8
+    g = torch.Generator().manual_seed(123)
+    tgt = torch.randn(B, K + 1, V, generator=g) * 3 + 400.0
+    drf = 0.6 * tgt[:, :K] + 0.4 * (torch.randn(B, K, V, generator=g) * 3 + 400.0)
+    T = torch.tensor([0.01, 0.003, 0.05, 0.2, 0.01, 1.0, 0.02, 0.004])
+    # drafted tokens the draft could have produced: its top token at the lowest
+    # temperatures (where every other weight is below fp32's range on both rows),
+    # its second one elsewhere
+    ranks = drf.argsort(dim=-1, descending=True)
+    dtok = torch.where((T < 0.05)[:, None], ranks[..., 0], ranks[..., 1]).to(torch.int32)
+    k = torch.tensor([0, 0, 20, 0, 50, 0, 0, 5], dtype=torch.int32)
+    P = torch.tensor([0.9, 1.0, 0.95, 0.8, 1.0, 0.99, 0.5, 1.0])
+    out, n = sv.spec_verify(tgt.to(DEV), drf.to(DEV), dtok.to(DEV), T.to(DEV), k.to(DEV),
+                            P.to(DEV), seed=6, offset=2)
+    res = oracle_verify(tgt, drf, dtok, T, k, P, 6, 2, parallel=False)
+    rep = compare(out.cpu(), n.cpu(), res, T)
+    assert not rep.bad_mismatches, rep.bad_mismatches
+    # the same rows' truncated probabilities
+    rows = tgt.reshape(-1, V)
+    worst, _ = _probs_case(rows, T.repeat_interleave(K + 1), k.repeat_interleave(K + 1),
+                           P.repeat_interleave(K + 1))
+    assert worst < PROB_TOL, worst
 
 
 def test_data_errors_are_reported_in_band():
