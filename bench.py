@@ -279,6 +279,75 @@ def other_workloads(args, dev, peak):
     return res
 
 
+def measured_bf16_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def greedy_from_hidden(dev, steps: int = 20, warmup: int = 3):
+    """The greedy batch's shape computed from hidden states (B = 256, K = 3,
+    V = 151,936, d = 1,024, bf16): the LM-head GEMM with the argmax epilogue and
+    the acceptance kernel (spec_verify_greedy_from_hidden, no logit row written)
+    against the GEMM writing fp32 rows followed by spec_verify on them
+    (spec_verify_from_hidden). CUDA events around each call; W (311 MB) is larger
+    than L2."""
+    import torch
+    import speculative_decoding_verification_30_gb300 as sv
+    from speculative_decoding_verification_30_gb300.workloads import hidden_batch
+    B, K, V, d = 256, 3, 151_936, 1024
+    h, W = hidden_batch(B, K + 1, d, V, seed=1, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    dtok = torch.randint(0, V, (B, K), generator=g, device=dev, dtype=torch.int32)
+    ws = sv.Workspace(B, K, dev)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    ot, on = torch.empty(B, K + 1, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev)
+    ot2, on2 = torch.empty_like(ot), torch.empty_like(on)
+    scratch = torch.empty(B * (2 * K + 1) * V, dtype=torch.float32, device=dev)
+    T = torch.zeros(B, device=dev)
+    kk = torch.zeros(B, dtype=torch.int32, device=dev)
+    P = torch.ones(B, device=dev)
+
+    def fused():
+        sv.spec_verify_greedy_from_hidden(h, W, dtok, flag=flag, out_tokens=ot, out_n=on, workspace=ws)
+
+    def unfused():
+        sv.spec_verify_from_hidden(h, W, None, None, dtok, T, kk, P, logits_scratch=scratch, flag=flag,
+                                   out_tokens=ot2, out_n=on2, workspace=ws)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    clk = ClockSampler(dev.index or 0)
+    with clk:
+        ms_f = timed(fused)
+        ms_u = timed(unfused)
+    agree = bool(torch.equal(ot, ot2) and torch.equal(on, on2)) and int(flag.item()) == 0
+    flops = 2.0 * B * (K + 1) * V * d
+    peak, src = measured_bf16_tflops()
+    tf = flops / (ms_f / 1e3) / 1e12
+    del scratch
+    return {"config": {"B": B, "K": K, "V": V, "d": d, "hidden": "bf16 0.5 N(0,1)",
+                       "weight": "bf16 0.1 N(0,1)", "drafted": "random ids"},
+            "fused_ms": ms_f, "unfused_ms": ms_u, "speedup": ms_u / ms_f,
+            "fused_TFLOPs": tf, "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
+                                             "unit": "TFLOP/s", "frac": tf / peak, "peak_source": src},
+            "logit_bytes_not_written": B * (K + 1) * V * 4, "fused_equals_unfused": agree,
+            "clocks": clk.summary(), "steps": steps}
+
+
 def bench_gpu(args):
     import torch
     import torch.distributed as dist
@@ -395,6 +464,8 @@ def bench_gpu(args):
         del sets
         torch.cuda.empty_cache()
         line["other_workloads"] = other_workloads(args, dev, peak)
+        torch.cuda.empty_cache()
+        line["other_workloads"]["greedy_from_hidden"] = greedy_from_hidden(dev)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if rank == 0:

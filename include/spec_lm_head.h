@@ -12,7 +12,9 @@
  * The GEMM kernel runs on the 5th-generation tensor cores: tcgen05.mma with
  * TMA-staged operands (128-byte swizzle) and a TMEM accumulator. Its logits are
  * checked against the float64 oracle within the fp32 accumulation bound, and the
- * verify step fed from it against the oracle's verify on those logits.
+ * verify step fed from it against the oracle's verify on those logits. For a
+ * greedy batch the projection and the token choice are fused: the GEMM's
+ * epilogue keeps only each row's first maximum, so no logit row is written.
  */
 #ifndef SPEC_LM_HEAD_H
 #define SPEC_LM_HEAD_H
@@ -67,6 +69,43 @@ sv_status spec_verify_from_hidden(const void* hidden_target, const void* weight_
                                   uint64_t philox_offset, int B, int K, int V, float* logits_scratch,
                                   int32_t* flag, int32_t* out_tokens, int32_t* out_n_accepted,
                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* The greedy (temperature 0) verify step fused with the LM head: the target
+ * logits are never written to memory.
+ * What the pages define: the decode step chooses the token from the row z = h .
+ * W^T ("Apple Silikon İçin Cihaz Üstü Çıkarımı Optimize Etme", decode section; its
+ * section on the limits of further optimisation tried fusing this projection
+ * with the token choice), and greedy verification compares each drafted token
+ * with the target argmax ("after three fixes, Qwen3.5/3.6 MTP head reaches 1.4x
+ * on Apple Silicon", deniz.in, section "Verification under sampling was wrong"):
+ * the drafted tokens are kept while each equals its row's argmax, and the target
+ * argmax is emitted at the first mismatch or after the K-th position.
+ *   hidden_target [B][K+1][d] bf16, device, 16-byte aligned: the target's final
+ *                 hidden states at positions 0..K
+ *   weight        [V][d] bf16, device, 16-byte aligned: the LM-head weight
+ *   draft_tokens  [B][K] int32, device: the drafted ids
+ *   flag          [1] int32, device, caller-owned: set to 1 when a wait of the
+ *                 GEMM timed out; the results are then not valid. The caller
+ *                 zeroes it before the call.
+ *   out_tokens [B][K+1], out_n_accepted [B]: as spec_verify with every temperature
+ *                 0: n drafted tokens, then the target argmax, then -1; a row whose
+ *                 maximum is NaN or +inf or whose logits are all -inf, or a drafted
+ *                 id outside [0, V), gives n = -1 and K+1 tokens -1.
+ *   workspace     spec_verify_workspace_bytes(B, K) bytes, 16-byte aligned and
+ *                 zero-filled, left zero-filled (its first B(K+1) 64-bit words
+ *                 hold the rows' keys during the call).
+ * The argmax is that of the fp32-accumulated logits (lowest id among equal
+ * maxima); it can differ from the exact dot products' only where two logits lie
+ * within the fp32 accumulation bound of spec_lm_head_logits.
+ * Limits: 1 <= B <= 65535, 1 <= K <= 16, 2 <= V <= 262144, d a positive multiple
+ * of 64 and at most 65,536. Returns SV_ERR_NULL, SV_ERR_SHAPE, SV_ERR_ALIGN or
+ * SV_ERR_WORKSPACE before launching anything; SV_ERR_CUDA when the tensor-map
+ * encoder or a launch fails; SV_OK once the GEMM and the acceptance kernel are
+ * queued on `stream`. */
+sv_status spec_verify_greedy_from_hidden(const void* hidden_target, const void* weight, int d,
+                                         const int32_t* draft_tokens, int B, int K, int V, int32_t* flag,
+                                         int32_t* out_tokens, int32_t* out_n_accepted, void* workspace,
+                                         size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

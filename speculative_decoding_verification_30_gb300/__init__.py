@@ -17,7 +17,8 @@ from ._build import LIB, build
 
 __all__ = ["load", "spec_verify", "spec_verify_noalloc", "spec_verify_workspace_bytes",
            "spec_truncated_probs", "NOALLOC_SCRATCH_BYTES",
-           "spec_sample", "spec_philox_uniforms", "spec_lm_head_logits", "spec_verify_from_hidden", "sv_version", "Workspace", "SV_BF16", "SV_F32", "SpecVerifyError"]
+           "spec_sample", "spec_philox_uniforms", "spec_lm_head_logits", "spec_verify_from_hidden",
+           "spec_verify_greedy_from_hidden", "sv_version", "Workspace", "SV_BF16", "SV_F32", "SpecVerifyError"]
 
 SV_BF16, SV_F32 = 0, 1
 _STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "workspace", 5: "cuda",
@@ -64,6 +65,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_from_hidden.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, u64, u64, i32,
                                             i32, i32, vp, vp, vp, vp, vp, sz, vp]
     lib.spec_verify_from_hidden.restype = i32
+    lib.spec_verify_greedy_from_hidden.argtypes = [vp, vp, i32, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.spec_verify_greedy_from_hidden.restype = i32
     lib.sv_status_string.argtypes = [i32]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_version.argtypes = []
@@ -266,7 +269,7 @@ def spec_lm_head_logits(hidden: torch.Tensor, weight: torch.Tensor, out: torch.T
                         flag: torch.Tensor | None = None, stream=None):
     """logits [..., V] fp32 = hidden [..., d] . weight [V, d]^T on the tensor cores
     (bf16 operands). Returns (logits, flag); flag [1] int32 becomes 1 if a wait of
-    the kernel timed out. The kernel has not yet been run on a GPU."""
+    the kernel timed out."""
     d = hidden.shape[-1]
     V = weight.shape[0]
     if weight.dim() != 2 or weight.shape[1] != d:
@@ -323,4 +326,35 @@ def spec_verify_from_hidden(hidden_target: torch.Tensor, weight_target: torch.Te
         _dev(out_tokens, "out_tokens", torch.int32), _dev(out_n, "out_n", torch.int32),
         workspace.buf.data_ptr(), workspace.nbytes, _stream(stream))
     _check(st, "spec_verify_from_hidden")
+    return out_tokens, out_n, flag
+
+
+def spec_verify_greedy_from_hidden(hidden_target: torch.Tensor, weight: torch.Tensor,
+                                   draft_tokens: torch.Tensor, flag: torch.Tensor | None = None,
+                                   out_tokens: torch.Tensor | None = None, out_n: torch.Tensor | None = None,
+                                   workspace: "Workspace | None" = None, stream=None):
+    """Greedy (temperature 0) verify fused with the LM head: hidden_target
+    [B, K+1, d] and weight [V, d] (bf16) give the target rows, whose argmax the
+    GEMM epilogue keeps without writing the logits. Returns (out_tokens, out_n,
+    flag); the results are valid only when flag stays 0."""
+    B, K1, d = hidden_target.shape
+    K = K1 - 1
+    V = weight.shape[0]
+    if weight.dim() != 2 or weight.shape[1] != d:
+        raise SpecVerifyError("weight must be [V, d] with the hidden states' d")
+    dev = hidden_target.device
+    if flag is None:
+        flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    if out_n is None:
+        out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = Workspace(B, K, dev)
+    st = load().spec_verify_greedy_from_hidden(
+        _dev(hidden_target, "hidden_target", torch.bfloat16), _dev(weight, "weight", torch.bfloat16), d,
+        _dev(draft_tokens, "draft_tokens", torch.int32), B, K, V, _dev(flag, "flag", torch.int32),
+        _dev(out_tokens, "out_tokens", torch.int32), _dev(out_n, "out_n", torch.int32),
+        workspace.buf.data_ptr(), workspace.nbytes, _stream(stream))
+    _check(st, "spec_verify_greedy_from_hidden")
     return out_tokens, out_n, flag

@@ -9,8 +9,10 @@
 // (128-byte swizzle, one 64-element K slice per stage) into a 4-stage ring; one
 // thread issues tcgen05.mma (M = 128, N = 256, K = 16) into a 256-column TMEM
 // accumulator; the four warps read it back with tcgen05.ld (warp w owns TMEM lanes
-// 32w..32w+31, i.e. those output rows) and store fp32 rows. Every wait is bounded:
-// a timeout sets the caller's flag, the CTA lets its issued copies land and frees
+// 32w..32w+31, i.e. those output rows) and either store fp32 rows or, for the
+// greedy verify step, reduce them to each row's maximum and the lowest column
+// holding it, so that the logits never reach memory. Every wait is bounded: a
+// timeout sets the caller's flag, the CTA lets its issued copies land and frees
 // its TMEM before it returns.
 //
 #include <cuda.h>
@@ -108,9 +110,26 @@ __device__ __forceinline__ void commit(unsigned long long* bar) {
                : "memory");
 }
 
+// Epilogues: EPI_STORE writes the fp32 logit tile to Z; EPI_ARGMAX reduces each
+// row of the tile to (order key of its maximum << 32 | ~lowest column holding
+// it) and merges that into keys[row] with a 64-bit atomicMax, so the largest key
+// over all column tiles names the row's first maximum. NaN takes the largest
+// order key, so a row holding one reads as NaN.
+constexpr int EPI_STORE = 0, EPI_ARGMAX = 1;
+
+// Order-preserving 32-bit key of an fp32 value (NaN: 0xFFFFFFFF).
+__device__ __forceinline__ uint32_t order_key(uint32_t u) {
+  if (__uint_as_float(u) != __uint_as_float(u)) return 0xFFFFFFFFu;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+constexpr uint32_t KEY_NEG_INF = 0x007FFFFFu;   // order_key(-inf)
+constexpr uint32_t KEY_POS_INF = 0xFF800000u;   // order_key(+inf)
+
+template <int EPI>
 __global__ void __launch_bounds__(128, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapW,
-                   float* __restrict__ Z, int M, int N, int d, int32_t* flag) {
+                   float* __restrict__ Z, unsigned long long* __restrict__ keys, int M, int N, int d,
+                   int32_t* flag) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -181,6 +200,7 @@ __global__ void __launch_bounds__(128, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (ok) {
     const int row = m0 + warp * 32 + lane;
+    uint32_t bkey = 0u, bcol = 0u;   // EPI_ARGMAX: the thread's best order key and its column
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
@@ -197,7 +217,18 @@ __global__ void __launch_bounds__(128, 1)
           : "r"(ta));
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       const int col = n0 + c * 32;
-      if (row < M && col < N) {
+      if (EPI == EPI_ARGMAX) {
+        // ascending columns and a strict comparison: the first maximum is kept
+        const int lim = min(32, N - col);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t key = order_key(r[j]);
+          if (j < lim && key > bkey) {
+            bkey = key;
+            bcol = (uint32_t)(col + j);
+          }
+        }
+      } else if (row < M && col < N) {
         float* zr = Z + (size_t)row * N + col;
         const int lim = min(32, N - col);
         if (lim == 32 && (reinterpret_cast<uintptr_t>(zr) & 15) == 0) {
@@ -210,6 +241,8 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     }
+    if (EPI == EPI_ARGMAX && row < M && bkey != 0u)
+      atomicMax(keys + row, ((unsigned long long)bkey << 32) | (unsigned long long)(~bcol));
   }
   // after a timeout, the copies issued but never consumed land before the CTA leaves
   if (warp == 0 && lane == 0 && C.err) {
@@ -224,6 +257,40 @@ __global__ void __launch_bounds__(128, 1)
                  : "memory");
   }
   if (tid == 0 && !ok) atomicExch(flag, 1);
+}
+
+// Greedy acceptance of sequence b from its K+1 row keys (one thread per
+// sequence): the drafted tokens are kept while each equals its row's first
+// maximum; the first row that disagrees (or row K after K matches) gives the last
+// token. A row whose maximum is NaN or +inf or whose logits are all -inf, or a
+// drafted token outside [0, V), makes the sequence a data error (n = -1, every
+// token -1). The keys are zeroed for the next call.
+__global__ void lm_greedy_kernel(unsigned long long* __restrict__ keys, const int32_t* __restrict__ dtok,
+                                 int B, int K, int V, int32_t* __restrict__ out_tokens,
+                                 int32_t* __restrict__ out_n) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int K1 = K + 1;
+  unsigned long long* kb = keys + (size_t)b * K1;
+  const int32_t* db = dtok + (size_t)b * K;
+  bool bad = false;
+  for (int q = 0; q < K; ++q) bad |= db[q] < 0 || db[q] >= V;
+  int n = 0;
+  int last = -1;
+  for (int i = 0; i < K1; ++i) {
+    const unsigned long long key = kb[i];
+    kb[i] = 0ull;
+    const uint32_t ok = (uint32_t)(key >> 32);
+    bad |= ok <= KEY_NEG_INF || ok >= KEY_POS_INF;
+    const int amax = (int)~(uint32_t)key;
+    if (n == i && last < 0) {
+      if (i < K && db[i] == amax) ++n;
+      else last = amax;
+    }
+  }
+  int32_t* ob = out_tokens + (size_t)b * K1;
+  for (int q = 0; q < K1; ++q) ob[q] = bad ? -1 : (q < n ? db[q] : (q == n ? last : -1));
+  out_n[b] = bad ? -1 : n;
 }
 
 typedef CUresult (*EncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -262,6 +329,26 @@ static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 static sv::LaunchCache g_lm_cache;
 
+// Encodes the operand maps and launches one GEMM (arguments already checked).
+template <int EPI>
+static sv_status launch_gemm(const void* hidden, const void* weight, int M, int N, int d, float* logits,
+                             unsigned long long* keys, int32_t* flag, cudaStream_t stream) {
+  CUtensorMap mh, mw;
+  if (!make_map(&mh, hidden, M, d, BM) || !make_map(&mw, weight, N, d, BN)) return SV_ERR_CUDA;
+  // the kernel's shared-memory limit, raised once per device
+  int dev = 0, done = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      g_lm_cache.get(dev, reinterpret_cast<const void*>(lm_head_kernel<EPI>), SMEM_BYTES, 0, &done, [](int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(lm_head_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_BYTES);
+      }) != cudaSuccess)
+    return SV_ERR_CUDA;
+  const dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((N + BN - 1) / BN));
+  lm_head_kernel<EPI><<<grid, 128, SMEM_BYTES, stream>>>(mh, mw, logits, keys, M, N, d, flag);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 }  // namespace svlm
 
 sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int N, int d, float* logits,
@@ -272,19 +359,8 @@ sv_status spec_lm_head_logits(const void* hidden, const void* weight, int M, int
     return SV_ERR_SHAPE;
   if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(logits, 4) || !aligned(flag, 4))
     return SV_ERR_ALIGN;
-  CUtensorMap mh, mw;
-  if (!make_map(&mh, hidden, M, d, BM) || !make_map(&mw, weight, N, d, BN)) return SV_ERR_CUDA;
-  // the kernel's shared-memory limit, raised once per device
-  int dev = 0, done = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      g_lm_cache.get(dev, reinterpret_cast<const void*>(lm_head_kernel), SMEM_BYTES, 0, &done, [](int* v) {
-        *v = 1;
-        return cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-      }) != cudaSuccess)
-    return SV_ERR_CUDA;
-  const dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((N + BN - 1) / BN));
-  lm_head_kernel<<<grid, 128, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(mh, mw, logits, M, N, d, flag);
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  return svlm::launch_gemm<svlm::EPI_STORE>(hidden, weight, M, N, d, logits, nullptr, flag,
+                                            static_cast<cudaStream_t>(stream));
 }
 
 sv_status spec_verify_from_hidden(const void* hidden_target, const void* weight_target, int d,
@@ -319,4 +395,29 @@ sv_status spec_verify_from_hidden(const void* hidden_target, const void* weight_
   return spec_verify(zt, hidden_draft ? zd : nullptr, SV_F32, draft_tokens, temperature, top_k, top_p,
                      philox_seed, philox_offset, B, K, V, out_tokens, out_n_accepted, workspace,
                      workspace_bytes, stream);
+}
+
+sv_status spec_verify_greedy_from_hidden(const void* hidden_target, const void* weight, int d,
+                                         const int32_t* draft_tokens, int B, int K, int V, int32_t* flag,
+                                         int32_t* out_tokens, int32_t* out_n_accepted, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (!hidden_target || !weight || !draft_tokens || !flag || !out_tokens || !out_n_accepted || !workspace)
+    return SV_ERR_NULL;
+  if (B < 1 || B > 65535 || K < 1 || K > 16 || V < 2 || V > 262144 || d < svlm::BK || d > 65536 ||
+      d % svlm::BK != 0)
+    return SV_ERR_SHAPE;
+  if (!svlm::aligned(hidden_target, 16) || !svlm::aligned(weight, 16) || !svlm::aligned(draft_tokens, 4) ||
+      !svlm::aligned(flag, 4) || !svlm::aligned(out_tokens, 4) || !svlm::aligned(out_n_accepted, 4))
+    return SV_ERR_ALIGN;
+  if (!svlm::aligned(workspace, 16) || workspace_bytes < spec_verify_workspace_bytes(B, K))
+    return SV_ERR_WORKSPACE;
+  // the row keys use the workspace's first B(K+1) 64-bit words (zero between calls)
+  unsigned long long* keys = static_cast<unsigned long long*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const sv_status s = svlm::launch_gemm<svlm::EPI_ARGMAX>(hidden_target, weight, B * (K + 1), V, d, nullptr,
+                                                         keys, flag, st);
+  if (s != SV_OK) return s;
+  svlm::lm_greedy_kernel<<<(B + 127) / 128, 128, 0, st>>>(keys, draft_tokens, B, K, V, out_tokens,
+                                                         out_n_accepted);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -166,3 +166,17 @@ def draft_tokens_by_rank(draft: torch.Tensor, step: int = 0, cid: int = 0,
     r = torch.clamp((-torch.log2(1.0 - u)).floor().long(), max=max_rank - 1)   # geometric
     top = torch.topk(draft.float(), max_rank, dim=-1).indices                    # [B, K, max_rank]
     return torch.gather(top, -1, r.to(top.device).unsqueeze(-1)).squeeze(-1).to(torch.int32)
+
+
+def hidden_batch(B: int, K1: int, d: int, V: int, seed: int = 0, device="cpu"):
+    """Seeded final hidden states [B, K1, d] and an LM-head weight [V, d], bf16:
+    h ~ 0.5 N(0, 1) and W ~ 0.1 N(0, 1) elementwise, so that a logit h . W_v has a
+    standard deviation of 0.05 sqrt(d). No trained weights exist here; these stand
+    in for a model's last hidden states and its output projection."""
+    g = _generator(device, 0, 6, seed)
+    h = (0.5 * torch.randn(B, K1, d, generator=g, device=device)).to(torch.bfloat16)
+    W = torch.empty(V, d, dtype=torch.bfloat16, device=device)
+    for v0 in range(0, V, 16384):                       # bounded fp32 temporaries
+        v1 = min(V, v0 + 16384)
+        W[v0:v1] = (0.1 * torch.randn(v1 - v0, d, generator=g, device=device)).to(torch.bfloat16)
+    return h, W

@@ -28,7 +28,8 @@ def test_library_builds_and_exports_every_declared_symbol():
     lib = ctypes.CDLL(path)
     names = declared_functions()
     assert {"spec_verify", "spec_verify_workspace_bytes", "spec_truncated_probs",
-            "spec_sample", "sv_status_string", "spec_lm_head_logits", "spec_verify_from_hidden"} <= set(names)
+            "spec_sample", "sv_status_string", "spec_lm_head_logits", "spec_verify_from_hidden",
+            "spec_verify_greedy_from_hidden"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -105,6 +106,15 @@ def test_lm_head_entry_points_validate_before_launching():
     assert vh(d=65) == 2 and vh(dd=100) == 2
     assert vh(z=A + 4) == 6 and vh(ht=A + 8) == 6
     assert vh(wsb=8) == 4
+
+    def gh(ht=A, w=A, d=128, dt=A, B=2, K=2, V=1024, f=A, ot=A, on=A, ws=A, wsb=wsb):
+        return lib.spec_verify_greedy_from_hidden(ht, w, d, dt, B, K, V, f, ot, on, ws, wsb, None)
+    assert gh(ht=None) == 1 and gh(w=None) == 1 and gh(dt=None) == 1 and gh(f=None) == 1
+    assert gh(ot=None) == 1 and gh(on=None) == 1 and gh(ws=None) == 1
+    assert gh(B=0) == 2 and gh(B=65536) == 2 and gh(K=0) == 2 and gh(K=17) == 2
+    assert gh(V=1) == 2 and gh(V=262145) == 2 and gh(d=0) == 2 and gh(d=96) == 2 and gh(d=65600) == 2
+    assert gh(ht=A + 8) == 6 and gh(w=A + 4) == 6 and gh(dt=A + 2) == 6 and gh(on=A + 1) == 6
+    assert gh(ws=A + 8) == 4 and gh(wsb=wsb - 1) == 4
 
 
 def test_launch_cache_is_per_device_and_thread_safe():
