@@ -5,15 +5,19 @@
 // output projection that ends a decode step ("Apple Silikon İçin Cihaz Üstü
 // Çıkarımı Optimize Etme", perplexity.coolkeypoint.com, decode section).
 //
-// One CTA per 128 x 256 output tile. Both operands are K-major and staged by TMA
-// (128-byte swizzle, one 64-element K slice per stage) into a 4-stage ring; one
-// thread issues tcgen05.mma (M = 128, N = 256, K = 16) into a 256-column TMEM
-// accumulator; the four warps read it back with tcgen05.ld (warp w owns TMEM lanes
-// 32w..32w+31, i.e. those output rows) and either store fp32 rows or, for the
-// greedy verify step, reduce them to each row's maximum and the lowest column
-// holding it, so that the logits never reach memory. Every wait is bounded: a
-// timeout sets the caller's flag, the CTA lets its issued copies land and frees
-// its TMEM before it returns.
+// A persistent grid (one CTA per SM) walks the 128 x 256 output tiles, the
+// column-tile index outer, so the CTAs at work at any time share few W tiles and
+// W is read from HBM about once. Warp roles: warp 0 issues the TMA loads of both
+// K-major operands (128-byte swizzle, one 64-element K slice per stage) into a
+// 4-stage ring, running ahead across tiles; warp 1 allocates two 256-column fp32
+// TMEM accumulators and one of its threads issues tcgen05.mma (M = 128, N = 256,
+// K = 16) into them in turn; warps 2-5 read a finished accumulator back with
+// tcgen05.ld (each warp its quarter of the TMEM lanes, i.e. 32 output rows) while
+// the next tile is being multiplied into the other one, and either store fp32
+// rows or, for the greedy verify step, reduce them to each row's maximum and the
+// lowest column holding it, so that the logits never reach memory. Every wait is
+// bounded: a timeout sets the caller's flag, the CTA lets its issued copies and
+// MMAs land and frees its TMEM before it returns.
 //
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -28,11 +32,15 @@ namespace svlm {
 constexpr int BM = 128, BN = 256, BK = 64;   // BK bf16 = 128 bytes: one swizzle row
 constexpr int NS = 4;                          // pipeline stages
 constexpr int STAGE_A = BM * BK * 2, STAGE_B = BN * BK * 2;   // 16 KB and 32 KB
-constexpr int TMEM_COLS = BN;                  // fp32 accumulator, 128 lanes x 256 columns
+constexpr int TMEM_COLS = 2 * BN;              // two fp32 accumulators, 128 lanes x 256 columns each
+constexpr int NEPI = 4;                        // epilogue warps (one TMEM lane quarter each)
+constexpr int NTHREADS = 64 + 32 * NEPI;       // TMA warp, MMA warp, epilogue warps
 constexpr uint64_t WAIT_NS = 200ull * 1000 * 1000;
 
 struct __align__(8) Ctl {
-  unsigned long long full[NS], empty[NS], done;
+  unsigned long long full[NS], empty[NS];      // stage loaded / stage consumed by the MMAs
+  unsigned long long acc_full[2], acc_empty[2];   // accumulator finished / read back
+  unsigned long long done;                     // every MMA of the CTA finished
   uint32_t taddr;
   int err;
 };
@@ -61,6 +69,9 @@ __device__ __forceinline__ bool bar_try(unsigned long long* b, uint32_t parity) 
       : "r"(sa(b)), "r"(parity)
       : "memory");
   return ok != 0;
+}
+__device__ __forceinline__ void bar_arrive(unsigned long long* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
 }
 // Waits for phase `parity` of b for at most WAIT_NS; false on timeout.
 __device__ __forceinline__ bool bar_wait(unsigned long long* b, uint32_t parity) {
@@ -126,7 +137,7 @@ constexpr uint32_t KEY_NEG_INF = 0x007FFFFFu;   // order_key(-inf)
 constexpr uint32_t KEY_POS_INF = 0xFF800000u;   // order_key(+inf)
 
 template <int EPI>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapW,
                    float* __restrict__ Z, unsigned long long* __restrict__ keys, int M, int N, int d,
                    int32_t* flag) {
@@ -136,10 +147,10 @@ __global__ void __launch_bounds__(128, 1)
   unsigned char* sA = smem;
   unsigned char* sB = smem + NS * STAGE_A;
   Ctl& C = *reinterpret_cast<Ctl*>(smem + NS * (STAGE_A + STAGE_B));
+  volatile int* err = &C.err;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // consecutive CTAs take the M tiles of one N tile, so a W tile is read from HBM
-  // once and served to the other M tiles from L2
-  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  const int mt = (M + BM - 1) / BM;
+  const long long ntiles = (long long)mt * ((N + BN - 1) / BN);
   const int nk = d / BK;
 
   if (tid == 0) {
@@ -147,11 +158,15 @@ __global__ void __launch_bounds__(128, 1)
       bar_init(&C.full[s], 1);
       bar_init(&C.empty[s], 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      bar_init(&C.acc_full[b], 1);
+      bar_init(&C.acc_empty[b], 32 * NEPI);
+    }
     bar_init(&C.done, 1);
     C.err = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 2) {   // the whole warp allocates (and later frees) the accumulator
+  if (warp == 1) {   // the whole warp allocates (and later frees) the accumulators
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sa(&C.taddr)),
                  "r"(TMEM_COLS)
                  : "memory");
@@ -162,101 +177,143 @@ __global__ void __launch_bounds__(128, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t taddr = C.taddr;
 
-  int issued = 0;   // K slices the producer has loaded
-  if (warp == 0 && lane == 0) {
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % NS;
-      // reuse of stage s waits for the MMAs of its previous slice
-      if (kb >= NS && !bar_wait(&C.empty[s], (uint32_t)((kb / NS - 1) & 1))) {
-        atomicExch(&C.err, 1);
-        break;
+  // K slices loaded and consumed are counted over all tiles of the CTA: slice
+  // number `it` uses stage it % NS in its (it / NS)-th round
+  long long issued = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      long long it = 0;
+      for (long long t = blockIdx.x; t < ntiles && !*err; t += gridDim.x) {
+        const int m0 = (int)(t % mt) * BM, n0 = (int)(t / mt) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = (int)(it % NS);
+          // reuse of stage s waits for the MMAs of its previous slice
+          if (it >= NS && !bar_wait(&C.empty[s], (uint32_t)((it / NS - 1) & 1))) {
+            atomicExch(&C.err, 1);
+            break;
+          }
+          if (*err) break;
+          bar_expect(&C.full[s], STAGE_A + STAGE_B);
+          tma_load(sA + s * STAGE_A, &mapH, kb * BK, m0, &C.full[s]);
+          tma_load(sB + s * STAGE_B, &mapW, kb * BK, n0, &C.full[s]);
+          issued = it + 1;
+        }
       }
-      if (*reinterpret_cast<volatile int*>(&C.err)) break;
-      bar_expect(&C.full[s], STAGE_A + STAGE_B);
-      tma_load(sA + s * STAGE_A, &mapH, kb * BK, m0, &C.full[s]);
-      tma_load(sB + s * STAGE_B, &mapW, kb * BK, n0, &C.full[s]);
-      issued = kb + 1;
     }
-  } else if (warp == 1 && lane == 0) {
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % NS;
-      if (!bar_wait(&C.full[s], (uint32_t)((kb / NS) & 1))) {
-        atomicExch(&C.err, 1);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      long long it = 0;
+      int j = 0;   // tiles of this CTA so far; tile j accumulates into buffer j & 1
+      for (long long t = blockIdx.x; t < ntiles && !*err; t += gridDim.x, ++j) {
+        const int buf = j & 1;
+        // the epilogue has read this buffer's previous tile
+        if (j >= 2 && !bar_wait(&C.acc_empty[buf], (uint32_t)((j / 2 - 1) & 1))) {
+          atomicExch(&C.err, 1);
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t tacc = taddr + (uint32_t)(buf * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = (int)(it % NS);
+          if (!bar_wait(&C.full[s], (uint32_t)((it / NS) & 1))) {
+            atomicExch(&C.err, 1);
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t a0 = sa(sA + s * STAGE_A), b0 = sa(sB + s * STAGE_B);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)   // 16 bf16 = 32 bytes along K per instruction
+            mma(tacc, sdesc(a0 + k * 32), sdesc(b0 + k * 32), (kb | k) != 0);
+          commit(&C.empty[s]);
+        }
+        if (!ok) break;
+        commit(&C.acc_full[buf]);
+      }
+      commit(&C.done);
+    }
+  } else {
+    // epilogue: warp w may read TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31
+    const int q = warp & 3;
+    int j = 0;
+    for (long long t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
+      const int buf = j & 1;
+      const bool got = bar_wait(&C.acc_full[buf], (uint32_t)((j / 2) & 1)) && !*err;
+      // tcgen05.ld is warp-collective: the whole warp takes the same branch
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) atomicExch(&C.err, 1);
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a0 = sa(sA + s * STAGE_A), b0 = sa(sB + s * STAGE_B);
-#pragma unroll
-      for (int k = 0; k < BK / 16; ++k)   // 16 bf16 = 32 bytes along K per instruction
-        mma(taddr, sdesc(a0 + k * 32), sdesc(b0 + k * 32), (kb | k) != 0);
-      commit(&C.empty[s]);
-    }
-    commit(&C.done);
-  }
-  __syncwarp();
-
-  // tcgen05.ld is warp-collective: every thread of the block takes the same branch
-  const bool ok = __syncthreads_and(bar_wait(&C.done, 0u) && !*reinterpret_cast<volatile int*>(&C.err)) != 0;
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  if (ok) {
-    const int row = m0 + warp * 32 + lane;
-    uint32_t bkey = 0u, bcol = 0u;   // EPI_ARGMAX: the thread's best order key and its column
+      const int m0 = (int)(t % mt) * BM, n0 = (int)(t / mt) * BN;
+      const int row = m0 + q * 32 + lane;
+      uint32_t bkey = 0u, bcol = 0u;   // EPI_ARGMAX: the thread's best order key and its column
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      const uint32_t ta = taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32);
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-          "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
-          "[%32];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-            "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-            "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-            "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-          : "r"(ta));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const int col = n0 + c * 32;
-      if (EPI == EPI_ARGMAX) {
-        // ascending columns and a strict comparison: the first maximum is kept
-        const int lim = min(32, N - col);
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        const uint32_t ta = taddr + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c * 32);
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+            "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+            "[%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+            : "r"(ta));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int col = n0 + c * 32;
+        if (EPI == EPI_ARGMAX) {
+          // ascending columns and a strict comparison: the first maximum is kept
+          const int lim = min(32, N - col);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t key = order_key(r[j]);
-          if (j < lim && key > bkey) {
-            bkey = key;
-            bcol = (uint32_t)(col + j);
+          for (int jj = 0; jj < 32; ++jj) {
+            const uint32_t key = order_key(r[jj]);
+            if (jj < lim && key > bkey) {
+              bkey = key;
+              bcol = (uint32_t)(col + jj);
+            }
+          }
+        } else if (row < M && col < N) {
+          float* zr = Z + (size_t)row * N + col;
+          const int lim = min(32, N - col);
+          if (lim == 32 && (reinterpret_cast<uintptr_t>(zr) & 15) == 0) {
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4)
+              *reinterpret_cast<float4*>(zr + jj) = make_float4(
+                  __uint_as_float(r[jj]), __uint_as_float(r[jj + 1]), __uint_as_float(r[jj + 2]),
+                  __uint_as_float(r[jj + 3]));
+          } else {
+            for (int jj = 0; jj < lim; ++jj) zr[jj] = __uint_as_float(r[jj]);
           }
         }
-      } else if (row < M && col < N) {
-        float* zr = Z + (size_t)row * N + col;
-        const int lim = min(32, N - col);
-        if (lim == 32 && (reinterpret_cast<uintptr_t>(zr) & 15) == 0) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(zr + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                             __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-        } else {
-          for (int j = 0; j < lim; ++j) zr[j] = __uint_as_float(r[j]);
-        }
       }
+      // the buffer may take the next tile once every epilogue thread has read it
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      bar_arrive(&C.acc_empty[buf]);
+      if (EPI == EPI_ARGMAX && row < M && bkey != 0u)
+        atomicMax(keys + row, ((unsigned long long)bkey << 32) | (unsigned long long)(~bcol));
     }
-    if (EPI == EPI_ARGMAX && row < M && bkey != 0u)
-      atomicMax(keys + row, ((unsigned long long)bkey << 32) | (unsigned long long)(~bcol));
   }
-  // after a timeout, the copies issued but never consumed land before the CTA leaves
-  if (warp == 0 && lane == 0 && C.err) {
-    for (int kb = issued > NS ? issued - NS : 0; kb < issued; ++kb)
-      bar_wait(&C.full[kb % NS], (uint32_t)((kb / NS) & 1));
+  __syncwarp();
+  __syncthreads();
+  // before TMEM is freed: every MMA issued has finished (the MMA thread's last
+  // commit) and, after a timeout, the copies issued but never consumed have landed
+  if (tid == 0) bar_wait(&C.done, 0u);
+  if (warp == 0 && lane == 0 && *err) {
+    for (long long it = issued > NS ? issued - NS : 0; it < issued; ++it)
+      bar_wait(&C.full[it % NS], (uint32_t)((it / NS) & 1));
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TMEM_COLS)
                  : "memory");
   }
-  if (tid == 0 && !ok) atomicExch(flag, 1);
+  if (tid == 0 && *err) atomicExch(flag, 1);
 }
 
 // Greedy acceptance of sequence b from its K+1 row keys (one thread per
@@ -344,8 +401,12 @@ static sv_status launch_gemm(const void* hidden, const void* weight, int M, int 
                                     SMEM_BYTES);
       }) != cudaSuccess)
     return SV_ERR_CUDA;
-  const dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((N + BN - 1) / BN));
-  lm_head_kernel<EPI><<<grid, 128, SMEM_BYTES, stream>>>(mh, mw, logits, keys, M, N, d, flag);
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return SV_ERR_CUDA;
+  const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+  lm_head_kernel<EPI><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mh, mw, logits, keys, M, N, d, flag);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
