@@ -130,3 +130,22 @@ def test_launch_cache_is_per_device_and_thread_safe():
     assert list(out[:4]) == [152 * 2, 132 * 2, 152 * 2 + 1, 132 * 2 + 1]
     assert out[4] == 4            # one entry per (device, kernel)
     assert out[5] == 1            # every thread saw the same values
+
+
+def test_binding_rejects_bad_tensors_before_calling_the_library():
+    # argument marshalling only: shape and device errors surface as SpecVerifyError
+    # before anything reaches the C ABI (no GPU needed)
+    import torch
+    h = torch.zeros(2, 3, 64, dtype=torch.bfloat16)
+    W = torch.zeros(100, 128, dtype=torch.bfloat16)
+    dt = torch.zeros(2, 2, dtype=torch.int32)
+    with pytest.raises(sv.SpecVerifyError, match="weight must be"):
+        sv.spec_verify_greedy_from_hidden(h, W, dt)
+    with pytest.raises(sv.SpecVerifyError, match="weight must be"):
+        sv.spec_lm_head_logits(h, W)
+    W64 = torch.zeros(100, 64, dtype=torch.bfloat16)
+    flag = torch.zeros(1, dtype=torch.int32)
+    out, n = torch.zeros(2, 3, dtype=torch.int32), torch.zeros(2, dtype=torch.int32)
+    ws = type("W", (), {"buf": torch.zeros(16, dtype=torch.uint8), "nbytes": 16})()
+    with pytest.raises(sv.SpecVerifyError, match="CUDA tensor"):
+        sv.spec_verify_greedy_from_hidden(h, W64, dt, flag=flag, out_tokens=out, out_n=n, workspace=ws)
