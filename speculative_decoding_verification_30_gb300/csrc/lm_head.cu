@@ -44,7 +44,9 @@ struct __align__(8) Ctl {
   uint32_t taddr;
   int err;
 };
-constexpr int SMEM_BYTES = 1024 /* alignment slack */ + NS * (STAGE_A + STAGE_B) + (int)sizeof(Ctl);
+constexpr int CTL_BYTES = ((int)sizeof(Ctl) + 15) & ~15;
+constexpr int STG_BYTES = NEPI * 32 * 33 * 4;   // EPI_STORE: one 32 x 32 transpose block per epilogue warp
+constexpr int SMEM_BYTES = 1024 /* alignment slack */ + NS * (STAGE_A + STAGE_B) + CTL_BYTES + STG_BYTES;
 
 __device__ __forceinline__ uint32_t sa(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   unsigned char* sA = smem;
   unsigned char* sB = smem + NS * STAGE_A;
   Ctl& C = *reinterpret_cast<Ctl*>(smem + NS * (STAGE_A + STAGE_B));
+  float* stg = reinterpret_cast<float*>(smem + NS * (STAGE_A + STAGE_B) + CTL_BYTES);
   volatile int* err = &C.err;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = (M + BM - 1) / BM;
@@ -276,18 +279,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               bcol = (uint32_t)(col + jj);
             }
           }
-        } else if (row < M && col < N) {
-          float* zr = Z + (size_t)row * N + col;
-          const int lim = min(32, N - col);
-          if (lim == 32 && (reinterpret_cast<uintptr_t>(zr) & 15) == 0) {
+        } else if (col < N) {
+          // a lane holds one row's 32 columns; through the warp's block of shared
+          // memory (row stride 33: no bank conflicts either way) each store
+          // instruction writes 32 consecutive columns of one row instead
+          float* st = stg + q * (32 * 33);
 #pragma unroll
-            for (int jj = 0; jj < 32; jj += 4)
-              *reinterpret_cast<float4*>(zr + jj) = make_float4(
-                  __uint_as_float(r[jj]), __uint_as_float(r[jj + 1]), __uint_as_float(r[jj + 2]),
-                  __uint_as_float(r[jj + 3]));
-          } else {
-            for (int jj = 0; jj < lim; ++jj) zr[jj] = __uint_as_float(r[jj]);
-          }
+          for (int jj = 0; jj < 32; ++jj) st[lane * 33 + jj] = __uint_as_float(r[jj]);
+          __syncwarp();
+          const int cl = col + lane;
+          const int rb = m0 + q * 32, nr = min(32, M - rb);
+          for (int i = 0; i < nr; ++i)
+            if (cl < N) Z[(size_t)(rb + i) * N + cl] = st[i * 33 + lane];
+          __syncwarp();
         }
       }
       // the buffer may take the next tile once every epilogue thread has read it
