@@ -145,3 +145,20 @@ def test_error_bound_is_nearly_attained():
     err = z - float(acc)
     bound = lm_head.logit_error_bound(h, W)[0]
     assert 0.9 * bound <= err <= bound
+
+
+def test_greedy_from_hidden_ties_take_the_lowest_id():
+    # W[v] = e_(v mod 4): logits z_v = h[v mod 4] repeat with period 4, so every
+    # maximum appears twice; the greedy step must take the lower id (closed form)
+    V, d, K = 8, 4, 2
+    W = np.zeros((V, d))
+    W[np.arange(V), np.arange(V) % d] = 1.0
+    ht = np.array([[[1.0, 5.0, 2.0, 0.0],      # max 5 at ids 1 and 5
+                    [3.0, 0.0, 3.0, 1.0],      # max 3 at ids 0, 2, 4 and 6
+                    [0.0, 0.0, 0.0, 4.0]]])    # max 4 at ids 3 and 7
+    zeros, ones = np.zeros(1), np.ones(1)
+    for dtok, tokens, n in (([1, 0], [1, 0, 3], 2),     # both drafts are the lowest maxima
+                            ([5, 0], [1, -1, -1], 0),   # an equal maximum with a higher id is rejected
+                            ([1, 2], [1, 0, -1], 1)):
+        r = lm_head.verify_from_hidden(ht, W, None, np.array([dtok]), zeros, np.zeros(1, int), ones, 0, 0)[0]
+        assert r.n_accepted == n and list(r.tokens) == tokens, (dtok, r.tokens)
