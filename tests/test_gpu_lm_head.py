@@ -190,3 +190,21 @@ def test_greedy_from_hidden_full_vocabulary_and_unfused_path():
     o, nn = out.cpu().numpy(), n.cpu().numpy()
     unclear = _check_greedy(o, nn, dt.numpy(), seqs, zt, bound)
     assert unclear <= 4, unclear
+
+
+def test_greedy_from_hidden_exact_ties_take_the_lowest_id():
+    # W[v] = e_(v mod 4) with d = 64: the logits are exact integers repeating with
+    # period 4 across three 256-column tiles, so each row's maximum appears about 150
+    # times; the merged key must name the lowest id (the oracle's closed form)
+    B, K, V, d = 3, 2, 600, 64
+    W = torch.zeros(V, d)
+    W[torch.arange(V), torch.arange(V) % 4] = 1.0
+    h = torch.zeros(B, K + 1, d)
+    h[:, :, :4] = torch.tensor([[1.0, 5.0, 2.0, 0.0], [3.0, 0.0, 3.0, 1.0], [0.0, 0.0, 0.0, 4.0]])
+    dtok = torch.tensor([[1, 0], [5, 0], [1, 2]], dtype=torch.int32)
+    out, n, flag = sv.spec_verify_greedy_from_hidden(h.to(torch.bfloat16).to(DEV), W.to(torch.bfloat16).to(DEV),
+                                                     dtok.to(DEV))
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    assert out.cpu().tolist() == [[1, 0, 3], [1, -1, -1], [1, 0, -1]]
+    assert n.cpu().tolist() == [2, 0, 1]
